@@ -1,0 +1,442 @@
+"""Benchmark: paged decode attention KV GB/s and sequences/s on one GB300.
+
+One step = one decode step of one attention layer for the whole batch:
+pkv_append of every sequence's new token (K/V scatter) followed by
+pkv_decode_attention (split-KV decode + LSE combine), all through the C ABI.
+
+Default workload: the 70B-class GQA decode batch (B=64, H_q=64, H_kv=8,
+d_head=128, 16-token blocks, context ~ U[512, 8192], bf16 KV; about 1.14 GB of
+K/V read per step, far larger than the 129 MB L2, so no flush is needed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--split-tokens T]
+
+Prints one JSON line.  value = KV bytes attended per step * steps / time
+(GB/s, 1e9 bytes), whole job over all ranks.  With --gpus N > 1 (torchrun)
+each rank runs an independent replica on its own GPU (the path has no
+exchange step); value sums the ranks' bytes over the slowest rank's time.
+
+--impl reference times the float64 CPU oracle (the reference of this
+library) on the host cores over a bounded sample of the same workload.
+"""
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s & seqs/s at 1 GB300; fraction of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_bf16")
+    ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- oracle leg
+
+def _oracle_unit_worker(args):
+    """Oracle decode of one (sequence, KV head) unit on its own blocks."""
+    import numpy as np
+    from oracle import paged_attention as PA
+    q_bits, k_blocks, v_blocks, ctx, bs, scale = args
+    n = k_blocks.shape[0]
+    table = np.arange(n, dtype=np.int32)[None, :]
+    t0 = time.perf_counter()
+    out = PA.decode_attention(q_bits[None], k_blocks, v_blocks, PA.BF16, table, np.array([ctx]), scale)
+    return time.perf_counter() - t0, out.shape
+
+
+def _unit_payload(case, b, h, ctx_attended):
+    import torch
+    from tests.gpu_support import bits16
+    G = case["H_q"] // case["H_kv"]
+    n = -(-ctx_attended // case["bs"])
+    ids = case["block_tables"][b, :n].to(torch.int64).to(case["k_cache"].device)
+    kb = bits16(case["k_cache"][ids][:, h:h + 1])
+    vb = bits16(case["v_cache"][ids][:, h:h + 1])
+    q = bits16(case["q"][0, b, h * G:(h + 1) * G])
+    return (q, kb, vb, ctx_attended, case["bs"], case["scale"])
+
+
+def oracle_throughput(case, seconds, order_seed=0):
+    """Run the oracle over (sequence, KV head) units in a spawn process pool,
+    one single-threaded process per host core, until `seconds` of wall time
+    are used.  Returns (GB/s of KV attended, units done, processes)."""
+    import multiprocessing as mp
+    import numpy as np
+    cores = len(os.sched_getaffinity(0))
+    procs = max(1, min(cores, 32))
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    rng = np.random.default_rng(order_seed)
+    units = [(b, h) for b in range(case["B"]) for h in range(case["H_kv"])]
+    rng.shuffle(units)
+    ctx = (case["ctx"] + 1).tolist()
+    per_unit_bytes = lambda b: ctx[b] * case["D"] * 2 * 2
+    ctxm = mp.get_context("spawn")
+    done_bytes = 0
+    done = 0
+    with ctxm.Pool(procs) as pool:
+        # warm the workers (imports) before timing
+        pool.map(_noop, range(procs))
+        t0 = time.perf_counter()
+        i = 0
+        while i < len(units) and time.perf_counter() - t0 < seconds:
+            batch = units[i:i + procs]
+            payloads = [_unit_payload(case, b, h, ctx[b]) for b, h in batch]
+            pool.map(_oracle_unit_worker, payloads)
+            done_bytes += sum(per_unit_bytes(b) for b, _ in batch)
+            done += len(batch)
+            i += procs
+        wall = time.perf_counter() - t0
+    return done_bytes / wall / 1e9, done, procs, wall
+
+
+def _noop(_):
+    import numpy  # noqa: F401
+    from oracle import paged_attention  # noqa: F401
+    return 0
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self, t_begin, t_end):
+        rows = []
+        try:
+            with open(self.file.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    rows.append((ts, parts))
+        finally:
+            os.unlink(self.file.name)
+        inside = [p for ts, p in rows if t_begin - 0.05 <= ts <= t_end + 0.05]
+        use = inside if inside else [p for _, p in rows]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for p in use if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in use for n, v in zip(names, p[6:10]) if v.lower() == "active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+               "samples": len(use), "samples_in_timed_region": len(inside)}
+        pw = [float(p[4]) for p in use if p[4].replace(".", "").isdigit()]
+        if pw:
+            out["power_w_max"] = max(pw)
+        return out
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "pkv_device.cuh", "pkv_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_222_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, split_tokens):
+    """DRAM bytes per launch of the split kernel from a committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    for r in rec.get("records", []):
+        if r.get("workload") == workload and r.get("kernel_src") == kernel_source_hash():
+            return r.get("dram_bytes_per_launch_full")
+    return None
+
+
+def workload_config(case, args, kv_bytes, plan):
+    ctx = case["ctx"]
+    cfg = {"workload": args.workload, "B": case["B"], "H_q": case["H_q"], "H_kv": case["H_kv"],
+           "d_head": case["D"], "block_size": case["bs"], "kv_dtype": case["kv"],
+           "context_attended": f"{int(ctx.min()) + 1}..{int(ctx.max()) + 1} (mean {float(ctx.float().mean()) + 1:.0f})",
+           "kv_bytes_per_step": kv_bytes, "split_tokens": plan.split_tokens, "max_splits": plan.max_splits,
+           "l2": "inputs larger than L2 (no flush)" if kv_bytes > 129e6 else "L2 flushed between steps",
+           "parallelism": "replicas"}
+    return cfg
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample of
+    the workload's (sequence, KV head) units."""
+    if rank != 0:
+        return
+    import workloads as W
+    case = W.make_case(args.workload, device="cpu")
+    per_step = max(2.0, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    cores = None
+    units = 0
+    for s in range(args.warmup + args.steps):
+        gbs, n, procs, wall = oracle_throughput(case, per_step, order_seed=s)
+        cores = procs
+        if s >= args.warmup:
+            vals.append(gbs)
+            units += n
+    value = statistics.median(vals) if vals else 0.0
+    kv_bytes = int(((case["ctx"] + 1).to(float) * case["H_kv"] * case["D"] * 4).sum())
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": kv_bytes / (value * 1e9) * 1e3 if value else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": case["B"], "H_q": case["H_q"], "H_kv": case["H_kv"],
+                       "d_head": case["D"], "block_size": case["bs"], "kv_bytes_per_step": kv_bytes},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{units} (sequence, KV head) units over {args.steps} steps of "
+                                       f"~{per_step:.0f} s each; float64 numpy oracle, one process per core"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_222_gb300 as pkv
+    import workloads as W
+    from paged_kv_cache_222_gb300 import build
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    seed_shift = 1000 * rank
+    spec = W.spec(args.workload)
+    spec["seed"] = spec["seed"] + seed_shift
+    case = W.make_case(spec, device=dev)
+    B, bs = case["B"], case["bs"]
+    fp8 = case["kv"] == "e4m3"
+    if fp8:
+        from tests.gpu_support import fill_fp8_cache
+        fill_fp8_cache(case)
+    bt = case["block_tables"].to(dev)
+    ctx = case["ctx"].to(dev)
+    lens = (ctx + 1).to(torch.int32)
+    max_len = int(case["ctx"].max()) + 1
+    slots = pkv.slots_for_positions(bt, torch.arange(B, device=dev), ctx.to(torch.int64), bs)
+    q = case["q"][0].contiguous()
+    kn = case["k_new"][0].contiguous()
+    vn = case["v_new"][0].contiguous()
+    ks = case.get("k_scale") if fp8 else None
+    vs = case.get("v_scale") if fp8 else None
+    out = torch.empty((B, case["H_q"], case["D"]), dtype=torch.float32, device=dev)
+    plan = pkv.decode_plan(B, case["H_q"], case["k_cache"], max_len, args.split_tokens)
+    ws = torch.empty(max(1, int(plan.workspace_bytes)), dtype=torch.uint8, device=dev)
+    esz = 1 if fp8 else 2
+    kv_bytes = int(((case["ctx"] + 1).to(torch.float64) * case["H_kv"] * case["D"] * 2 * esz).sum())
+
+    def step():
+        pkv.append(kn, vn, slots, case["k_cache"], case["v_cache"], ks, vs)
+        pkv.decode_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"], ks, vs,
+                             max_context_len=max_len, out=out, split_tokens=args.split_tokens,
+                             workspace=ws)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if pkv.device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    pkv.trace_read()
+    pkv.trace_enable(True)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    pkv.trace_enable(False)
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    trace = pkv.trace_read()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = kv_bytes * args.steps * world / (ms_max / 1e3) / 1e9
+    seqs = B * args.steps * world / (ms_max / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_kn, h_vn = pin(q), pin(kn), pin(vn)
+    h_slots, h_bt, h_lens = pin(slots), pin(bt), pin(lens)
+    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    d_slots, d_bt, d_lens = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_bt, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(3, min(args.steps, 500))
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_slots, h_slots), (d_bt, h_bt),
+                     (d_lens, h_lens)):
+            d.copy_(h, non_blocking=True)
+        pkv.append(d_kn, d_vn, d_slots, case["k_cache"], case["v_cache"], ks, vs)
+        pkv.decode_attention(d_q, case["k_cache"], case["v_cache"], d_bt, d_lens, case["scale"], ks, vs,
+                             max_context_len=max_len, out=out, split_tokens=args.split_tokens,
+                             workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = kv_bytes * e2e_steps * world / (float(e2e_t.item()) / 1e3) / 1e9
+    if pkv.device_error(dev) != 0:
+        raise RuntimeError("device error during the timed region")
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    split = trace.get("decode_split", (0, 0.0))
+    avg_ms = split[1] / split[0] if split[0] else float("nan")
+    achieved = kv_bytes / (avg_ms / 1e3) / 1e9 if split[0] else None
+    launches = sum(n for n, _ in trace.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not fp8 else "e4m3",
+        "data": "synthetic",
+        "config": workload_config(case, args, kv_bytes, plan),
+        "seqs_per_s": seqs,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None,
+                     "peak_source": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+                     "kernel": "decode_split", "algorithmic_bytes_per_launch": kv_bytes,
+                     "avg_launch_ms": avg_ms,
+                     "traffic": recorded_traffic(args.workload, args.split_tokens)},
+        "kernel_times_ms": {k: {"launches": n, "avg_ms": t / n} for k, (n, t) in trace.items()},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        gbs, n, procs, wall = oracle_throughput(case, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle",
+                                "sample": f"{n} of {B * case['H_kv']} (sequence, KV head) units of the "
+                                          f"{args.workload} step, {wall:.1f} s wall, float64 numpy, "
+                                          f"one process per core"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,236 @@
+/*
+ * pkv.h — C ABI of the GB300 (sm_103a) paged-KV decode-attention library.
+ *
+ * Two calls make up one decode step of one attention layer:
+ *
+ *   pkv_append            write each new token's K/V rows into their cache slots
+ *                         (bf16 copy, or FP8 E4M3 quantisation with scales);
+ *   pkv_decode_attention  single-token attention of every sequence over its
+ *                         paged K/V (GQA, split-KV flash-decoding + LSE combine).
+ *
+ * Sources for what is computed (web pages, cited by title and section):
+ *   [FN] FactNode, "Sub-Millisecond Token Scheduling: Inside Disaggregated
+ *        KV-Cache Paging for Frontier LLMs".
+ *   [SC] systemcraft.online lesson "LLM inference: prefill, decode, KV cache".
+ *   [UI] ultrainstinct.tech, "Architecting Multi-Tier Disaggregated KV-Cache
+ *        Hierarchies for Terabyte-Scale LLM Inference".
+ *
+ * Conventions for every call:
+ *   - Pointers named *_cache, q, out, k_new, v_new, slot_mapping, block_tables,
+ *     context_lens, k_scale, v_scale and workspace are DEVICE pointers owned by
+ *     the caller; the library never frees them and keeps no reference after the
+ *     call returns.  Descriptor structs are host memory, read during the call.
+ *   - Tensors are dense, row-major (last index fastest), with the shapes given.
+ *   - Work is enqueued on `stream` and the call returns without synchronising.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns PKV_ERR_INVALID_ARG (or PKV_ERR_UNSUPPORTED for a
+ *     shape this build has no kernel for) and enqueues nothing.  A CUDA
+ *     runtime failure returns PKV_ERR_CUDA.  pkv_last_error() gives a message.
+ *   - Values that only the device can see (block ids, slots, lengths) are
+ *     checked in the kernels: an out-of-range value is skipped (reads as zero,
+ *     writes are dropped) and its code is recorded in a per-device error word
+ *     read by pkv_get_device_error().  Kernels never trap.
+ *   - Thread safety: calls may come from several host threads; the library's
+ *     shared state (per-device workspace pool, trace buffer) is locked.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* a pointer, size, dtype or stride is not acceptable */
+  PKV_ERR_UNSUPPORTED = 2,  /* valid in principle, no kernel built for it          */
+  PKV_ERR_CUDA = 3,         /* the CUDA runtime reported an error                  */
+  PKV_ERR_WORKSPACE = 4     /* caller workspace smaller than required              */
+} pkv_status;
+
+typedef enum {
+  PKV_BF16 = 0,  /* bfloat16 (2 bytes)                                   */
+  PKV_F32 = 1,   /* IEEE binary32 (4 bytes); append sources only         */
+  PKV_E4M3 = 2   /* OCP FP8 E4M3 (1 byte), no infinities, max 448        */
+} pkv_dtype;
+
+/*
+ * One layer's paged cache.  K and V are separate tensors of identical shape
+ *   [num_blocks, num_kv_heads, block_size, head_dim]
+ * ([UI] "High-Throughput Paged Attention Kernel Integration": the decode
+ * kernel's K_Buffer / V_Buffer arguments).  Token t of a sequence whose block
+ * table row is tbl lives at cache[tbl[t / block_size], h, t % block_size, :]
+ * ([SC] "PagedAttention & Memory Management (vLLM)").
+ *   block_size    16 or 32 tokens ([FN] "Paged KV-Cache with Radix Tree
+ *                 Prefix Cache": fixed blocks of typically 16 or 32 tokens)
+ *   head_dim      64 or 128
+ *   num_kv_heads  >= 1
+ *   dtype         PKV_BF16 or PKV_E4M3
+ * Both cache pointers must be 16-byte aligned.
+ */
+typedef struct {
+  int64_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype;
+} pkv_cache_desc;
+
+/*
+ * pkv_append — KV append ([SC] "4. Internal workings", step 5 "Autoregressive
+ * Cache Append & Loopback": the new token's K/V vectors are appended to the
+ * cache before it attends; FP8 E4M3 with per-head scaling factors: [FN] FAQ
+ * "How much HBM memory does FP8 KV-cache quantization save?").
+ *
+ *   k_new, v_new   [n_tokens, num_kv_heads, head_dim] of src_dtype
+ *                  (PKV_BF16 or PKV_F32), 16-byte aligned.
+ *   slot_mapping   int64 [n_tokens]: row i goes to flat slot
+ *                  s = physical_block * block_size + offset; s < 0 skips the
+ *                  row (padding).  s >= num_blocks * block_size is recorded in
+ *                  the device error word and skipped.  Two rows with the same
+ *                  slot in one call: which one lands is unspecified.
+ *   k_cache, v_cache  written in place (only the addressed slots change).
+ *   k_scale, v_scale  E4M3 caches only (NULL otherwise): float32, row i and
+ *                  KV head h use element [i * scale_row_stride + h];
+ *                  scale_row_stride 0 gives one scale per KV head.  The code is
+ *                  RNE-satfinite(x / scale) with x / scale an IEEE binary32
+ *                  division.  bf16 caches: bf16 sources are copied bit for bit,
+ *                  f32 sources are rounded to nearest even.
+ *   n_tokens == 0 is a no-op.
+ */
+pkv_status pkv_append(const void* k_new, const void* v_new, int32_t src_dtype,
+                      int64_t n_tokens, const int64_t* slot_mapping,
+                      void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                      const float* k_scale, const float* v_scale,
+                      int64_t scale_row_stride, pkv_stream_t stream);
+
+/*
+ * pkv_decode_attention — single-token decode attention over a paged cache
+ * ([SC] "Why We Need the Key-Value (KV) Cache" and step 4 "Decode Phase";
+ * [UI] "High-Throughput Paged Attention Kernel Integration" for the argument
+ * list; softmax(q K^T * scale) V as in [UI] "Mathematical Formulation of Block
+ * Salience", definition of A).
+ *
+ *   q              bf16 [batch, num_q_heads, head_dim], 16-byte aligned.
+ *                  num_q_heads = G * num_kv_heads with 1 <= G <= 16; query
+ *                  head hq reads KV head hq / G ([SC] "Attention Architectures:
+ *                  MHA vs. MQA vs. GQA").
+ *   block_tables   int32 [batch, max_blocks_per_seq].  Entries at index
+ *                  >= ceil(context_lens[b] / block_size) are never read.
+ *   context_lens   int32 [batch]: tokens attended by sequence b, the token
+ *                  appended in this step included.  0 gives an all-zero row.
+ *                  A length above max_blocks_per_seq * block_size or above
+ *                  max_context_len is recorded in the error word and clamped.
+ *   max_context_len  host-side upper bound on context_lens (it sizes the
+ *                  split-KV grid without reading device memory).
+ *   scale          softmax scale (typically 1 / sqrt(head_dim)).
+ *   out            float32 [batch, num_q_heads, head_dim], 16-byte aligned.
+ *   k_scale, v_scale  E4M3 caches only (NULL otherwise): float32, sequence b
+ *                  and KV head h use [b * scale_row_stride + h]; stride 0 gives
+ *                  one scale per KV head.
+ *
+ * The split-KV partial results need scratch memory; this call takes it from a
+ * library-owned stream-ordered pool on the current device (released by
+ * pkv_shutdown).  pkv_decode_attention_ex takes caller memory instead.
+ */
+pkv_status pkv_decode_attention(const void* q, int32_t batch, int32_t num_q_heads,
+                                const void* k_cache, const void* v_cache,
+                                const pkv_cache_desc* cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t max_context_len,
+                                float scale, float* out,
+                                const float* k_scale, const float* v_scale,
+                                int64_t scale_row_stride, pkv_stream_t stream);
+
+/*
+ * Split-KV plan (host only, no CUDA call): how pkv_decode_attention_ex with
+ * `split_tokens` (0 = automatic) divides each sequence into chunks.
+ *   split_tokens  tokens per split (a multiple of 64)
+ *   max_splits    ceil(max_context_len / split_tokens)
+ *   workspace_bytes  scratch needed (0 when max_splits <= 1)
+ * `num_sms` is the GPU's SM count (152 on GB300); <= 0 means 152.
+ */
+typedef struct {
+  int32_t split_tokens;
+  int32_t max_splits;
+  int64_t workspace_bytes;
+} pkv_decode_plan_t;
+
+pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
+                           int32_t max_context_len, int32_t split_tokens, int32_t num_sms,
+                           pkv_decode_plan_t* plan);
+
+/*
+ * pkv_decode_attention_ex — as pkv_decode_attention, with caller scratch.
+ *   workspace        device memory of at least plan.workspace_bytes for the
+ *                    same (batch, num_q_heads, cache, max_context_len,
+ *                    split_tokens), 256-byte aligned; may be NULL when that is
+ *                    0.  Overlapping calls must not share a workspace.
+ *   split_tokens     0 = automatic, else tokens per split (multiple of 64).
+ */
+pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_heads,
+                                   const void* k_cache, const void* v_cache,
+                                   const pkv_cache_desc* cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t max_context_len,
+                                   float scale, float* out,
+                                   const float* k_scale, const float* v_scale,
+                                   int64_t scale_row_stride,
+                                   void* workspace, size_t workspace_bytes,
+                                   int32_t split_tokens, pkv_stream_t stream);
+
+/* Device error codes (first one recorded wins). */
+enum {
+  PKV_DEVERR_NONE = 0,
+  PKV_DEVERR_WAIT_TIMEOUT = 1,    /* a pipeline wait gave up (bounded spin)     */
+  PKV_DEVERR_BLOCK_ID = 2,        /* block table entry outside [0, num_blocks)  */
+  PKV_DEVERR_CONTEXT_LEN = 3,     /* context length beyond the table or bound   */
+  PKV_DEVERR_SLOT = 4             /* append slot beyond the cache               */
+};
+
+/*
+ * Reads and clears the current device's error word.  Synchronises `stream`
+ * first (the only call that waits for the GPU).  Returns the code, or -1 if
+ * the read itself failed.
+ */
+int32_t pkv_get_device_error(pkv_stream_t stream);
+
+/* Human-readable name of a status. */
+const char* pkv_status_string(int32_t status);
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char* pkv_last_error(void);
+
+/* ABI version of this library (major * 100 + minor). */
+int32_t pkv_abi_version(void);
+
+/*
+ * Kernel timing trace.  While enabled, every kernel the library launches is
+ * bracketed by CUDA events recorded on the stream it runs on.
+ * pkv_trace_read synchronises those events and returns, per kernel kind,
+ * the number of launches and their summed device time; it then clears the
+ * buffer.  Kinds: 0 append, 1 decode split, 2 combine.
+ */
+typedef struct {
+  int32_t kind;
+  int32_t launches;
+  double total_ms;
+} pkv_trace_entry;
+
+pkv_status pkv_trace_enable(int32_t on);
+int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity);
+
+/* Frees library-owned device memory (workspace pools, trace events). */
+pkv_status pkv_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

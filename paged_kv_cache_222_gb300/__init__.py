@@ -1,0 +1,231 @@
+"""GB300-native paged-KV decode attention: Python binding of libpkv.so.
+
+Every function here only checks tensor shapes / dtypes and hands raw device
+pointers plus the current CUDA stream to the C ABI (include/pkv.h); all of the
+computation runs in the library's sm_103a kernels.  PyTorch supplies device
+memory and streams.
+
+    append(k_new, v_new, slot_mapping, k_cache, v_cache[, k_scale, v_scale])
+    decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale
+                     [, k_scale, v_scale]) -> out (float32)
+
+Cache tensors are [num_blocks, H_kv, block_size, head_dim], bf16 or E4M3
+(torch.uint8 or torch.float8_e4m3fn storage).
+"""
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (PKV_BF16, PKV_E4M3, PKV_F32, CacheDesc, DecodePlan, PkvError,  # noqa: F401
+                   TraceEntry)
+
+__all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slots_for_positions",
+           "device_error", "trace_enable", "trace_read", "library", "PkvError"]
+
+KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine"}
+
+
+def library():
+    """The loaded ctypes library (raises if libpkv.so is not built)."""
+    return _lib.load()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _cache_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return PKV_E4M3
+    raise TypeError(f"cache dtype {t.dtype}: expected bfloat16 or uint8/float8_e4m3fn")
+
+
+def cache_desc(k_cache):
+    """C descriptor of a [num_blocks, H_kv, block_size, head_dim] cache tensor."""
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    nb, hkv, bs, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, _cache_dtype(k_cache))
+
+
+def _check_pair(k_cache, v_cache):
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    if k_cache.device != v_cache.device or k_cache.device.type != "cuda":
+        raise ValueError("caches must be CUDA tensors on one device")
+
+
+def _contig(t, dtype, name, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
+           scale_row_stride=None):
+    """Write rows k_new[i] / v_new[i] ([N, H_kv, D], bf16 or fp32) into flat slots
+    slot_mapping[i] (int64; phys * block_size + offset; < 0 skips).
+
+    E4M3 caches need k_scale / v_scale (float32): [N, H_kv] per-row scales, or
+    [H_kv] per-head scales (then scale_row_stride defaults to 0).
+    """
+    lib = library()
+    _check_pair(k_cache, v_cache)
+    dev = k_cache.device
+    desc = cache_desc(k_cache)
+    if k_new.shape != v_new.shape or k_new.dim() != 3:
+        raise ValueError("k_new / v_new must both be [N, H_kv, D]")
+    n, hkv, d = k_new.shape
+    if hkv != desc.num_kv_heads or d != desc.head_dim:
+        raise ValueError("k_new heads / head_dim do not match the cache")
+    if k_new.dtype == torch.bfloat16:
+        src = PKV_BF16
+    elif k_new.dtype == torch.float32:
+        src = PKV_F32
+    else:
+        raise TypeError(f"k_new dtype {k_new.dtype}: expected bfloat16 or float32")
+    _contig(k_new, k_new.dtype, "k_new", dev)
+    _contig(v_new, k_new.dtype, "v_new", dev)
+    _contig(slot_mapping, torch.int64, "slot_mapping", dev)
+    if slot_mapping.numel() != n:
+        raise ValueError("slot_mapping must have one entry per row")
+    if desc.dtype == PKV_E4M3:
+        if k_scale is None or v_scale is None:
+            raise ValueError("E4M3 cache needs k_scale and v_scale")
+        _contig(k_scale, torch.float32, "k_scale", dev)
+        _contig(v_scale, torch.float32, "v_scale", dev)
+        if scale_row_stride is None:
+            scale_row_stride = hkv if k_scale.dim() == 2 else 0
+    else:
+        scale_row_stride = 0
+    st = lib.pkv_append(_ptr(k_new), _ptr(v_new), src, n, _ptr(slot_mapping), _ptr(k_cache),
+                        _ptr(v_cache), ctypes.byref(desc), _ptr(k_scale), _ptr(v_scale),
+                        int(scale_row_stride), _stream(dev))
+    _lib.check(st, "pkv_append")
+
+
+def decode_plan(batch, num_q_heads, k_cache_or_desc, max_context_len, split_tokens=0, num_sms=0):
+    """Split-KV plan (host only): tokens per split, splits, workspace bytes."""
+    lib = library()
+    desc = k_cache_or_desc if isinstance(k_cache_or_desc, CacheDesc) else cache_desc(k_cache_or_desc)
+    plan = DecodePlan()
+    st = lib.pkv_decode_plan(int(batch), int(num_q_heads), ctypes.byref(desc), int(max_context_len),
+                             int(split_tokens), int(num_sms), ctypes.byref(plan))
+    _lib.check(st, "pkv_decode_plan")
+    return plan
+
+
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=None,
+                     v_scale=None, max_context_len=None, out=None, split_tokens=0,
+                     workspace=None, scale_row_stride=None):
+    """Single-token decode attention over the paged cache.
+
+    q [B, H_q, D] bf16; block_tables [B, MB] int32; context_lens [B] int32
+    (tokens attended, the appended one included); returns out [B, H_q, D]
+    float32.  `max_context_len` is a host bound on context_lens (if None it is
+    read from the device, which synchronises).  E4M3 caches take k_scale /
+    v_scale float32 [B, H_kv] (or [H_kv] for one scale per head).
+    """
+    lib = library()
+    _check_pair(k_cache, v_cache)
+    dev = k_cache.device
+    desc = cache_desc(k_cache)
+    _contig(q, torch.bfloat16, "q", dev)
+    if q.dim() != 3 or q.shape[2] != desc.head_dim:
+        raise ValueError("q must be [B, H_q, head_dim]")
+    b, hq, d = q.shape
+    _contig(block_tables, torch.int32, "block_tables", dev)
+    _contig(context_lens, torch.int32, "context_lens", dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if b > 0 else 0
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=torch.float32, device=dev)
+    else:
+        _contig(out, torch.float32, "out", dev)
+        if out.shape != (b, hq, d):
+            raise ValueError("out must be [B, H_q, D]")
+    stride = 0
+    if desc.dtype == PKV_E4M3:
+        if k_scale is None or v_scale is None:
+            raise ValueError("E4M3 cache needs k_scale and v_scale")
+        _contig(k_scale, torch.float32, "k_scale", dev)
+        _contig(v_scale, torch.float32, "v_scale", dev)
+        stride = scale_row_stride if scale_row_stride is not None else (
+            desc.num_kv_heads if k_scale.dim() == 2 else 0)
+    mb = block_tables.shape[1] if b > 0 else 1
+    plan = decode_plan(b, hq, desc, max_context_len, split_tokens)
+    ws_bytes = int(plan.workspace_bytes)
+    if ws_bytes > 0 and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    st = lib.pkv_decode_attention_ex(
+        _ptr(q), b, hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables), mb,
+        _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), _ptr(k_scale),
+        _ptr(v_scale), int(stride), _ptr(workspace) if ws_bytes > 0 else ctypes.c_void_p(0),
+        ws_bytes if ws_bytes > 0 else 0, int(split_tokens), _stream(dev))
+    _lib.check(st, "pkv_decode_attention_ex")
+    return out
+
+
+def decode_attention_pooled(q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                            out, k_scale=None, v_scale=None, scale_row_stride=None):
+    """The plain C entry point (library-owned scratch pool), same arguments."""
+    lib = library()
+    desc = cache_desc(k_cache)
+    b, hq, _ = q.shape
+    stride = 0
+    if desc.dtype == PKV_E4M3:
+        stride = scale_row_stride if scale_row_stride is not None else (
+            desc.num_kv_heads if k_scale.dim() == 2 else 0)
+    st = lib.pkv_decode_attention(
+        _ptr(q), b, hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        _ptr(k_scale), _ptr(v_scale), int(stride), _stream(k_cache.device))
+    _lib.check(st, "pkv_decode_attention")
+    return out
+
+
+def slots_for_positions(block_tables, seq_index, positions, block_size):
+    """Flat cache slots of logical token `positions` of sequences `seq_index`:
+    block_tables[s, p // block_size] * block_size + p % block_size (int64).
+    The block manager's addressing rule, computed with tensor ops on the
+    tables' device."""
+    seq_index = seq_index.to(block_tables.device, torch.int64)
+    positions = positions.to(block_tables.device, torch.int64)
+    phys = block_tables.to(torch.int64)[seq_index, positions // block_size]
+    return phys * block_size + positions % block_size
+
+
+def device_error(device=None):
+    """Read and clear the device error word (synchronises the current stream)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        return library().pkv_get_device_error(_stream(dev))
+
+
+def trace_enable(on=True):
+    _lib.check(library().pkv_trace_enable(1 if on else 0), "pkv_trace_enable")
+
+
+def trace_read():
+    """{kernel name: (launches, total_ms)} since the last read; clears the trace."""
+    buf = (TraceEntry * 8)()
+    n = library().pkv_trace_read(buf, 8)
+    if n < 0:
+        raise RuntimeError("pkv_trace_read failed")
+    return {KERNEL_KINDS[buf[i].kind]: (buf[i].launches, buf[i].total_ms) for i in range(n)}

@@ -1,0 +1,539 @@
+// C ABI of the paged-KV library: argument checks, split-KV planning, TMA
+// descriptors, scratch memory, launches, the device error word and the kernel
+// timing trace.  Every check that can be made on the host is made before any
+// CUDA runtime call, so a rejected call touches no GPU state.
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+using pkv::AppendParams;
+using pkv::DecodeParams;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultSms = 152;
+
+thread_local std::string t_last_error;
+
+pkv_status fail(pkv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ device state
+
+__device__ int g_device_error;  // one word per device: first bad value seen
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+pkv_status current_device(int* dev, DeviceState** st) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device index %d", *dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[*dev];
+  if (!s.ready) {
+    e = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, *dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    s.ready = true;
+  }
+  *st = &s;
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D view (d, token-in-block, kv-head, block) of one cache tensor; a box is
+// one 16-token tile of up to 128 bytes per row, swizzled for ldmatrix.
+pkv_status make_cache_tmap(CUtensorMap* tm, const void* base, const pkv_cache_desc& c) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const uint64_t esz = c.dtype == PKV_E4M3 ? 1 : 2;
+  const uint64_t row = static_cast<uint64_t>(c.head_dim) * esz;
+  const uint64_t boxb = row < 128 ? row : 128;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.head_dim), static_cast<cuuint64_t>(c.block_size),
+                        static_cast<cuuint64_t>(c.num_kv_heads),
+                        static_cast<cuuint64_t>(c.num_blocks)};
+  cuuint64_t strides[3] = {row, row * c.block_size, row * c.block_size * c.num_kv_heads};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(boxb / esz), static_cast<cuuint32_t>(pkv::kTileTokens),
+                       1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(tm, c.dtype == PKV_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  boxb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------ trace
+
+struct TraceRec {
+  int kind;
+  int dev;
+  cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<std::pair<int, cudaEvent_t>> g_event_pool;
+
+cudaEvent_t take_event(int dev) {
+  for (size_t i = 0; i < g_event_pool.size(); ++i) {
+    if (g_event_pool[i].first == dev) {
+      cudaEvent_t e = g_event_pool[i].second;
+      g_event_pool.erase(g_event_pool.begin() + i);
+      return e;
+    }
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+template <class F>
+cudaError_t traced(int kind, cudaStream_t stream, F&& launch) {
+  bool on;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    on = g_trace_on;
+  }
+  if (!on) return launch();
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaEvent_t a, b;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    a = take_event(dev);
+    b = take_event(dev);
+  }
+  if (a == nullptr || b == nullptr) return launch();
+  cudaEventRecord(a, stream);
+  cudaError_t e = launch();
+  cudaEventRecord(b, stream);
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.push_back({kind, dev, a, b});
+  return e;
+}
+
+// ------------------------------------------------------------ checks
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+  if (c == nullptr) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+  if (c->dtype != PKV_BF16 && c->dtype != PKV_E4M3)
+    return fail(PKV_ERR_INVALID_ARG, "cache dtype %d (want PKV_BF16 or PKV_E4M3)", c->dtype);
+  if (c->block_size != 16 && c->block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (16 or 32)", c->block_size);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", c->head_dim);
+  if (c->num_kv_heads < 1 || c->num_kv_heads > 65535)
+    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads %d", c->num_kv_heads);
+  if (c->num_blocks < 1 || c->num_blocks > 0x7FFFFFFFll)
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld", static_cast<long long>(c->num_blocks));
+  return PKV_OK;
+}
+
+int32_t auto_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int32_t sms) {
+  // Largest power-of-two chunk (256..4096 tokens) that still gives about eight
+  // waves of two CTAs per SM when every sequence is as long as the bound.
+  const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
+  const int64_t want = static_cast<int64_t>(sms) * 2 * 8;
+  int32_t st = 4096;
+  while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
+  return st;
+}
+
+pkv_status plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int32_t max_ctx,
+                int32_t split_tokens, int32_t sms, pkv_decode_plan_t* out) {
+  pkv_status s = check_cache(c);
+  if (s != PKV_OK) return s;
+  if (batch < 0 || batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch %d", batch);
+  if (num_q_heads < 1 || num_q_heads % c->num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                num_q_heads, c->num_kv_heads);
+  if (num_q_heads / c->num_kv_heads > 16)
+    return fail(PKV_ERR_UNSUPPORTED, "group size %d > 16", num_q_heads / c->num_kv_heads);
+  if (max_ctx < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d", max_ctx);
+  if (split_tokens < 0 || split_tokens % 64 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (0 or a multiple of 64)", split_tokens);
+  if (sms <= 0) sms = kDefaultSms;
+  const int32_t st = split_tokens ? split_tokens : auto_split_tokens(batch, c->num_kv_heads, max_ctx, sms);
+  const int64_t splits = max_ctx > 0 ? ceil_div(max_ctx, st) : 1;
+  if (splits > 0x7FFFFFFFll) return fail(PKV_ERR_INVALID_ARG, "too many splits");
+  out->split_tokens = st;
+  out->max_splits = static_cast<int32_t>(splits);
+  out->workspace_bytes = 0;
+  if (splits > 1) {
+    const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * splits;
+    const int64_t o_bytes = (rows * c->head_dim * 4 + 255) / 256 * 256;
+    out->workspace_bytes = o_bytes + rows * 2 * 4;
+  }
+  return PKV_OK;
+}
+
+struct DecodeArgs {
+  const void* q;
+  int32_t batch, num_q_heads;
+  const void* k_cache;
+  const void* v_cache;
+  const pkv_cache_desc* cache;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* context_lens;
+  int32_t max_ctx;
+  float scale;
+  float* out;
+  const float* k_scale;
+  const float* v_scale;
+  int64_t scale_stride;
+};
+
+pkv_status check_decode(const DecodeArgs& a) {
+  pkv_status s = check_cache(a.cache);
+  if (s != PKV_OK) return s;
+  const pkv_cache_desc& c = *a.cache;
+  if (a.batch < 0 || a.batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch %d", a.batch);
+  if (a.num_q_heads < 1 || a.num_q_heads % c.num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                a.num_q_heads, c.num_kv_heads);
+  if (a.num_q_heads / c.num_kv_heads > 16)
+    return fail(PKV_ERR_UNSUPPORTED, "group size %d > 16", a.num_q_heads / c.num_kv_heads);
+  if (!std::isfinite(a.scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (a.max_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", a.max_blocks);
+  if (a.max_ctx < 0 || static_cast<int64_t>(a.max_ctx) > static_cast<int64_t>(a.max_blocks) * c.block_size)
+    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d outside [0, max_blocks_per_seq * block_size]",
+                a.max_ctx);
+  const bool fp8 = c.dtype == PKV_E4M3;
+  if (fp8 && (a.k_scale == nullptr || a.v_scale == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "E4M3 cache needs k_scale and v_scale");
+  if (!fp8 && (a.k_scale != nullptr || a.v_scale != nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "scales given for a bf16 cache");
+  if (a.scale_stride < 0) return fail(PKV_ERR_INVALID_ARG, "scale_row_stride < 0");
+  if (a.batch == 0) return PKV_OK;
+  if (a.q == nullptr || a.k_cache == nullptr || a.v_cache == nullptr || a.out == nullptr ||
+      a.block_tables == nullptr || a.context_lens == nullptr)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned(a.q, 16) || !aligned(a.k_cache, 16) || !aligned(a.v_cache, 16) || !aligned(a.out, 16))
+    return fail(PKV_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
+  if (!aligned(a.block_tables, 4) || !aligned(a.context_lens, 4))
+    return fail(PKV_ERR_INVALID_ARG, "block_tables / context_lens must be 4-byte aligned");
+  if (fp8 && (!aligned(a.k_scale, 4) || !aligned(a.v_scale, 4)))
+    return fail(PKV_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  return PKV_OK;
+}
+
+pkv_status run_decode(const DecodeArgs& a, void* ws, size_t ws_bytes, int32_t split_tokens,
+                      cudaStream_t stream, bool own_workspace) {
+  int dev;
+  DeviceState* st;
+  pkv_status s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  pkv_decode_plan_t pl;
+  s = plan(a.batch, a.num_q_heads, a.cache, a.max_ctx, split_tokens, st->sms, &pl);
+  if (s != PKV_OK) return s;
+  if (!own_workspace && pl.workspace_bytes > 0) {
+    if (ws == nullptr || ws_bytes < static_cast<size_t>(pl.workspace_bytes))
+      return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes, need %lld", ws_bytes,
+                  static_cast<long long>(pl.workspace_bytes));
+    if (!aligned(ws, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  const pkv_cache_desc& c = *a.cache;
+  CUtensorMap tk, tv;
+  s = make_cache_tmap(&tk, a.k_cache, c);
+  if (s != PKV_OK) return s;
+  s = make_cache_tmap(&tv, a.v_cache, c);
+  if (s != PKV_OK) return s;
+
+  cudaError_t e;
+  if (own_workspace && pl.workspace_bytes > 0) {
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (st->pool == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        e = cudaMemPoolCreate(&st->pool, &props);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = ~0ull;
+        cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      }
+    }
+    e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(pl.workspace_bytes), st->pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(workspace)");
+  }
+
+  DecodeParams p = {};
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.out = a.out;
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.num_q_heads * pl.max_splits;
+  p.ws_o = pl.workspace_bytes > 0 ? static_cast<float*>(ws) : nullptr;
+  p.ws_ml = pl.workspace_bytes > 0
+                ? reinterpret_cast<float*>(static_cast<char*>(ws) + (rows * c.head_dim * 4 + 255) / 256 * 256)
+                : nullptr;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.scale_stride = a.scale_stride;
+  p.num_blocks = c.num_blocks;
+  p.batch = a.batch;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.group = a.num_q_heads / c.num_kv_heads;
+  p.head_dim = c.head_dim;
+  p.block_size = c.block_size;
+  p.max_blocks = a.max_blocks;
+  p.max_ctx = a.max_ctx;
+  p.split_tokens = pl.split_tokens;
+  p.max_splits = pl.max_splits;
+  p.qk_log2_scale = a.scale * 1.4426950408889634f;
+  p.cache_dtype = c.dtype;
+  p.err = st->err;
+
+  e = traced(pkv::kKindDecodeSplit, stream,
+             [&] { return pkv::launch_decode_split(p, tk, tv, stream); });
+  if (e == cudaSuccess && pl.max_splits > 1)
+    e = traced(pkv::kKindCombine, stream, [&] { return pkv::launch_decode_combine(p, stream); });
+  if (own_workspace && pl.workspace_bytes > 0) {
+    cudaError_t e2 = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_append(const void* k_new, const void* v_new, int32_t src_dtype, int64_t n_tokens,
+                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                      const pkv_cache_desc* cache, const float* k_scale, const float* v_scale,
+                      int64_t scale_row_stride, pkv_stream_t stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  if (src_dtype != PKV_BF16 && src_dtype != PKV_F32)
+    return fail(PKV_ERR_INVALID_ARG, "source dtype %d (PKV_BF16 or PKV_F32)", src_dtype);
+  if (n_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "n_tokens %lld", static_cast<long long>(n_tokens));
+  const bool fp8 = cache->dtype == PKV_E4M3;
+  if (fp8 && (k_scale == nullptr || v_scale == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "E4M3 cache needs k_scale and v_scale");
+  if (!fp8 && (k_scale != nullptr || v_scale != nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "scales given for a bf16 cache");
+  if (scale_row_stride < 0) return fail(PKV_ERR_INVALID_ARG, "scale_row_stride < 0");
+  if (n_tokens == 0) return PKV_OK;
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr || k_cache == nullptr ||
+      v_cache == nullptr)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_new, v_new and caches must be 16-byte aligned");
+  if (!aligned(slot_mapping, 8)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  if (fp8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4)))
+    return fail(PKV_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  AppendParams p = {};
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slots = slot_mapping;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.scale_stride = scale_row_stride;
+  p.n_tokens = n_tokens;
+  p.num_slots = cache->num_blocks * cache->block_size;
+  p.block_size = cache->block_size;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.head_dim = cache->head_dim;
+  p.src_dtype = src_dtype;
+  p.cache_dtype = cache->dtype;
+  p.err = st->err;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(pkv::kKindAppend, cs, [&] { return pkv::launch_append(p, cs); });
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
+                           int32_t max_context_len, int32_t split_tokens, int32_t num_sms,
+                           pkv_decode_plan_t* out) {
+  if (out == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan output is NULL");
+  return plan(batch, num_q_heads, cache, max_context_len, split_tokens, num_sms, out);
+}
+
+pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_heads,
+                                   const void* k_cache, const void* v_cache,
+                                   const pkv_cache_desc* cache, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                   int32_t max_context_len, float scale, float* out,
+                                   const float* k_scale, const float* v_scale,
+                                   int64_t scale_row_stride, void* workspace,
+                                   size_t workspace_bytes, int32_t split_tokens,
+                                   pkv_stream_t stream) {
+  DecodeArgs a = {q, batch, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                  context_lens, max_context_len, scale, out, k_scale, v_scale, scale_row_stride};
+  pkv_status s = check_decode(a);
+  if (s != PKV_OK) return s;
+  if (split_tokens < 0 || split_tokens % 64 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (0 or a multiple of 64)", split_tokens);
+  if (batch == 0) return PKV_OK;
+  return run_decode(a, workspace, workspace_bytes, split_tokens,
+                    reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+pkv_status pkv_decode_attention(const void* q, int32_t batch, int32_t num_q_heads,
+                                const void* k_cache, const void* v_cache,
+                                const pkv_cache_desc* cache, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                int32_t max_context_len, float scale, float* out,
+                                const float* k_scale, const float* v_scale,
+                                int64_t scale_row_stride, pkv_stream_t stream) {
+  DecodeArgs a = {q, batch, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                  context_lens, max_context_len, scale, out, k_scale, v_scale, scale_row_stride};
+  pkv_status s = check_decode(a);
+  if (s != PKV_OK) return s;
+  if (batch == 0) return PKV_OK;
+  return run_decode(a, nullptr, 0, 0, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int32_t pkv_get_device_error(pkv_stream_t stream) {
+  int dev;
+  DeviceState* st;
+  if (current_device(&dev, &st) != PKV_OK) return -1;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return -1;
+  int v = 0;
+  if (cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  const int zero = 0;
+  if (cudaMemcpy(st->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return -1;
+  return v;
+}
+
+const char* pkv_status_string(int32_t status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+    default: return "PKV_ERR_UNKNOWN";
+  }
+}
+
+const char* pkv_last_error(void) { return t_last_error.c_str(); }
+
+int32_t pkv_abi_version(void) { return 100; }
+
+pkv_status pkv_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = on != 0;
+  return PKV_OK;
+}
+
+int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity) {
+  std::vector<TraceRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    recs.swap(g_trace);
+  }
+  pkv_trace_entry agg[3] = {{0, 0, 0.0}, {1, 0, 0.0}, {2, 0, 0.0}};
+  int bad = 0;
+  for (const TraceRec& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      agg[r.kind].launches += 1;
+      agg[r.kind].total_ms += ms;
+    } else {
+      ++bad;
+    }
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_event_pool.push_back({r.dev, r.a});
+    g_event_pool.push_back({r.dev, r.b});
+  }
+  if (bad) return -1;
+  int n = 0;
+  for (int k = 0; k < 3 && n < capacity; ++k) {
+    if (agg[k].launches > 0 && entries != nullptr) entries[n++] = agg[k];
+  }
+  return n;
+}
+
+pkv_status pkv_shutdown(void) {
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (auto& pe : g_event_pool) cudaEventDestroy(pe.second);
+    g_event_pool.clear();
+    for (auto& r : g_trace) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+    g_trace.clear();
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& s : g_dev) {
+    if (s.pool != nullptr) {
+      cudaMemPoolDestroy(s.pool);
+      s.pool = nullptr;
+    }
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

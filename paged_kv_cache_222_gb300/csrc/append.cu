@@ -1,0 +1,131 @@
+// KV append: scatter each new token's K/V rows into their cache slots, copying
+// bf16 or quantising to FP8 E4M3 with a per-row, per-KV-head scale.
+//
+// What it computes: [SC] "LLM inference: prefill, decode, KV cache", section
+// "4. Internal workings", step 5 (the new token's K/V are appended to the
+// cache); FP8 E4M3 with per-head scales: [FN] "Sub-Millisecond Token
+// Scheduling...", FAQ "How much HBM memory does FP8 KV-cache quantization
+// save?".  Slot = physical_block * block_size + offset, negative = skip.
+//
+// Mapping: one thread per 8 consecutive elements of one (token, head) row, so a
+// warp moves 2 (D=128) or 4 (D=64) whole rows with 16-byte (bf16) or 8-byte
+// (E4M3) stores; loads are 16-byte (bf16 source) or 2x16-byte (f32 source).
+// Grid-stride, so any number of rows fits a bounded grid.
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kBF16 = 0, kF32 = 1, kE4M3 = 2;
+
+// Eight source elements as floats (bf16 widening is exact).
+template <int SRC>
+__device__ __forceinline__ void load8(const void* base, int64_t elem, float (&x)[8], uint4& raw) {
+  if constexpr (SRC == kBF16) {
+    raw = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16lo_to_f32(w[i]);
+      x[2 * i + 1] = bf16hi_to_f32(w[i]);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+    const float4 a = p[0], b = p[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+template <int SRC, int DST>
+__device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&x)[8], const uint4& raw,
+                                       float scale) {
+  if constexpr (DST == kBF16) {
+    uint4 o;
+    if constexpr (SRC == kBF16) {
+      o = raw;  // bit copy
+    } else {
+      o.x = pack_bf16x2(x[0], x[1]);
+      o.y = pack_bf16x2(x[2], x[3]);
+      o.z = pack_bf16x2(x[4], x[5]);
+      o.w = pack_bf16x2(x[6], x[7]);
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(cache) + elem) = o;
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // IEEE binary32 quotient, then one RNE-satfinite rounding to E4M3
+      const float lo = __fdiv_rn(x[2 * i], scale);
+      const float hi = __fdiv_rn(x[2 * i + 1], scale);
+      w[i] = f32x2_to_e4m3x2(lo, hi);
+    }
+    uint2 o;
+    o.x = w[0] | (w[1] << 16);
+    o.y = w[2] | (w[3] << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) = o;
+  }
+}
+
+template <int SRC, int DST>
+__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  const int D = p.head_dim;
+  const int H = p.num_kv_heads;
+  const int per_row = D / 8;
+  const int64_t total = p.n_tokens * H * per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const int64_t row = idx / per_row;  // token * H + head
+    const int part = static_cast<int>(idx - row * per_row);
+    const int64_t tok = row / H;
+    const int h = static_cast<int>(row - tok * H);
+    const int64_t slot = p.slots[tok];
+    if (slot < 0) continue;
+    if (slot >= p.num_slots) {
+      if (part == 0 && h == 0) record_error(p.err, kDevErrSlot);
+      continue;
+    }
+    const int64_t blk = slot / p.block_size;
+    const int64_t off = slot - blk * p.block_size;
+    const int64_t src_elem = row * D + part * 8;
+    const int64_t dst_elem = ((blk * H + h) * p.block_size + off) * D + part * 8;
+    float ks = 1.f, vs = 1.f;
+    if constexpr (DST == kE4M3) {
+      ks = p.k_scale[tok * p.scale_stride + h];
+      vs = p.v_scale[tok * p.scale_stride + h];
+    }
+    float x[8];
+    uint4 raw;
+    load8<SRC>(p.k_new, src_elem, x, raw);
+    store8<SRC, DST>(p.k_cache, dst_elem, x, raw, ks);
+    load8<SRC>(p.v_new, src_elem, x, raw);
+    store8<SRC, DST>(p.v_cache, dst_elem, x, raw, vs);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
+  const int64_t work = p.n_tokens * p.num_kv_heads * (p.head_dim / 8);
+  if (work == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (work + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 152 * 32 ? want : 152 * 32);
+  if (p.cache_dtype == kBF16) {
+    if (p.src_dtype == kBF16)
+      append_kernel<kBF16, kBF16><<<blocks, threads, 0, stream>>>(p);
+    else
+      append_kernel<kF32, kBF16><<<blocks, threads, 0, stream>>>(p);
+  } else {
+    if (p.src_dtype == kBF16)
+      append_kernel<kBF16, kE4M3><<<blocks, threads, 0, stream>>>(p);
+    else
+      append_kernel<kF32, kE4M3><<<blocks, threads, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,78 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units (append.cu, decode.cu).  Not installed; no stability promise.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+// Mirrors PKV_DEVERR_* of pkv.h (kept separate so device code needs no C ABI).
+constexpr int kDevErrWaitTimeout = 1;
+constexpr int kDevErrBlockId = 2;
+constexpr int kDevErrContextLen = 3;
+constexpr int kDevErrSlot = 4;
+
+// Tokens per pipeline tile: one mma M dimension of keys.
+constexpr int kTileTokens = 16;
+// Consumer warps per decode CTA.
+constexpr int kDecodeWarps = 4;
+
+enum KernelKind { kKindAppend = 0, kKindDecodeSplit = 1, kKindCombine = 2 };
+
+struct AppendParams {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;
+  void* k_cache;
+  void* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  int64_t scale_stride;
+  int64_t n_tokens;
+  int64_t num_slots;  // num_blocks * block_size
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t src_dtype;    // PKV_BF16 / PKV_F32
+  int32_t cache_dtype;  // PKV_BF16 / PKV_E4M3
+  int* err;
+};
+
+struct DecodeParams {
+  const void* q;              // bf16 [B, H_q, D]
+  const int32_t* block_tables;  // [B, MB]
+  const int32_t* context_lens;  // [B]
+  float* out;                 // [B, H_q, D]
+  float* ws_o;                // [B, H_q, S, D]   (S = max_splits > 1 only)
+  float* ws_ml;               // [B, H_q, S, 2]
+  const float* k_scale;
+  const float* v_scale;
+  int64_t scale_stride;
+  int64_t num_blocks;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;              // G = H_q / H_kv
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t max_blocks;         // MB
+  int32_t max_ctx;
+  int32_t split_tokens;
+  int32_t max_splits;
+  float qk_log2_scale;        // softmax scale * log2(e)
+  int32_t cache_dtype;
+  int* err;
+};
+
+// Launchers (return the launch's cudaError_t; nothing is synchronised).
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tmap_k,
+                                const CUtensorMap& tmap_v, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+
+// Dynamic shared memory the split kernel needs for (head_dim, dtype, groups).
+int decode_smem_bytes(int head_dim, int cache_dtype, int n_tiles8);
+
+}  // namespace pkv

@@ -1,0 +1,185 @@
+"""C-ABI library: loads, exports what include/pkv.h declares, and rejects bad
+arguments on the host before touching the GPU (CPU only, no compute calls)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_222_gb300 import build as B
+from paged_kv_cache_222_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _declared_functions()
+    for n in ["pkv_append", "pkv_decode_attention", "pkv_decode_attention_ex", "pkv_decode_plan",
+              "pkv_get_device_error", "pkv_status_string", "pkv_last_error", "pkv_abi_version",
+              "pkv_trace_enable", "pkv_trace_read", "pkv_shutdown"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding declares a signature for each of them
+    assert set(_declared_functions()) <= set(L.SIGNATURES)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pkv_abi_version() == 100
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(1) == b"PKV_ERR_INVALID_ARG"
+    assert lib.pkv_status_string(4) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
+
+
+def _desc(**kw):
+    d = dict(num_blocks=64, block_size=16, num_kv_heads=8, head_dim=128, dtype=L.PKV_BF16)
+    d.update(kw)
+    return L.CacheDesc(d["num_blocks"], d["block_size"], d["num_kv_heads"], d["head_dim"], d["dtype"])
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced
+NULL = ctypes.c_void_p(0)
+
+
+def _decode(lib, desc, **kw):
+    a = dict(q=FAKE, batch=2, hq=64, kc=FAKE, vc=FAKE, bt=FAKE, mb=8, cl=FAKE, max_ctx=100,
+             scale=0.125, out=FAKE, ks=NULL, vs=NULL, stride=0, ws=NULL, ws_bytes=0, split=0)
+    a.update(kw)
+    return lib.pkv_decode_attention_ex(a["q"], a["batch"], a["hq"], a["kc"], a["vc"], ctypes.byref(desc),
+                                       a["bt"], a["mb"], a["cl"], a["max_ctx"], a["scale"], a["out"],
+                                       a["ks"], a["vs"], a["stride"], a["ws"], a["ws_bytes"], a["split"],
+                                       NULL)
+
+
+@pytest.mark.parametrize("kw,desc_kw,code", [
+    (dict(hq=60), {}, L.PKV_ERR_INVALID_ARG),                 # not a multiple of H_kv
+    (dict(hq=8 * 17), {}, L.PKV_ERR_UNSUPPORTED),             # group of 17
+    (dict(batch=-1), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(batch=70000), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(max_ctx=8 * 16 + 1), {}, L.PKV_ERR_INVALID_ARG),     # beyond the table
+    (dict(max_ctx=-5), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(mb=0), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(q=NULL), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p(0x10004)), {}, L.PKV_ERR_INVALID_ARG),   # misaligned
+    (dict(kc=ctypes.c_void_p(0x10008)), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(ks=FAKE, vs=FAKE), {}, L.PKV_ERR_INVALID_ARG),       # scales on a bf16 cache
+    (dict(), dict(dtype=L.PKV_E4M3), L.PKV_ERR_INVALID_ARG),    # E4M3 without scales
+    (dict(), dict(dtype=L.PKV_F32), L.PKV_ERR_INVALID_ARG),     # f32 is not a cache dtype
+    (dict(), dict(head_dim=96), L.PKV_ERR_UNSUPPORTED),
+    (dict(), dict(block_size=8), L.PKV_ERR_UNSUPPORTED),
+    (dict(), dict(num_blocks=0), L.PKV_ERR_INVALID_ARG),
+    (dict(), dict(num_blocks=1 << 31), L.PKV_ERR_INVALID_ARG),
+    (dict(split=100), {}, L.PKV_ERR_INVALID_ARG),              # not a multiple of 64
+    (dict(stride=-1, ks=FAKE, vs=FAKE), dict(dtype=L.PKV_E4M3), L.PKV_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, desc_kw, code):
+    st = _decode(lib, _desc(**desc_kw), **kw)
+    assert st == code, lib.pkv_last_error()
+    assert lib.pkv_last_error()
+
+
+def test_decode_with_empty_batch_is_a_noop(lib):
+    assert _decode(lib, _desc(), batch=0, q=NULL, out=NULL) == L.PKV_OK
+
+
+def _append(lib, desc, **kw):
+    a = dict(k=FAKE, v=FAKE, src=L.PKV_BF16, n=4, slots=FAKE, kc=FAKE, vc=FAKE, ks=NULL, vs=NULL,
+             stride=0)
+    a.update(kw)
+    return lib.pkv_append(a["k"], a["v"], a["src"], a["n"], a["slots"], a["kc"], a["vc"],
+                          ctypes.byref(desc), a["ks"], a["vs"], a["stride"], NULL)
+
+
+@pytest.mark.parametrize("kw,desc_kw,code", [
+    (dict(src=L.PKV_E4M3), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(n=-1), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(k=NULL), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(slots=ctypes.c_void_p(0x10004)), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(v=ctypes.c_void_p(0x10002)), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(ks=FAKE, vs=FAKE), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(), dict(dtype=L.PKV_E4M3), L.PKV_ERR_INVALID_ARG),
+    (dict(ks=FAKE, vs=FAKE, stride=-2), dict(dtype=L.PKV_E4M3), L.PKV_ERR_INVALID_ARG),
+    (dict(), dict(head_dim=80), L.PKV_ERR_UNSUPPORTED),
+])
+def test_append_rejects_bad_arguments_on_host(lib, kw, desc_kw, code):
+    assert _append(lib, _desc(**desc_kw), **kw) == code
+
+
+def test_append_of_nothing_is_a_noop(lib):
+    assert _append(lib, _desc(), n=0, k=NULL, v=NULL, slots=NULL, kc=NULL, vc=NULL) == L.PKV_OK
+
+
+def _plan(lib, desc, batch, hq, max_ctx, split=0, sms=152):
+    p = L.DecodePlan()
+    st = lib.pkv_decode_plan(batch, hq, ctypes.byref(desc), max_ctx, split, sms, ctypes.byref(p))
+    assert st == L.PKV_OK, lib.pkv_last_error()
+    return p
+
+
+def test_plan_covers_the_context_and_sizes_the_workspace(lib):
+    d = _desc()
+    for batch, max_ctx in [(64, 8193), (256, 4097), (128, 5121), (8, 131104), (2, 101), (1, 1)]:
+        p = _plan(lib, d, batch, 64, max_ctx)
+        assert p.split_tokens % 64 == 0 and 256 <= p.split_tokens <= 4096
+        assert p.max_splits == -(-max_ctx // p.split_tokens)
+        assert (p.max_splits - 1) * p.split_tokens < max_ctx <= p.max_splits * p.split_tokens
+        rows = batch * 64 * p.max_splits
+        if p.max_splits > 1:
+            assert p.workspace_bytes >= rows * (128 + 2) * 4
+        else:
+            assert p.workspace_bytes == 0
+
+
+def test_plan_gives_enough_ctas_for_long_contexts(lib):
+    p = _plan(lib, _desc(), 8, 64, 131104)
+    assert 8 * 8 * p.max_splits >= 152 * 2 * 8
+    p2 = _plan(lib, _desc(), 8, 64, 131104, split=1024)
+    assert p2.split_tokens == 1024 and p2.max_splits == 129
+
+
+def test_plan_of_empty_contexts_has_one_split(lib):
+    p = _plan(lib, _desc(), 4, 64, 0)
+    assert p.max_splits == 1 and p.workspace_bytes == 0
+
+
+def test_workspace_too_small_is_reported(lib):
+    d = _desc(num_blocks=100000)
+    p = _plan(lib, d, 64, 64, 8193)
+    assert p.workspace_bytes > 0
+    st = _decode(lib, d, batch=64, mb=600, max_ctx=8193, ws=FAKE, ws_bytes=p.workspace_bytes - 1)
+    # rejected before any CUDA call: the size check precedes kernel setup only
+    # once the device is known, so without a GPU the CUDA query fails first
+    assert st in (L.PKV_ERR_WORKSPACE, L.PKV_ERR_CUDA)
+
+
+def test_slot_helper_matches_oracle_addressing():
+    import paged_kv_cache_222_gb300 as pkv
+    from oracle import paged_attention as PA
+    import workloads as W
+    case = W.make_case("tiny")
+    bt = case["block_tables"]
+    seq = torch.tensor([0, 0, 1, 1, 1])
+    pos = torch.tensor([0, 37, 5, 16, 100])
+    got = pkv.slots_for_positions(bt, seq, pos, case["bs"])
+    want = [PA.slot_of(bt[s].numpy(), int(p), case["bs"]) for s, p in zip(seq, pos)]
+    assert got.tolist() == want
