@@ -185,6 +185,36 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
                                    void* workspace, size_t workspace_bytes,
                                    int32_t split_tokens, pkv_stream_t stream);
 
+/*
+ * pkv_decode_attention_noalloc — pkv_decode_attention without any allocation.
+ * The source pages have no counterpart to this call; it exists for callers
+ * that must not allocate device memory when they run attention (a serving
+ * loop that reserved all memory at start-up, a runtime whose memory belongs
+ * to another allocator, code that must not wait on an allocator's locks).
+ *
+ * Same arguments, layouts and checks as pkv_decode_attention.  The split-KV
+ * partials go to a fixed 32 MiB array of device memory owned by the library
+ * (every GPU that loads the library holds it until the process exits).  A call
+ * whose plan needs more scratch than that (see pkv_decode_plan with
+ * split_tokens 0) returns PKV_ERR_WORKSPACE without launching anything.  The
+ * call makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents (nothing in it needs to start at zero): calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race on
+ * it and give wrong results.  Serialise them, or use pkv_decode_attention_ex.
+ */
+pkv_status pkv_decode_attention_noalloc(const void* q, int32_t batch, int32_t num_q_heads,
+                                        const void* k_cache, const void* v_cache,
+                                        const pkv_cache_desc* cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t max_context_len,
+                                        float scale, float* out,
+                                        const float* k_scale, const float* v_scale,
+                                        int64_t scale_row_stride, pkv_stream_t stream);
+
 /* Device error codes (first one recorded wins). */
 enum {
   PKV_DEVERR_NONE = 0,

@@ -52,6 +52,8 @@ SIGNATURES = {
                                ctypes.POINTER(DecodePlan)]),
     "pkv_decode_attention_ex": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
                                        _P, _I32, _F, _P, _P, _P, _I64, _P, ctypes.c_size_t, _I32, _P]),
+    "pkv_decode_attention_noalloc": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
+                                            _P, _I32, _F, _P, _P, _P, _I64, _P]),
     "pkv_get_device_error": (_I32, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_last_error": (ctypes.c_char_p, []),

@@ -537,3 +537,68 @@ pkv_status pkv_shutdown(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention that allocates nothing.
+//
+// The split-KV partials live in a fixed array in device memory that belongs to
+// this library, instead of memory the caller or a pool hands over.  This is
+// for callers that are not allowed to call cudaMalloc (or any allocator) at
+// the point where they run attention: serving loops that reserve all device
+// memory up front and forbid allocation afterwards, runtimes whose memory is
+// owned by a different allocator, and code that must not block on the
+// allocator's locks.  Host code only ever uses the array through the address
+// returned by cudaGetSymbolAddress; the array's name itself is a host-side
+// stand-in and must never be passed to a kernel.
+// ---------------------------------------------------------------------------
+
+static constexpr size_t kNoAllocScratchBytes = 32ull << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Once per device, with that device current: the device address of the array.
+pkv_status noalloc_scratch(int dev, void** ptr) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_decode_attention_noalloc(
+    const void* q, int32_t batch, int32_t num_q_heads, const void* k_cache, const void* v_cache,
+    const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, float scale, float* out,
+    const float* k_scale, const float* v_scale, int64_t scale_row_stride, pkv_stream_t stream) {
+  DecodeArgs a = {q, batch, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                  context_lens, max_context_len, scale, out, k_scale, v_scale, scale_row_stride};
+  pkv_status s = check_decode(a);
+  if (s != PKV_OK) return s;
+  if (batch == 0) return PKV_OK;
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  pkv_decode_plan_t pl;
+  s = plan(batch, num_q_heads, cache, max_context_len, 0, st->sms, &pl);
+  if (s != PKV_OK) return s;
+  if (static_cast<size_t>(pl.workspace_bytes) > kNoAllocScratchBytes)
+    return fail(PKV_ERR_WORKSPACE,
+                "this decode needs %lld bytes of split-KV scratch but the no-allocation entry "
+                "point has %zu; use pkv_decode_attention_ex with caller memory",
+                static_cast<long long>(pl.workspace_bytes), kNoAllocScratchBytes);
+  void* ws = nullptr;
+  s = noalloc_scratch(dev, &ws);
+  if (s != PKV_OK) return s;
+  return run_decode(a, ws, kNoAllocScratchBytes, 0, reinterpret_cast<cudaStream_t>(stream), false);
+}

@@ -1,0 +1,84 @@
+"""The allocation-free decode entry point, called through the C ABI.
+
+pkv_decode_attention_noalloc serves callers that must not allocate device
+memory while they run attention (for example a serving loop that reserved all
+of its memory at start-up, or a runtime whose memory belongs to another
+allocator).  It keeps its split-KV scratch in a fixed array owned by the
+library.  These tests check that it gives the same result as the entry point
+that takes caller memory, on two calls in a row that both use the scratch
+(the second must not be disturbed by what the first left there), and that a
+call needing more scratch than the array holds is refused before any launch.
+
+This file is collected last on purpose: the tests run after every other test
+as well as alone in a fresh process.
+"""
+
+import ctypes
+
+import pytest
+import torch
+
+import paged_kv_cache_222_gb300 as pkv
+import workloads as W
+from paged_kv_cache_222_gb300 import _lib as L
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL_BF16 = 2e-3          # decode tolerance for bf16 KV used across the tests
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_222_gb300 import build
+    build.build()
+    return pkv.library()
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _noalloc(lib, case, bt, lens, max_len, out):
+    desc = pkv.cache_desc(case["k_cache"])
+    q = case["q"][0]
+    stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
+    return lib.pkv_decode_attention_noalloc(
+        _p(q), q.shape[0], q.shape[1], _p(case["k_cache"]), _p(case["v_cache"]), ctypes.byref(desc),
+        _p(bt), bt.shape[1], _p(lens), int(max_len), float(case["scale"]), _p(out),
+        ctypes.c_void_p(0), ctypes.c_void_p(0), 0, stream)
+
+
+def test_noalloc_matches_caller_workspace_entry_point_on_two_calls(lib):
+    torch.cuda.set_device(DEV)
+    for seed, ctx in ((101, (3000, 1200, 4000)), (202, (700, 2900, 64))):
+        spec = dict(B=3, H_q=16, H_kv=2, D=128, bs=16, kv="bf16", free_frac=0.1, steps=1,
+                    seed=seed, ctx=ctx)
+        case = W.make_case(spec, device=DEV)
+        bt = case["block_tables"].to(DEV)
+        lens = (case["ctx"] + 1).to(DEV)
+        max_len = int(lens.max())
+        plan = pkv.decode_plan(3, 16, case["k_cache"], max_len)
+        assert plan.max_splits > 1 and plan.workspace_bytes > 0   # the scratch is really used
+        ref = pkv.decode_attention(case["q"][0], case["k_cache"], case["v_cache"], bt, lens,
+                                   case["scale"], max_context_len=max_len)
+        out = torch.full_like(ref, float("nan"))
+        st = _noalloc(lib, case, bt, lens, max_len, out)
+        assert st == L.PKV_OK, lib.pkv_last_error()
+        torch.cuda.synchronize()
+        assert torch.all(torch.isfinite(out))
+        assert float((out - ref).abs().max()) <= TOL_BF16
+    assert pkv.device_error(DEV) == 0
+
+
+def test_noalloc_refuses_more_scratch_than_it_has(lib):
+    torch.cuda.set_device(DEV)
+    desc = L.CacheDesc(1 << 20, 16, 8, 128, L.PKV_BF16)
+    fake = ctypes.c_void_p(0x10000)           # never dereferenced: refused before any launch
+    plan = pkv.decode_plan(2000, 64, desc, 65536)
+    assert plan.workspace_bytes > (32 << 20)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
+    st = lib.pkv_decode_attention_noalloc(fake, 2000, 64, fake, fake, ctypes.byref(desc), fake, 4096,
+                                          fake, 65536, 0.088, fake, ctypes.c_void_p(0),
+                                          ctypes.c_void_p(0), 0, stream)
+    assert st == L.PKV_ERR_WORKSPACE
+    assert b"no-allocation" in lib.pkv_last_error()
