@@ -149,17 +149,27 @@ pkv_status pkv_decode_attention(const void* q, int32_t batch, int32_t num_q_head
                                 int64_t scale_row_stride, pkv_stream_t stream);
 
 /*
- * Split-KV plan (host only, no CUDA call): how pkv_decode_attention_ex with
- * `split_tokens` (0 = automatic) divides each sequence into chunks.
- *   split_tokens  tokens per split (a multiple of 64)
- *   max_splits    ceil(max_context_len / split_tokens)
- *   workspace_bytes  scratch needed (0 when max_splits <= 1)
+ * Split-KV plan (host only, no CUDA call): how a decode call with
+ * `split_tokens` divides the work, and the scratch it needs.
+ *   mode          1 = fixed splits of `split_tokens` tokens per sequence (the
+ *                 default; split_tokens 0 picks the size), one CTA each, which
+ *                 the hardware scheduler balances across SMs.
+ *                 0 = balanced ("stream-K"), on request with split_tokens -1
+ *                 and batch <= 2048: the (sequence, KV head, 16-token tile)
+ *                 space is cut into equal contiguous ranges, one per warp of a
+ *                 persistent grid (`workers` warps).
+ *   split_tokens  tokens per split (mode 1), 0 in mode 0
+ *   max_splits    ceil(max_context_len / split_tokens) (mode 1), 0 in mode 0
+ *   workers       warps of the persistent grid (mode 0), 0 in mode 1
+ *   workspace_bytes  scratch needed (0 when mode 1 has one split)
  * `num_sms` is the GPU's SM count (152 on GB300); <= 0 means 152.
  */
 typedef struct {
   int32_t split_tokens;
   int32_t max_splits;
   int64_t workspace_bytes;
+  int32_t mode;
+  int32_t workers;
 } pkv_decode_plan_t;
 
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
@@ -172,7 +182,8 @@ pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_d
  *                    same (batch, num_q_heads, cache, max_context_len,
  *                    split_tokens), 256-byte aligned; may be NULL when that is
  *                    0.  Overlapping calls must not share a workspace.
- *   split_tokens     0 = automatic, else tokens per split (multiple of 64).
+ *   split_tokens     0 = automatic, -1 = balanced ranges, else tokens per
+ *                    split (a multiple of 64); see pkv_decode_plan.
  */
 pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_heads,
                                    const void* k_cache, const void* v_cache,

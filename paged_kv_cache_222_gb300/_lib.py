@@ -32,7 +32,8 @@ class CacheDesc(ctypes.Structure):
 
 class DecodePlan(ctypes.Structure):
     _fields_ = [("split_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("mode", ctypes.c_int32),
+                ("workers", ctypes.c_int32)]
 
 
 class TraceEntry(ctypes.Structure):

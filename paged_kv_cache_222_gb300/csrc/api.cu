@@ -186,14 +186,16 @@ pkv_status check_cache(const pkv_cache_desc* c) {
 }
 
 int32_t auto_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int32_t sms) {
-  // Largest power-of-two chunk (256..4096 tokens) that still gives about eight
-  // waves of two CTAs per SM when every sequence is as long as the bound.
+  // Largest power-of-two chunk (256..4096 tokens) that still gives about six
+  // waves of three CTAs per SM when every sequence is as long as the bound.
   const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
-  const int64_t want = static_cast<int64_t>(sms) * 2 * 8;
+  const int64_t want = static_cast<int64_t>(sms) * 3 * 6;
   int32_t st = 4096;
   while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
   return st;
 }
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
 pkv_status plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int32_t max_ctx,
                 int32_t split_tokens, int32_t sms, pkv_decode_plan_t* out) {
@@ -206,19 +208,35 @@ pkv_status plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int
   if (num_q_heads / c->num_kv_heads > 16)
     return fail(PKV_ERR_UNSUPPORTED, "group size %d > 16", num_q_heads / c->num_kv_heads);
   if (max_ctx < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d", max_ctx);
-  if (split_tokens < 0 || split_tokens % 64 != 0)
-    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (0 or a multiple of 64)", split_tokens);
+  if (split_tokens < -1 || (split_tokens > 0 && split_tokens % 64 != 0))
+    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (-1, 0 or a multiple of 64)", split_tokens);
   if (sms <= 0) sms = kDefaultSms;
-  const int32_t st = split_tokens ? split_tokens : auto_split_tokens(batch, c->num_kv_heads, max_ctx, sms);
+  const int64_t gp = num_q_heads / c->num_kv_heads > 8 ? 16 : 8;
+  const int64_t tiles_bound =
+      static_cast<int64_t>(batch) * c->num_kv_heads * ceil_div(max_ctx, pkv::kTileTokens);
+  *out = pkv_decode_plan_t{};
+  // Fixed splits by default: many CTAs that the hardware scheduler balances
+  // across SMs (whose share of HBM bandwidth differs); balanced static ranges
+  // on request.
+  const bool want_balanced = split_tokens == -1;
+  if (want_balanced && batch <= pkv::kMaxStreamKBatch && tiles_bound < 0x7FFFFFFFll) {
+    const int64_t w = pkv::streamk_grid_workers(c->head_dim, c->dtype, sms);
+    out->mode = pkv::kModeStreamK;
+    out->workers = static_cast<int32_t>(w);
+    out->workspace_bytes = align256(2 * w * gp * c->head_dim * 4) + align256(2 * w * gp * 2 * 4) +
+                           align256((static_cast<int64_t>(batch) + 1) * 4);
+    return PKV_OK;
+  }
+  const int32_t st =
+      split_tokens > 0 ? split_tokens : auto_split_tokens(batch, c->num_kv_heads, max_ctx, sms);
   const int64_t splits = max_ctx > 0 ? ceil_div(max_ctx, st) : 1;
   if (splits > 0x7FFFFFFFll) return fail(PKV_ERR_INVALID_ARG, "too many splits");
+  out->mode = pkv::kModeFixedSplit;
   out->split_tokens = st;
   out->max_splits = static_cast<int32_t>(splits);
-  out->workspace_bytes = 0;
   if (splits > 1) {
     const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * splits;
-    const int64_t o_bytes = (rows * c->head_dim * 4 + 255) / 256 * 256;
-    out->workspace_bytes = o_bytes + rows * 2 * 4;
+    out->workspace_bytes = align256(rows * c->head_dim * 4) + rows * 2 * 4;
   }
   return PKV_OK;
 }
@@ -320,11 +338,18 @@ pkv_status run_decode(const DecodeArgs& a, void* ws, size_t ws_bytes, int32_t sp
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.out = a.out;
-  const int64_t rows = static_cast<int64_t>(a.batch) * a.num_q_heads * pl.max_splits;
-  p.ws_o = pl.workspace_bytes > 0 ? static_cast<float*>(ws) : nullptr;
-  p.ws_ml = pl.workspace_bytes > 0
-                ? reinterpret_cast<float*>(static_cast<char*>(ws) + (rows * c.head_dim * 4 + 255) / 256 * 256)
-                : nullptr;
+  if (pl.mode == pkv::kModeStreamK) {
+    const int64_t gp = a.num_q_heads / c.num_kv_heads > 8 ? 16 : 8;
+    const int64_t o_bytes = align256(2 * static_cast<int64_t>(pl.workers) * gp * c.head_dim * 4);
+    const int64_t ml_bytes = align256(2 * static_cast<int64_t>(pl.workers) * gp * 2 * 4);
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+    p.ws_q = reinterpret_cast<int*>(static_cast<char*>(ws) + o_bytes + ml_bytes);
+  } else if (pl.workspace_bytes > 0) {
+    const int64_t rows = static_cast<int64_t>(a.batch) * a.num_q_heads * pl.max_splits;
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * c.head_dim * 4));
+  }
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
   p.scale_stride = a.scale_stride;
@@ -341,11 +366,13 @@ pkv_status run_decode(const DecodeArgs& a, void* ws, size_t ws_bytes, int32_t sp
   p.max_splits = pl.max_splits;
   p.qk_log2_scale = a.scale * 1.4426950408889634f;
   p.cache_dtype = c.dtype;
+  p.mode = pl.mode;
+  p.workers = pl.workers;
   p.err = st->err;
 
   e = traced(pkv::kKindDecodeSplit, stream,
              [&] { return pkv::launch_decode_split(p, tk, tv, stream); });
-  if (e == cudaSuccess && pl.max_splits > 1)
+  if (e == cudaSuccess && (pl.mode == pkv::kModeStreamK || pl.max_splits > 1))
     e = traced(pkv::kKindCombine, stream, [&] { return pkv::launch_decode_combine(p, stream); });
   if (own_workspace && pl.workspace_bytes > 0) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
@@ -431,8 +458,8 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
                   context_lens, max_context_len, scale, out, k_scale, v_scale, scale_row_stride};
   pkv_status s = check_decode(a);
   if (s != PKV_OK) return s;
-  if (split_tokens < 0 || split_tokens % 64 != 0)
-    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (0 or a multiple of 64)", split_tokens);
+  if (split_tokens < -1 || (split_tokens > 0 && split_tokens % 64 != 0))
+    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (-1, 0 or a multiple of 64)", split_tokens);
   if (batch == 0) return PKV_OK;
   return run_decode(a, workspace, workspace_bytes, split_tokens,
                     reinterpret_cast<cudaStream_t>(stream), false);
@@ -479,7 +506,7 @@ const char* pkv_status_string(int32_t status) {
 
 const char* pkv_last_error(void) { return t_last_error.c_str(); }
 
-int32_t pkv_abi_version(void) { return 100; }
+int32_t pkv_abi_version(void) { return 101; }
 
 pkv_status pkv_trace_enable(int32_t on) {
   std::lock_guard<std::mutex> lk(g_trace_mu);

@@ -71,6 +71,11 @@ __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&
 
 template <int SRC, int DST>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  // Let the next kernel in the stream start launching now (it waits for this
+  // grid to finish before it reads anything), then wait for the previous one:
+  // a slot written here may be one it still reads.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int D = p.head_dim;
   const int H = p.num_kv_heads;
   const int per_row = D / 8;
@@ -114,18 +119,23 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int threads = 256;
   const int64_t want = (work + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 152 * 32 ? want : 152 * 32);
-  if (p.cache_dtype == kBF16) {
-    if (p.src_dtype == kBF16)
-      append_kernel<kBF16, kBF16><<<blocks, threads, 0, stream>>>(p);
-    else
-      append_kernel<kF32, kBF16><<<blocks, threads, 0, stream>>>(p);
-  } else {
-    if (p.src_dtype == kBF16)
-      append_kernel<kBF16, kE4M3><<<blocks, threads, 0, stream>>>(p);
-    else
-      append_kernel<kF32, kE4M3><<<blocks, threads, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  void (*kern)(AppendParams);
+  if (p.cache_dtype == kBF16)
+    kern = p.src_dtype == kBF16 ? append_kernel<kBF16, kBF16> : append_kernel<kF32, kBF16>;
+  else
+    kern = p.src_dtype == kBF16 ? append_kernel<kBF16, kE4M3> : append_kernel<kF32, kE4M3>;
+  // programmatic dependent launch: may be scheduled while the previous kernel
+  // drains; the kernel itself waits for it before touching memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace pkv

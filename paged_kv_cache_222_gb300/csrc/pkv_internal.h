@@ -21,6 +21,14 @@ constexpr int kDecodeWarps = 4;
 
 enum KernelKind { kKindAppend = 0, kKindDecodeSplit = 1, kKindCombine = 2 };
 
+// Decode work split: balanced stream-K ranges over the flattened
+// (sequence, head, tile) space, or fixed `split_tokens` chunks per sequence.
+constexpr int kModeStreamK = 0;
+constexpr int kModeFixedSplit = 1;
+// Largest batch the stream-K kernel takes (its tile prefix lives in shared
+// memory); larger batches use fixed splits.
+constexpr int kMaxStreamKBatch = 2048;
+
 struct AppendParams {
   const void* k_new;
   const void* v_new;
@@ -45,8 +53,9 @@ struct DecodeParams {
   const int32_t* block_tables;  // [B, MB]
   const int32_t* context_lens;  // [B]
   float* out;                 // [B, H_q, D]
-  float* ws_o;                // [B, H_q, S, D]   (S = max_splits > 1 only)
-  float* ws_ml;               // [B, H_q, S, 2]
+  float* ws_o;                // fixed split: [B, H_q, S, D]; stream-K: [2W, GP, D]
+  float* ws_ml;               // fixed split: [B, H_q, S, 2]; stream-K: [2W, GP, 2]
+  int* ws_q;                  // stream-K: tile prefix over sequences [B + 1]
   const float* k_scale;
   const float* v_scale;
   int64_t scale_stride;
@@ -63,6 +72,8 @@ struct DecodeParams {
   int32_t max_splits;
   float qk_log2_scale;        // softmax scale * log2(e)
   int32_t cache_dtype;
+  int32_t mode;               // kModeStreamK / kModeFixedSplit
+  int32_t workers;            // stream-K: warps of the persistent grid (W)
   int* err;
 };
 
@@ -74,5 +85,8 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 
 // Dynamic shared memory the split kernel needs for (head_dim, dtype, groups).
 int decode_smem_bytes(int head_dim, int cache_dtype, int n_tiles8);
+
+// Warps in the stream-K kernel's persistent grid on a GPU with `sms` SMs.
+int streamk_grid_workers(int head_dim, int cache_dtype, int sms);
 
 }  // namespace pkv

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.pkv_abi_version() == 100
+    assert lib.pkv_abi_version() == 101
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(1) == b"PKV_ERR_INVALID_ARG"
     assert lib.pkv_status_string(4) == b"PKV_ERR_WORKSPACE"
@@ -90,6 +90,7 @@ def _decode(lib, desc, **kw):
     (dict(), dict(num_blocks=0), L.PKV_ERR_INVALID_ARG),
     (dict(), dict(num_blocks=1 << 31), L.PKV_ERR_INVALID_ARG),
     (dict(split=100), {}, L.PKV_ERR_INVALID_ARG),              # not a multiple of 64
+    (dict(split=-2), {}, L.PKV_ERR_INVALID_ARG),
     (dict(stride=-1, ks=FAKE, vs=FAKE), dict(dtype=L.PKV_E4M3), L.PKV_ERR_INVALID_ARG),
 ])
 def test_decode_rejects_bad_arguments_on_host(lib, kw, desc_kw, code):
@@ -136,11 +137,15 @@ def _plan(lib, desc, batch, hq, max_ctx, split=0, sms=152):
     return p
 
 
-def test_plan_covers_the_context_and_sizes_the_workspace(lib):
+def test_fixed_split_plan_covers_the_context_and_sizes_the_workspace(lib):
     d = _desc()
-    for batch, max_ctx in [(64, 8193), (256, 4097), (128, 5121), (8, 131104), (2, 101), (1, 1)]:
-        p = _plan(lib, d, batch, 64, max_ctx)
-        assert p.split_tokens % 64 == 0 and 256 <= p.split_tokens <= 4096
+    for batch, max_ctx, split in [(64, 8193, 1024), (256, 4097, 512), (8, 131104, 2048), (2, 101, 64),
+                                  (1, 1, 256), (3000, 4097, 0)]:
+        p = _plan(lib, d, batch, 64, max_ctx, split=split)
+        assert p.mode == 1 and p.workers == 0
+        assert p.split_tokens % 64 == 0 and 64 <= p.split_tokens <= 4096
+        if split:
+            assert p.split_tokens == split
         assert p.max_splits == -(-max_ctx // p.split_tokens)
         assert (p.max_splits - 1) * p.split_tokens < max_ctx <= p.max_splits * p.split_tokens
         rows = batch * 64 * p.max_splits
@@ -150,16 +155,26 @@ def test_plan_covers_the_context_and_sizes_the_workspace(lib):
             assert p.workspace_bytes == 0
 
 
-def test_plan_gives_enough_ctas_for_long_contexts(lib):
-    p = _plan(lib, _desc(), 8, 64, 131104)
-    assert 8 * 8 * p.max_splits >= 152 * 2 * 8
-    p2 = _plan(lib, _desc(), 8, 64, 131104, split=1024)
-    assert p2.split_tokens == 1024 and p2.max_splits == 129
+def test_balanced_plan_on_request_up_to_2048_sequences(lib):
+    for D, G, dtype in [(128, 8, L.PKV_E4M3), (64, 4, L.PKV_E4M3), (128, 16, L.PKV_BF16)]:
+        d = _desc(dtype=dtype, head_dim=D, num_kv_heads=2)
+        for batch, max_ctx in [(1, 1), (64, 8193), (2048, 4097), (8, 131104), (5, 0)]:
+            p = _plan(lib, d, batch, 2 * G, max_ctx, split=-1, sms=152)
+            assert p.mode == 0 and p.split_tokens == 0 and p.max_splits == 0
+            assert p.workers > 0 and p.workers % 152 == 0
+            gp = 16 if G > 8 else 8
+            assert p.workspace_bytes >= 2 * p.workers * gp * (D + 2) * 4 + (batch + 1) * 4
+        assert _plan(lib, d, 2049, 2 * G, 4097, split=-1).mode == 1     # larger batches: fixed
+        assert _plan(lib, d, 64, 2 * G, 8193).mode == 1                  # default: fixed splits
+    # the grid follows the SM count
+    d8 = _desc(dtype=L.PKV_E4M3)
+    assert _plan(lib, d8, 64, 64, 8193, split=-1, sms=100).workers * 152 == \
+        _plan(lib, d8, 64, 64, 8193, split=-1, sms=152).workers * 100
 
 
-def test_plan_of_empty_contexts_has_one_split(lib):
-    p = _plan(lib, _desc(), 4, 64, 0)
-    assert p.max_splits == 1 and p.workspace_bytes == 0
+def test_fixed_split_auto_size_gives_enough_ctas_for_long_contexts(lib):
+    p = _plan(lib, _desc(), 3000, 64, 4097)
+    assert p.mode == 1 and 3000 * 8 * p.max_splits >= 152 * 3 * 6
 
 
 def test_workspace_too_small_is_reported(lib):

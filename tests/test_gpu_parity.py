@@ -178,10 +178,8 @@ def test_decode_sweep_matches_oracle(kv, D, G, H_kv, bs):
     else:
         S.poison_unused(case)
     snaps = snaps_for(case)
-    for st in (0, 64, 256):
-        if kv == "bf16":
-            # re-run from the same cache: the append rewrites the same slot
-            pass
+    for st in (0, -1, 64, 256):
+        # re-running rewrites the same slot with the same token
         out = S.run_step(case, 0, split_tokens=st)
         check_all_units(case, out, 0, snaps)
 
@@ -191,7 +189,7 @@ def test_ragged_lengths_around_tile_and_block_edges():
     case = small_case(kv="bf16", D=128, G=8, H_kv=1, bs=32, B=len(ctx), ctx=ctx, seed=77)
     S.poison_unused(case)
     snaps = snaps_for(case)
-    for st in (0, 64):
+    for st in (0, -1, 64):
         out = S.run_step(case, 0, split_tokens=st)
         check_all_units(case, out, 0, snaps)
 
@@ -201,7 +199,7 @@ def test_empty_context_gives_zero_rows():
     dev = DEV
     bt = case["block_tables"].to(dev)
     lens = torch.tensor([0, 10, 0], dtype=torch.int32, device=dev)
-    for st in (0, 64):
+    for st in (0, -1, 64):
         out = pkv.decode_attention(case["q"][0], case["k_cache"], case["v_cache"], bt, lens,
                                    case["scale"], max_context_len=10, split_tokens=st)
         o = out.cpu()
@@ -212,9 +210,71 @@ def test_empty_context_gives_zero_rows():
 def test_split_count_does_not_change_the_result():
     case = small_case(kv="bf16", D=128, G=8, H_kv=2, bs=16, B=3, ctx=[3000, 1500, 4095], seed=9,
                       q_mult=4.0)
-    outs = [S.run_step(case, 0, split_tokens=st).cpu() for st in (64, 256, 1024, 4096)]
+    outs = [S.run_step(case, 0, split_tokens=st).cpu() for st in (0, -1, 64, 256, 1024, 4096)]
     for o in outs[1:]:
         assert torch.max(torch.abs(o - outs[0])) < 1e-5
+
+
+def test_balanced_split_with_empty_sequences_between_others():
+    case = small_case(kv="bf16", D=128, G=8, H_kv=2, bs=16, B=6, ctx=[0, 0, 3000, 0, 17, 0], seed=61)
+    S.poison_unused(case)
+    snaps = snaps_for(case)
+    dev = DEV
+    bt = case["block_tables"].to(dev)
+    lens = torch.tensor([0, 0, 3001, 0, 18, 0], dtype=torch.int32, device=dev)
+    slots = pkv.slots_for_positions(bt, torch.tensor([2, 4], device=dev), torch.tensor([3000, 17], device=dev), 16)
+    pkv.append(case["k_new"][0][[2, 4]].contiguous(), case["v_new"][0][[2, 4]].contiguous(), slots,
+               case["k_cache"], case["v_cache"])
+    out = pkv.decode_attention(case["q"][0], case["k_cache"], case["v_cache"], bt, lens, case["scale"],
+                               max_context_len=3001, split_tokens=-1).cpu().numpy()
+    G = 8
+    for b in (0, 1, 3, 5):
+        assert np.all(out[b] == 0)
+    for b in (2, 4):
+        for h in range(2):
+            ref = S.oracle_unit(case, b, h, 0, snaps[(b, h)])
+            assert np.max(np.abs(out[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+
+
+def test_one_long_sequence_cut_into_many_pieces():
+    # 1 sequence x 1 KV head: every warp of the balanced split takes a piece
+    case = small_case(kv="bf16", D=128, G=8, H_kv=1, bs=32, B=1, ctx=[40000], seed=62, q_mult=4.0)
+    snaps = snaps_for(case)
+    plan = pkv.decode_plan(1, 8, case["k_cache"], 40001, split_tokens=-1)
+    assert plan.mode == 0
+    out = S.run_step(case, 0, split_tokens=-1)
+    check_all_units(case, out, 0, snaps)
+    ref_fixed = S.run_step(case, 0, split_tokens=1024)
+    assert torch.max(torch.abs(out - ref_fixed)) < 1e-5
+
+
+def test_all_contexts_empty():
+    case = small_case(kv="bf16", D=64, G=4, H_kv=2, bs=16, B=3, ctx=[4, 4, 4], seed=63)
+    lens = torch.zeros(3, dtype=torch.int32, device=DEV)
+    for st in (0, -1):
+        out = pkv.decode_attention(case["q"][0], case["k_cache"], case["v_cache"],
+                                   case["block_tables"].to(DEV), lens, case["scale"],
+                                   max_context_len=0, split_tokens=st)
+        assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_batch_above_balanced_limit_uses_fixed_splits(kv):
+    case = small_case(kv=kv, D=64, G=4, H_kv=1, bs=16, B=2100, ctx_range=(1, 80), seed=64)
+    if kv == "e4m3":
+        case["k_cache"].fill_(S.E4M3_NAN)
+        case["v_cache"].fill_(S.E4M3_NAN)
+        S.fill_fp8_cache(case)
+    else:
+        S.poison_unused(case)
+    assert pkv.decode_plan(2100, 4, case["k_cache"], 81).mode == 1
+    assert pkv.decode_plan(2100, 4, case["k_cache"], 81, split_tokens=-1).mode == 1
+    units = [(b, 0) for b in (0, 1, 777, 2099)]
+    snaps = snaps_for(case, units)
+    out = S.run_step(case, 0).cpu().numpy()
+    for b, h in units:
+        ref = S.oracle_unit(case, b, h, 0, None if snaps is None else snaps[(b, h)])
+        assert np.max(np.abs(out[b, 0:4] - ref)) <= S.tolerance(case)
 
 
 def test_block_relabelling_gives_identical_output():
