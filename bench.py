@@ -184,6 +184,27 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
+def max_over_ranks(x, device="cpu"):
+    """Largest value of x over all ranks (x itself with one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, steps, world, slowest_ms):
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return bytes_per_rank_step * steps * world / (slowest_ms / 1e3) / 1e9
+
+
+def replica_seed(base_seed, rank):
+    """Each replica draws its own workload (same shapes, different values)."""
+    return base_seed + 1000 * rank
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -275,9 +296,8 @@ def run_ours(args, rank, world, local_rank):
     dist = None
     if world > 1:
         import torch.distributed as dist
-    seed_shift = 1000 * rank
     spec = W.spec(args.workload)
-    spec["seed"] = spec["seed"] + seed_shift
+    spec["seed"] = replica_seed(spec["seed"], rank)
     case = W.make_case(spec, device=dev)
     B, bs = case["B"], case["bs"]
     fp8 = case["kv"] == "e4m3"
@@ -345,11 +365,8 @@ def run_ours(args, rank, world, local_rank):
     pkv.trace_enable(False)
     trace = pkv.trace_read()
 
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = kv_bytes * args.steps * world / (ms_max / 1e3) / 1e9
+    ms_max = max_over_ranks(ms, dev)
+    value = job_throughput(kv_bytes, args.steps, world, ms_max)
     seqs = B * args.steps * world / (ms_max / 1e3)
 
     # ---- end to end through the public API with host buffers
@@ -383,11 +400,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = kv_bytes * e2e_steps * world / (float(e2e_t.item()) / 1e3) / 1e9
+    e2e_value = job_throughput(kv_bytes, e2e_steps, world, max_over_ranks(e0.elapsed_time(e1), dev))
     if pkv.device_error(dev) != 0:
         raise RuntimeError("device error during the timed region")
 
