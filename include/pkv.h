@@ -170,6 +170,8 @@ typedef struct {
   int64_t workspace_bytes;
   int32_t mode;
   int32_t workers;
+  int32_t prefix_split_tokens;   /* cascade plans only (mode 2) */
+  int32_t reserved;
 } pkv_decode_plan_t;
 
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
@@ -225,6 +227,44 @@ pkv_status pkv_decode_attention_noalloc(const void* q, int32_t batch, int32_t nu
                                         float scale, float* out,
                                         const float* k_scale, const float* v_scale,
                                         int64_t scale_row_stride, pkv_stream_t stream);
+
+/*
+ * Cascade (shared-prefix) decode — decode attention for a batch whose
+ * sequences all begin with the same `prefix_len` tokens held in the same
+ * physical blocks (shared by reference: [FN] "Paged KV-Cache with Radix Tree
+ * Prefix Cache", copy-on-write prefix blocks; [SC] "7. Practical
+ * applications", prompt caching of identical prefixes).  The result equals
+ * pkv_decode_attention's; the prefix is attended once for all B x G query rows
+ * of each KV head (a dense Q.K^T / P.V product on the tensor cores) instead
+ * of once per sequence, and merged with each private suffix by the same
+ * log-sum-exp combine.
+ *
+ *   prefix_blocks  int32 [prefix_len / block_size]: the prefix's physical
+ *                  blocks.  For every sequence b the first prefix_len /
+ *                  block_size entries of block_tables[b] must equal them
+ *                  (they are not read), and context_lens[b] >= prefix_len.
+ *   prefix_len     > 0, a multiple of block_size, <= max_context_len.
+ *   Other arguments as pkv_decode_attention_ex; bf16 caches only (E4M3:
+ *   PKV_ERR_UNSUPPORTED).  Scratch: at least plan.workspace_bytes from
+ *   pkv_cascade_plan, 256-byte aligned.
+ *
+ * pkv_cascade_plan (host only): mode 2; split_tokens / max_splits describe the
+ * suffix splits, workers the number of prefix ranges and prefix_split_tokens
+ * their length.
+ */
+pkv_status pkv_cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
+                            int32_t prefix_len, int32_t max_context_len, int32_t num_sms,
+                            pkv_decode_plan_t* plan);
+
+pkv_status pkv_cascade_decode_attention(const void* q, int32_t batch, int32_t num_q_heads,
+                                        const void* k_cache, const void* v_cache,
+                                        const pkv_cache_desc* cache,
+                                        const int32_t* prefix_blocks, int32_t prefix_len,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t max_context_len,
+                                        float scale, float* out,
+                                        void* workspace, size_t workspace_bytes,
+                                        pkv_stream_t stream);
 
 /* Device error codes (first one recorded wins). */
 enum {

@@ -22,9 +22,10 @@ from ._lib import (PKV_BF16, PKV_E4M3, PKV_F32, CacheDesc, DecodePlan, PkvError,
                    TraceEntry)
 
 __all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slots_for_positions",
+           "cascade_plan", "cascade_decode_attention",
            "device_error", "trace_enable", "trace_read", "library", "PkvError"]
 
-KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine"}
+KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix"}
 
 
 def library():
@@ -197,6 +198,44 @@ def decode_attention_pooled(q, k_cache, v_cache, block_tables, context_lens, sca
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         _ptr(k_scale), _ptr(v_scale), int(stride), _stream(k_cache.device))
     _lib.check(st, "pkv_decode_attention")
+    return out
+
+
+def cascade_plan(batch, num_q_heads, k_cache_or_desc, prefix_len, max_context_len, num_sms=0):
+    """Plan of a cascade decode (host only)."""
+    lib = library()
+    desc = k_cache_or_desc if isinstance(k_cache_or_desc, CacheDesc) else cache_desc(k_cache_or_desc)
+    plan = DecodePlan()
+    st = lib.pkv_cascade_plan(int(batch), int(num_q_heads), ctypes.byref(desc), int(prefix_len),
+                              int(max_context_len), int(num_sms), ctypes.byref(plan))
+    _lib.check(st, "pkv_cascade_plan")
+    return plan
+
+
+def cascade_decode_attention(q, k_cache, v_cache, prefix_blocks, prefix_len, block_tables, context_lens,
+                             scale, max_context_len, out=None, workspace=None):
+    """Decode attention for a batch that shares its first `prefix_len` tokens
+    (physical blocks `prefix_blocks`, int32); same result as decode_attention."""
+    lib = library()
+    _check_pair(k_cache, v_cache)
+    dev = k_cache.device
+    desc = cache_desc(k_cache)
+    _contig(q, torch.bfloat16, "q", dev)
+    _contig(prefix_blocks, torch.int32, "prefix_blocks", dev)
+    _contig(block_tables, torch.int32, "block_tables", dev)
+    _contig(context_lens, torch.int32, "context_lens", dev)
+    b, hq, d = q.shape
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=torch.float32, device=dev)
+    plan = cascade_plan(b, hq, desc, prefix_len, max_context_len)
+    if workspace is None:
+        workspace = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dev)
+    st = lib.pkv_cascade_decode_attention(
+        _ptr(q), b, hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(prefix_blocks),
+        int(prefix_len), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        int(max_context_len), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
+        _stream(dev))
+    _lib.check(st, "pkv_cascade_decode_attention")
     return out
 
 

@@ -33,7 +33,8 @@ class CacheDesc(ctypes.Structure):
 class DecodePlan(ctypes.Structure):
     _fields_ = [("split_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("mode", ctypes.c_int32),
-                ("workers", ctypes.c_int32)]
+                ("workers", ctypes.c_int32), ("prefix_split_tokens", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class TraceEntry(ctypes.Structure):
@@ -55,6 +56,10 @@ SIGNATURES = {
                                        _P, _I32, _F, _P, _P, _P, _I64, _P, ctypes.c_size_t, _I32, _P]),
     "pkv_decode_attention_noalloc": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
                                             _P, _I32, _F, _P, _P, _P, _I64, _P]),
+    "pkv_cascade_plan": (_I32, [_I32, _I32, ctypes.POINTER(CacheDesc), _I32, _I32, _I32,
+                                ctypes.POINTER(DecodePlan)]),
+    "pkv_cascade_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
+                                            _P, _I32, _P, _I32, _F, _P, _P, ctypes.c_size_t, _P]),
     "pkv_get_device_error": (_I32, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_last_error": (ctypes.c_char_p, []),

@@ -368,6 +368,8 @@ pkv_status run_decode(const DecodeArgs& a, void* ws, size_t ws_bytes, int32_t sp
   p.cache_dtype = c.dtype;
   p.mode = pl.mode;
   p.workers = pl.workers;
+  p.extra_slot = -1;
+  p.slots_per_row = pl.max_splits;
   p.err = st->err;
 
   e = traced(pkv::kKindDecodeSplit, stream,
@@ -520,7 +522,7 @@ int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity) {
     std::lock_guard<std::mutex> lk(g_trace_mu);
     recs.swap(g_trace);
   }
-  pkv_trace_entry agg[3] = {{0, 0, 0.0}, {1, 0, 0.0}, {2, 0, 0.0}};
+  pkv_trace_entry agg[4] = {{0, 0, 0.0}, {1, 0, 0.0}, {2, 0, 0.0}, {3, 0, 0.0}};
   int bad = 0;
   for (const TraceRec& r : recs) {
     float ms = 0.f;
@@ -536,7 +538,7 @@ int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity) {
   }
   if (bad) return -1;
   int n = 0;
-  for (int k = 0; k < 3 && n < capacity; ++k) {
+  for (int k = 0; k < 4 && n < capacity; ++k) {
     if (agg[k].launches > 0 && entries != nullptr) entries[n++] = agg[k];
   }
   return n;
@@ -564,6 +566,133 @@ pkv_status pkv_shutdown(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Cascade (shared-prefix) decode.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int32_t prefix_len,
+                        int32_t max_ctx, int32_t sms, pkv_decode_plan_t* out) {
+  pkv_status s = check_cache(c);
+  if (s != PKV_OK) return s;
+  if (c->dtype != PKV_BF16) return fail(PKV_ERR_UNSUPPORTED, "cascade decode takes bf16 caches");
+  if (batch < 1 || batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch %d", batch);
+  if (num_q_heads < 1 || num_q_heads % c->num_kv_heads != 0 || num_q_heads / c->num_kv_heads > 16)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d for %d KV heads", num_q_heads, c->num_kv_heads);
+  if (prefix_len <= 0 || prefix_len % c->block_size != 0)
+    return fail(PKV_ERR_INVALID_ARG, "prefix_len %d (a positive multiple of block_size %d)", prefix_len,
+                c->block_size);
+  if (max_ctx < prefix_len) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d < prefix_len %d", max_ctx, prefix_len);
+  if (sms <= 0) sms = kDefaultSms;
+  const int32_t suffix = max_ctx - prefix_len;
+  const int32_t st = auto_split_tokens(batch, c->num_kv_heads, suffix > 0 ? suffix : 1, sms);
+  const int64_t splits = suffix > 0 ? ceil_div(suffix, st) : 1;
+  // prefix ranges: enough CTAs for two per SM, each at least one 64-token tile
+  // and at most 1024 blocks
+  const int64_t rows = static_cast<int64_t>(batch) * (num_q_heads / c->num_kv_heads);
+  const int64_t row_blocks = ceil_div(rows, pkv::kCascadeRows) * c->num_kv_heads;
+  int64_t nps = ceil_div(2LL * sms, row_blocks);
+  const int64_t tiles = ceil_div(prefix_len, pkv::kCascadeTile);
+  if (nps > tiles) nps = tiles;
+  if (nps < 1) nps = 1;
+  int64_t pst = ceil_div(ceil_div(prefix_len, nps), pkv::kCascadeTile) * pkv::kCascadeTile;
+  const int64_t max_pst = 1024LL * c->block_size / pkv::kCascadeTile * pkv::kCascadeTile;
+  if (pst > max_pst) pst = max_pst;
+  nps = ceil_div(prefix_len, pst);
+  *out = pkv_decode_plan_t{};
+  out->mode = 2;
+  out->split_tokens = st;
+  out->max_splits = static_cast<int32_t>(splits);
+  out->workers = static_cast<int32_t>(nps);
+  const int64_t slots = static_cast<int64_t>(batch) * num_q_heads * (splits + nps);
+  out->workspace_bytes = align256(slots * c->head_dim * 4) + slots * 2 * 4;
+  out->prefix_split_tokens = static_cast<int32_t>(pst);
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
+                                       int32_t prefix_len, int32_t max_context_len, int32_t num_sms,
+                                       pkv_decode_plan_t* plan) {
+  if (plan == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan output is NULL");
+  return cascade_plan(batch, num_q_heads, cache, prefix_len, max_context_len, num_sms, plan);
+}
+
+extern "C" pkv_status pkv_cascade_decode_attention(
+    const void* q, int32_t batch, int32_t num_q_heads, const void* k_cache, const void* v_cache,
+    const pkv_cache_desc* cache, const int32_t* prefix_blocks, int32_t prefix_len,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, float scale, float* out, void* workspace, size_t workspace_bytes,
+    pkv_stream_t stream) {
+  DecodeArgs a = {q, batch, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                  context_lens, max_context_len, scale, out, nullptr, nullptr, 0};
+  pkv_status s = check_decode(a);
+  if (s != PKV_OK) return s;
+  if (batch == 0) return PKV_OK;
+  if (prefix_blocks == nullptr || !aligned(prefix_blocks, 4))
+    return fail(PKV_ERR_INVALID_ARG, "prefix_blocks must be a 4-byte aligned device pointer");
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  pkv_decode_plan_t pl;
+  s = cascade_plan(batch, num_q_heads, cache, prefix_len, max_context_len, st->sms, &pl);
+  if (s != PKV_OK) return s;
+  if (workspace == nullptr || workspace_bytes < static_cast<size_t>(pl.workspace_bytes))
+    return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes, need %lld", workspace_bytes,
+                static_cast<long long>(pl.workspace_bytes));
+  if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const pkv_cache_desc& c = *cache;
+  CUtensorMap tk, tv;
+  s = make_cache_tmap(&tk, k_cache, c);
+  if (s != PKV_OK) return s;
+  s = make_cache_tmap(&tv, v_cache, c);
+  if (s != PKV_OK) return s;
+
+  const int64_t slots = pl.max_splits + pl.workers;
+  const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * slots;
+  DecodeParams p = {};
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * c.head_dim * 4));
+  p.num_blocks = c.num_blocks;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.group = num_q_heads / c.num_kv_heads;
+  p.head_dim = c.head_dim;
+  p.block_size = c.block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_ctx = max_context_len;
+  p.split_tokens = pl.split_tokens;
+  p.max_splits = pl.max_splits;
+  p.qk_log2_scale = scale * 1.4426950408889634f;
+  p.cache_dtype = c.dtype;
+  p.mode = pkv::kModeFixedSplit;
+  p.token_offset = prefix_len;
+  p.force_partial = 1;
+  p.extra_slot = pl.max_splits;
+  p.extra_count = pl.workers;
+  p.slots_per_row = static_cast<int32_t>(slots);
+  p.prefix_blocks = prefix_blocks;
+  p.prefix_len = prefix_len;
+  p.prefix_split_tokens = pl.prefix_split_tokens;
+  p.err = st->err;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(pkv::kKindCascadePrefix, cs, [&] { return pkv::launch_cascade_prefix(p, tk, tv, cs); });
+  if (e == cudaSuccess)
+    e = traced(pkv::kKindDecodeSplit, cs, [&] { return pkv::launch_decode_split(p, tk, tv, cs); });
+  if (e == cudaSuccess)
+    e = traced(pkv::kKindCombine, cs, [&] { return pkv::launch_decode_combine(p, cs); });
+  if (e != cudaSuccess) return cuda_fail(e, "cascade decode launch");
+  return PKV_OK;
+}
 
 // ---------------------------------------------------------------------------
 // Decode attention that allocates nothing.

@@ -416,16 +416,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
     record_error(p.err, kDevErrContextLen);
   const int64_t row0 = static_cast<int64_t>(b) * p.num_q_heads + static_cast<int64_t>(h) * G;
 
-  const int t_begin = split * p.split_tokens;
+  // tokens [token_offset, ctx) are split; token_offset > 0 leaves a shared
+  // prefix to the cascade prefix kernel
+  const int t_begin = p.token_offset + split * p.split_tokens;
   if (t_begin >= ctx) {
-    if (ctx == 0 && split == 0) {
+    if (ctx == 0 && split == 0 && !p.force_partial) {
       for (int i = threadIdx.x; i < G * D; i += blockDim.x) p.out[row0 * D + i] = 0.f;
     }
     return;
   }
   const int t_end = min(ctx, t_begin + p.split_tokens);
   const int n_tiles = (t_end - t_begin + kTileTokens - 1) / kTileTokens;
-  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
+  const int nsplit = (ctx - p.token_offset + p.split_tokens - 1) / p.split_tokens;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BARS);
   float* s_ml = reinterpret_cast<float*>(smem + S::ML);
@@ -548,8 +550,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
   }
   __syncthreads();
 
-  const bool direct = (nsplit == 1);
-  const int64_t S_max = p.max_splits;
+  const bool direct = (nsplit == 1) && !p.force_partial;
+  const int64_t S_max = p.slots_per_row;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D, d = idx - (idx / D) * D;
     float M = -CUDART_INF_F;
@@ -591,9 +593,11 @@ __global__ void __launch_bounds__(128) combine_rows_kernel(const DecodeParams p)
   if (row >= static_cast<int64_t>(p.batch) * p.num_q_heads) return;
   const int b = static_cast<int>(row / p.num_q_heads);
   const int ctx = clamp_ctx(p, p.context_lens[b]);
-  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit <= 1) return;  // written by the split kernel
-  const int64_t S_max = p.max_splits;
+  const int cs = ctx > p.token_offset ? ctx - p.token_offset : 0;
+  const int nsplit = (cs + p.split_tokens - 1) / p.split_tokens;
+  if (!p.force_partial && nsplit <= 1) return;  // written by the split kernel
+  const int ntot = nsplit + p.extra_count;      // + shared-prefix pieces
+  const int64_t S_max = p.slots_per_row;
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + row * S_max * 2);
   const float* wo = p.ws_o + row * S_max * D + lane * V;
   float2 mlr[R];
@@ -603,13 +607,14 @@ __global__ void __launch_bounds__(128) combine_rows_kernel(const DecodeParams p)
     mlr[u] = make_float2(-CUDART_INF_F, 0.f);
 #pragma unroll
     for (int v = 0; v < V; ++v) x[u][v] = 0.f;
-    if (u < nsplit) {
-      mlr[u] = ml[u];
+    if (u < ntot) {
+      const int slot = u < nsplit ? u : p.extra_slot + (u - nsplit);
+      mlr[u] = ml[slot];
       if constexpr (V == 4) {
-        const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<int64_t>(u) * D);
+        const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<int64_t>(slot) * D);
         x[u][0] = t.x; x[u][1] = t.y; x[u][2] = t.z; x[u][3] = t.w;
       } else {
-        const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<int64_t>(u) * D);
+        const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<int64_t>(slot) * D);
         x[u][0] = t.x; x[u][1] = t.y;
       }
     }
@@ -655,15 +660,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
   const int64_t row = blockIdx.x;
   const int b = static_cast<int>(row / p.num_q_heads);
   const int ctx = clamp_ctx(p, p.context_lens[b]);
-  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit <= 1) return;  // written by the split kernel
-  const int64_t S_max = p.max_splits;
+  const int cs = ctx > p.token_offset ? ctx - p.token_offset : 0;
+  const int nsplit = (cs + p.split_tokens - 1) / p.split_tokens;
+  if (!p.force_partial && nsplit <= 1) return;  // written by the split kernel
+  const int ntot = nsplit + p.extra_count;      // + shared-prefix pieces
+  const int64_t S_max = p.slots_per_row;
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + row * S_max * 2);
   const float* wo = p.ws_o + row * S_max * D + lane * V;
   float M = -CUDART_INF_F, L = 0.f, acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  for (int i0 = warp; i0 < nsplit; i0 += 4 * R) {
+  for (int i0 = warp; i0 < ntot; i0 += 4 * R) {
     float2 mlr[R];
     float x[R][V];
 #pragma unroll
@@ -672,13 +679,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
       mlr[u] = make_float2(-CUDART_INF_F, 0.f);
 #pragma unroll
       for (int v = 0; v < V; ++v) x[u][v] = 0.f;
-      if (i < nsplit) {
-        mlr[u] = ml[i];
+      if (i < ntot) {
+        const int slot = i < nsplit ? i : p.extra_slot + (i - nsplit);
+        mlr[u] = ml[slot];
         if constexpr (V == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<int64_t>(i) * D);
+          const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<int64_t>(slot) * D);
           x[u][0] = t.x; x[u][1] = t.y; x[u][2] = t.z; x[u][3] = t.w;
         } else {
-          const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<int64_t>(i) * D);
+          const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<int64_t>(slot) * D);
           x[u][0] = t.x; x[u][1] = t.y;
         }
       }
@@ -1067,6 +1075,253 @@ __global__ void __launch_bounds__(128) streamk_fixup_kernel(const DecodeParams p
   }
 }
 
+// ----------------------------------------------------------------------------
+// Cascade prefix kernel.  When every sequence of the batch starts with the same
+// `prefix_len` tokens (the same physical blocks, shared by reference), the
+// prefix part of decode attention is one dense product per KV head:
+//   S = Q_h K_prefix^T,  Q_h = the B*G query rows (b, g) of KV head h,
+// followed by the online softmax and P V_prefix.  Each CTA takes 64 query rows
+// (4 warps x 16) of one KV head over one range of prefix tokens, streams the
+// range in 64-token K/V tiles (TMA, 3 stages, full/empty mbarriers), and
+// writes (acc, m, l) per row into the workspace slot reserved for its range;
+// the combine kernel merges those with the private-suffix splits.
+// Fragments: S^T of the decode kernel becomes S = Q . K^T here (rows: queries,
+// cols: 8-token n-tiles), P re-enters as the A operand of P . V straight from
+// the S accumulators (two n-tiles make one 16-token k-step), as bf16 hi + lo.
+// ----------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128, 2)
+    cascade_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  using L = Layout<D, false>;
+  constexpr int KS = D / 16;
+  constexpr int NSUB = kCascadeTile / kTileTokens;
+  constexpr int STAGE = NSUB * L::STAGEB;     // K and V of 64 tokens
+  constexpr int NS = 3;
+  constexpr int kMaxPrefixBlocks = 1024;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, j = lane & 3;
+  const int h = blockIdx.y, ps = blockIdx.z;
+  const int G = p.group;
+  const int rows = p.batch * G;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
+  uint64_t* empty = full + NS;
+  int* s_blk = reinterpret_cast<int*>(empty + NS);  // this CTA's prefix block ids
+  const uint32_t stage0 = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 4);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  wait_prior_grid();
+
+  const int t0 = ps * p.prefix_split_tokens;
+  const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
+  const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
+  for (int i = threadIdx.x; i < nblk && i < kMaxPrefixBlocks; i += blockDim.x) {
+    int phys = p.prefix_blocks[t0 / p.block_size + i];
+    if (phys < 0 || phys >= p.num_blocks) {
+      record_error(p.err, kDevErrBlockId);
+      phys = -1;
+    }
+    s_blk[i] = phys;
+  }
+  __syncthreads();
+  const int ntile = (t1 - t0 + kCascadeTile - 1) / kCascadeTile;
+
+  auto issue = [&](int k) {  // thread 0: the four 16-token sub-tiles of tile k
+    const int s = k % NS;
+    const uint32_t dst = stage0 + s * STAGE;
+    const uint32_t bar = smem_u32(full + s);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, STAGE);
+#pragma unroll
+    for (int i = 0; i < NSUB; ++i) {
+      const int t = t0 + k * kCascadeTile + i * kTileTokens;
+      // sub-tiles past the prefix end read as zeros (block -1 lies outside the map)
+      const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;
+      const int tok0 = t % p.block_size;
+#pragma unroll
+      for (int bx = 0; bx < L::NBOX; ++bx) {
+        tma_load_4d(dst + i * L::STAGEB + bx * L::BOX_BYTES, &tmap_k, bar, bx * L::BOX_ELEMS, tok0, h, phys);
+        tma_load_4d(dst + i * L::STAGEB + L::TILEB + bx * L::BOX_BYTES, &tmap_v, bar, bx * L::BOX_ELEMS,
+                    tok0, h, phys);
+      }
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < ntile && k < NS; ++k) issue(k);
+
+  // query fragments (A operand of S = Q K^T): rows ra = base + r and rb = ra + 8
+  const int ra = blockIdx.x * kCascadeRows + warp * 16 + r, rb = ra + 8;
+  uint32_t qa[KS][4];
+  {
+    const uint16_t* q = static_cast<const uint16_t*>(p.q);
+    const uint16_t* qra = ra < rows ? q + (static_cast<int64_t>(ra / G) * p.num_q_heads + h * G + ra % G) * D : nullptr;
+    const uint16_t* qrb = rb < rows ? q + (static_cast<int64_t>(rb / G) * p.num_q_heads + h * G + rb % G) * D : nullptr;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d0 = 16 * ks + 2 * j;
+      qa[ks][0] = qra ? *reinterpret_cast<const uint32_t*>(qra + d0) : 0u;
+      qa[ks][1] = qrb ? *reinterpret_cast<const uint32_t*>(qrb + d0) : 0u;
+      qa[ks][2] = qra ? *reinterpret_cast<const uint32_t*>(qra + d0 + 8) : 0u;
+      qa[ks][3] = qrb ? *reinterpret_cast<const uint32_t*>(qrb + d0 + 8) : 0u;
+    }
+  }
+
+  const float qk_mult = p.qk_log2_scale;
+  float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F, l_a = 0.f, l_b = 0.f;
+  float o[D / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  // ldmatrix lanes: K (tok 0-7,c)(tok 0-7,c+1)(tok 8-15,c)(tok 8-15,c+1);
+  //                 V (tok 0-7,c)(tok 8-15,c)(tok 0-7,c+1)(tok 8-15,c+1)
+  const int mq = lane >> 3;
+  const int tok_k = (lane & 7) + (mq >> 1) * 8, ch_k = mq & 1;
+  const int tok_v = (lane & 7) + (mq & 1) * 8, ch_v = mq >> 1;
+
+  bool healthy = true;
+  for (int k = 0; k < ntile; ++k) {
+    const int s = k % NS;
+    const uint32_t par = static_cast<uint32_t>((k / NS) & 1);
+    const bool arrived = mbar_wait(smem_u32(full + s), par, p.err);
+    if (!__all_sync(kFull, arrived)) healthy = false;
+    const uint32_t base = stage0 + s * STAGE;
+    if (healthy) {
+      // ---- S = Q K^T over the tile's 64 tokens: 8 n-tiles of 8 tokens
+      float sc[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+      for (int sub = 0; sub < NSUB; ++sub) {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t R[4];
+          ldsm_x4(base + sub * L::STAGEB + L::off(tok_k, 2 * ks + ch_k), R);
+          mma_bf16_16816(sc[2 * sub], qa[ks], R[0], R[1]);
+          mma_bf16_16816(sc[2 * sub + 1], qa[ks], R[2], R[3]);
+        }
+      }
+      // ---- online softmax, rows a (cols e = 0, 1) and b (e = 2, 3)
+      const int valid = t1 - (t0 + k * kCascadeTile);
+      float mx_a = -CUDART_INF_F, mx_b = -CUDART_INF_F;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x = sc[nt][e] * qk_mult;
+          if (nt * 8 + 2 * j + (e & 1) >= valid) x = -CUDART_INF_F;
+          sc[nt][e] = x;
+        }
+        mx_a = fmaxf(mx_a, fmaxf(sc[nt][0], sc[nt][1]));
+        mx_b = fmaxf(mx_b, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFull, mx_a, 1));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFull, mx_a, 2));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFull, mx_b, 1));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFull, mx_b, 2));
+      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      const float mu_a = (mn_a == -CUDART_INF_F) ? 0.f : mn_a;
+      const float mu_b = (mn_b == -CUDART_INF_F) ? 0.f : mn_b;
+      const float al_a = fast_exp2(m_a - mu_a), al_b = fast_exp2(m_b - mu_b);
+      m_a = mn_a;
+      m_b = mn_b;
+      float sum_a = 0.f, sum_b = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        sc[nt][0] = fast_exp2(sc[nt][0] - mu_a);
+        sc[nt][1] = fast_exp2(sc[nt][1] - mu_a);
+        sc[nt][2] = fast_exp2(sc[nt][2] - mu_b);
+        sc[nt][3] = fast_exp2(sc[nt][3] - mu_b);
+        sum_a += sc[nt][0] + sc[nt][1];
+        sum_b += sc[nt][2] + sc[nt][3];
+      }
+      l_a = l_a * al_a + sum_a;
+      l_b = l_b * al_b + sum_b;
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt) {
+        o[nt][0] *= al_a;
+        o[nt][1] *= al_a;
+        o[nt][2] *= al_b;
+        o[nt][3] *= al_b;
+      }
+      // ---- O += P V, one 16-token k-step per sub-tile
+#pragma unroll
+      for (int sub = 0; sub < NSUB; ++sub) {
+        uint32_t ph[4], pl[4];
+        const float* c0 = sc[2 * sub];
+        const float* c1 = sc[2 * sub + 1];
+        ph[0] = pack_bf16x2(c0[0], c0[1]);
+        ph[1] = pack_bf16x2(c0[2], c0[3]);
+        ph[2] = pack_bf16x2(c1[0], c1[1]);
+        ph[3] = pack_bf16x2(c1[2], c1[3]);
+        pl[0] = pack_bf16x2(c0[0] - bf16lo_to_f32(ph[0]), c0[1] - bf16hi_to_f32(ph[0]));
+        pl[1] = pack_bf16x2(c0[2] - bf16lo_to_f32(ph[1]), c0[3] - bf16hi_to_f32(ph[1]));
+        pl[2] = pack_bf16x2(c1[0] - bf16lo_to_f32(ph[2]), c1[1] - bf16hi_to_f32(ph[2]));
+        pl[3] = pack_bf16x2(c1[2] - bf16lo_to_f32(ph[3]), c1[3] - bf16hi_to_f32(ph[3]));
+        const uint32_t vt = base + sub * L::STAGEB + L::TILEB;
+#pragma unroll
+        for (int dp = 0; dp < KS; ++dp) {
+          uint32_t R[4];
+          ldsm_x4_trans(vt + L::off(tok_v, 2 * dp + ch_v), R);
+          mma_bf16_16816(o[2 * dp], ph, R[0], R[1]);
+          mma_bf16_16816(o[2 * dp], pl, R[0], R[1]);
+          mma_bf16_16816(o[2 * dp + 1], ph, R[2], R[3]);
+          mma_bf16_16816(o[2 * dp + 1], pl, R[2], R[3]);
+        }
+      }
+    }
+    // ---- release the stage; thread 0 refills it once all four warps are done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    if (threadIdx.x == 0 && healthy && k + NS < ntile) {
+      if (mbar_wait(smem_u32(empty + s), par, p.err)) issue(k + NS);
+    }
+    __syncwarp();
+  }
+  if (!healthy && threadIdx.x == 0) {
+    for (int s = 0; s < NS && s < ntile; ++s) {
+      const int klast = s + ((ntile - 1 - s) / NS) * NS;
+      mbar_wait(smem_u32(full + s), static_cast<uint32_t>((klast / NS) & 1), nullptr);
+    }
+  }
+  allow_next_grid();
+
+  // ---- row sums over the 4 lanes of each row; write this range's piece
+  l_a += __shfl_xor_sync(kFull, l_a, 1);
+  l_a += __shfl_xor_sync(kFull, l_a, 2);
+  l_b += __shfl_xor_sync(kFull, l_b, 1);
+  l_b += __shfl_xor_sync(kFull, l_b, 2);
+  const int64_t S_row = p.slots_per_row;
+  const int slot = p.extra_slot + ps;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int rr = half ? rb : ra;
+    if (rr >= rows) continue;
+    const int64_t orow = static_cast<int64_t>(rr / G) * p.num_q_heads + h * G + rr % G;
+    const int64_t piece = orow * S_row + slot;
+    float* dst = p.ws_o + piece * D;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt)
+      *reinterpret_cast<float2*>(dst + 8 * nt + 2 * j) =
+          half ? make_float2(o[nt][2], o[nt][3]) : make_float2(o[nt][0], o[nt][1]);
+    if (j == 0) {
+      p.ws_ml[piece * 2] = half ? m_b : m_a;
+      p.ws_ml[piece * 2 + 1] = half ? l_b : l_a;
+    }
+  }
+}
+
 // Persistent-grid shape of the stream-K kernel per (D, dtype): warps per CTA,
 // pipeline stages per warp, CTAs per SM.
 template <int D, bool FP8>
@@ -1190,6 +1445,38 @@ cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tk, co
                  : launch_split_t<64, false, 2>(p, tk, tv, stream);
 }
 
+int cascade_smem_bytes(int head_dim) {
+  const int stage = (kCascadeTile / kTileTokens) * 2 * kTileTokens * head_dim * 2;
+  return 3 * stage + 6 * 8 + 1024 * 4 + 1024;
+}
+
+template <int D>
+cudaError_t launch_cascade_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t stream) {
+  auto kern = cascade_prefix_kernel<D>;
+  const int smem = cascade_smem_bytes(D);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int rows = p.batch * p.group;
+  const int nps = (p.prefix_len + p.prefix_split_tokens - 1) / p.prefix_split_tokens;
+  const dim3 grid((rows + kCascadeRows - 1) / kCascadeRows, p.num_kv_heads, nps);
+  return launch_pdl(kern, grid, dim3(128), smem, stream, tk, tv, p);
+}
+
+cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t stream) {
+  if (p.head_dim == 128) return launch_cascade_t<128>(p, tk, tv, stream);
+  return launch_cascade_t<64>(p, tk, tv, stream);
+}
+
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.batch) * p.num_q_heads;
   if (rows == 0) return cudaSuccess;
@@ -1202,8 +1489,8 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
     return nt2 ? launch_pdl(streamk_fixup_kernel<64, 2>, dim3(units), dim3(128), 0, stream, p)
                : launch_pdl(streamk_fixup_kernel<64, 1>, dim3(units), dim3(128), 0, stream, p);
   }
-  if (p.max_splits <= 1) return cudaSuccess;
-  if (p.max_splits <= 8) {
+  if (p.max_splits + p.extra_count <= 1 && !p.force_partial) return cudaSuccess;
+  if (p.max_splits + p.extra_count <= 8) {
     const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
     if (p.head_dim == 128) return launch_pdl(combine_rows_kernel<128>, dim3(blocks), dim3(128), 0, stream, p);
     return launch_pdl(combine_rows_kernel<64>, dim3(blocks), dim3(128), 0, stream, p);

@@ -19,7 +19,7 @@ constexpr int kTileTokens = 16;
 // Consumer warps per decode CTA.
 constexpr int kDecodeWarps = 4;
 
-enum KernelKind { kKindAppend = 0, kKindDecodeSplit = 1, kKindCombine = 2 };
+enum KernelKind { kKindAppend = 0, kKindDecodeSplit = 1, kKindCombine = 2, kKindCascadePrefix = 3 };
 
 // Decode work split: balanced stream-K ranges over the flattened
 // (sequence, head, tile) space, or fixed `split_tokens` chunks per sequence.
@@ -74,6 +74,15 @@ struct DecodeParams {
   int32_t cache_dtype;
   int32_t mode;               // kModeStreamK / kModeFixedSplit
   int32_t workers;            // stream-K: warps of the persistent grid (W)
+  // cascade (shared-prefix) decode; zero / -1 / NULL otherwise
+  int32_t token_offset;       // fixed split: attend tokens [token_offset, ctx)
+  int32_t force_partial;      // fixed split: always write partials, never `out`
+  int32_t extra_slot;         // combine: first workspace slot of the prefix pieces (-1: none)
+  int32_t extra_count;        // combine: number of prefix pieces per row
+  int32_t slots_per_row;      // fixed split / cascade: workspace slots per (b, hq) row
+  const int32_t* prefix_blocks;  // [prefix_len / block_size] physical blocks
+  int32_t prefix_len;
+  int32_t prefix_split_tokens;   // prefix tokens per prefix CTA (multiple of 64)
   int* err;
 };
 
@@ -82,6 +91,13 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tmap_k,
                                 const CUtensorMap& tmap_v, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tmap_k,
+                                  const CUtensorMap& tmap_v, cudaStream_t stream);
+
+// Rows of query heads one cascade prefix CTA covers (4 warps x 16).
+constexpr int kCascadeRows = 64;
+// Keys per cascade prefix tile (4 sub-tiles of kTileTokens).
+constexpr int kCascadeTile = 64;
 
 // Dynamic shared memory the split kernel needs for (head_dim, dtype, groups).
 int decode_smem_bytes(int head_dim, int cache_dtype, int n_tiles8);

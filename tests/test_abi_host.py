@@ -198,3 +198,34 @@ def test_slot_helper_matches_oracle_addressing():
     got = pkv.slots_for_positions(bt, seq, pos, case["bs"])
     want = [PA.slot_of(bt[s].numpy(), int(p), case["bs"]) for s, p in zip(seq, pos)]
     assert got.tolist() == want
+
+
+def _cplan(lib, desc, batch, hq, prefix, max_ctx, sms=152):
+    p = L.DecodePlan()
+    st = lib.pkv_cascade_plan(batch, hq, ctypes.byref(desc), prefix, max_ctx, sms, ctypes.byref(p))
+    return st, p
+
+
+def test_cascade_plan_shapes(lib):
+    d = _desc(block_size=32)
+    st, p = _cplan(lib, d, 128, 64, 4096, 5121)
+    assert st == L.PKV_OK, lib.pkv_last_error()
+    assert p.mode == 2 and p.workers >= 1 and p.prefix_split_tokens % 64 == 0
+    assert p.workers * p.prefix_split_tokens >= 4096 > (p.workers - 1) * p.prefix_split_tokens
+    assert p.max_splits == -(-(5121 - 4096) // p.split_tokens)
+    slots = 128 * 64 * (p.max_splits + p.workers)
+    assert p.workspace_bytes >= slots * (128 + 2) * 4
+    # a small batch spreads the prefix over more ranges
+    st2, p2 = _cplan(lib, d, 2, 64, 4096, 4200)
+    assert st2 == L.PKV_OK and p2.workers > p.workers
+
+
+@pytest.mark.parametrize("desc_kw,prefix,max_ctx,code", [
+    (dict(block_size=32), 48, 100, L.PKV_ERR_INVALID_ARG),     # not whole blocks
+    (dict(block_size=16), 0, 100, L.PKV_ERR_INVALID_ARG),
+    (dict(block_size=16), 128, 100, L.PKV_ERR_INVALID_ARG),    # beyond the longest context
+    (dict(dtype=L.PKV_E4M3), 64, 100, L.PKV_ERR_UNSUPPORTED),
+])
+def test_cascade_plan_rejects(lib, desc_kw, prefix, max_ctx, code):
+    st, _ = _cplan(lib, _desc(**desc_kw), 4, 64, prefix, max_ctx)
+    assert st == code

@@ -1,0 +1,90 @@
+"""Cascade (shared-prefix) decode on the GPU: parity with the oracle and with
+the plain decode path on batches whose sequences share their first tokens."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_222_gb300 as pkv
+import workloads as W
+from tests import gpu_support as S
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_222_gb300 import build
+    build.build()
+    pkv.library()
+    assert pkv.device_error(DEV) == 0
+    yield
+    assert pkv.device_error(DEV) == 0
+
+
+def shared_case(B, prefix, suffix_range, G, H_kv, D, bs, seed, q_mult=1.0):
+    spec = dict(B=B, prefix=prefix, suffix_range=suffix_range, H_q=G * H_kv, H_kv=H_kv, D=D, bs=bs,
+                kv="bf16", free_frac=0.1, steps=1, seed=seed, q_mult=q_mult)
+    return W.make_case(spec, device=DEV)
+
+
+def run_cascade(case):
+    dev = DEV
+    B, bs = case["B"], case["bs"]
+    bt = case["block_tables"].to(dev)
+    ctx = case["ctx"].to(dev)
+    slots = pkv.slots_for_positions(bt, torch.arange(B, device=dev), ctx.to(torch.int64), bs)
+    pkv.append(case["k_new"][0].contiguous(), case["v_new"][0].contiguous(), slots, case["k_cache"],
+               case["v_cache"])
+    lens = (ctx + 1).to(torch.int32)
+    mx = int(case["ctx"].max()) + 1
+    prefix = case["prefix"]
+    pblocks = bt[0, : prefix // bs].contiguous()
+    out_c = pkv.cascade_decode_attention(case["q"][0].contiguous(), case["k_cache"], case["v_cache"],
+                                         pblocks, prefix, bt, lens, case["scale"], mx)
+    out_p = pkv.decode_attention(case["q"][0].contiguous(), case["k_cache"], case["v_cache"], bt, lens,
+                                 case["scale"], max_context_len=mx)
+    return out_c, out_p
+
+
+@pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs", [
+    (5, 64, (1, 300), 8, 2, 128, 16),
+    (3, 128, (1, 100), 8, 1, 128, 32),
+    (7, 48, (1, 50), 4, 2, 64, 16),        # prefix not a multiple of the 64-token tile
+    (2, 512, (1, 40), 16, 2, 128, 32),     # G = 16
+    (33, 96, (1, 20), 6, 1, 64, 32),       # ragged row blocks (33 * 6 rows)
+])
+def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, bs):
+    case = shared_case(B, prefix, suffix, G, H_kv, D, bs, seed=500 + B + prefix)
+    S.poison_unused(case)
+    snaps = {(b, h): S.snapshot_sequence(case, b, h) for b in range(B) for h in range(H_kv)}
+    out_c, out_p = run_cascade(case)
+    got = out_c.cpu().numpy()
+    for (b, h), snap in snaps.items():
+        ref = S.oracle_unit(case, b, h, 0, snap)
+        assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+    assert torch.max(torch.abs(out_c - out_p)) < 1e-4
+
+
+def test_cascade_full_size_shared_prefix_workload():
+    case = W.make_case("shared_prefix", device=DEV)
+    units = [(0, 0), (77, 5), (127, 7)]
+    snaps = {u: S.snapshot_sequence(case, *u) for u in units}
+    out_c, out_p = run_cascade(case)
+    assert torch.max(torch.abs(out_c - out_p)) < 1e-4
+    got = out_c.cpu().numpy()
+    G = case["H_q"] // case["H_kv"]
+    for (b, h) in units:
+        ref = S.oracle_unit(case, b, h, 0, snaps[(b, h)])
+        assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+
+
+def test_cascade_sharp_softmax():
+    case = shared_case(4, 1024, (100, 600), 8, 2, 128, 32, seed=77, q_mult=4.0)
+    snaps = {(b, h): S.snapshot_sequence(case, b, h) for b in range(4) for h in range(2)}
+    out_c, out_p = run_cascade(case)
+    got = out_c.cpu().numpy()
+    for (b, h), snap in snaps.items():
+        ref = S.oracle_unit(case, b, h, 0, snap)
+        assert np.max(np.abs(got[b, h * 8:(h + 1) * 8] - ref)) <= 2e-3
