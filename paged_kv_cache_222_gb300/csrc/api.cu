@@ -592,7 +592,7 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
   // prefix ranges: enough CTAs for two per SM, each at least one 64-token tile
   // and at most 1024 blocks
   const int64_t rows = static_cast<int64_t>(batch) * (num_q_heads / c->num_kv_heads);
-  const int64_t row_blocks = ceil_div(rows, pkv::kCascadeRows) * c->num_kv_heads;
+  const int64_t row_blocks = ceil_div(rows, pkv::kCascadeRowsTc) * c->num_kv_heads;
   int64_t nps = ceil_div(2LL * sms, row_blocks);
   const int64_t tiles = ceil_div(prefix_len, pkv::kCascadeTile);
   if (nps > tiles) nps = tiles;

@@ -94,8 +94,10 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tmap_k,
                                   const CUtensorMap& tmap_v, cudaStream_t stream);
 
-// Rows of query heads one cascade prefix CTA covers (4 warps x 16).
+// Rows of query heads one cascade prefix CTA covers: 4 warps x 16 (mma.sync
+// kernel), one TMEM lane per thread (tcgen05 kernel).
 constexpr int kCascadeRows = 64;
+constexpr int kCascadeRowsTc = 128;
 // Keys per cascade prefix tile (4 sub-tiles of kTileTokens).
 constexpr int kCascadeTile = 64;
 
