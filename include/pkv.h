@@ -51,7 +51,8 @@ typedef enum {
   PKV_ERR_INVALID_ARG = 1,  /* a pointer, size, dtype or stride is not acceptable */
   PKV_ERR_UNSUPPORTED = 2,  /* valid in principle, no kernel built for it          */
   PKV_ERR_CUDA = 3,         /* the CUDA runtime reported an error                  */
-  PKV_ERR_WORKSPACE = 4     /* caller workspace smaller than required              */
+  PKV_ERR_WORKSPACE = 4,    /* caller workspace smaller than required              */
+  PKV_ERR_OUT_OF_BLOCKS = 5 /* block manager: free pool exhausted (preempt, retry) */
 } pkv_status;
 
 typedef enum {
@@ -296,7 +297,8 @@ int32_t pkv_abi_version(void);
  * bracketed by CUDA events recorded on the stream it runs on.
  * pkv_trace_read synchronises those events and returns, per kernel kind,
  * the number of launches and their summed device time; it then clears the
- * buffer.  Kinds: 0 append, 1 decode split, 2 combine.
+ * buffer.  Kinds: 0 append, 1 decode split, 2 combine, 3 cascade prefix,
+ * 4 block copy.
  */
 typedef struct {
   int32_t kind;

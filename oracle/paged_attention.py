@@ -117,6 +117,46 @@ def decode_attention(q_bits, k_cache, v_cache, cache_dtype, block_tables,
     return out
 
 
+def multi_query_attention(q_bits, k_cache, v_cache, cache_dtype, block_tables,
+                          context_lens, scale, k_scale=None, v_scale=None, units=None):
+    """Paged attention of q_len new tokens per sequence, causal among them.
+
+    The q_len new tokens of sequence b are its last q_len positions
+    (context_lens[b] counts them, as for decode): query i sits at position
+    p = context_lens[b] - q_len + i and attends tokens 0..p of the sequence,
+    i.e. every cached token plus the new tokens up to itself.  Used for a
+    chunk of a chunked prefill run next to decode steps ([SC] "9. Failure
+    modes and limitations", item 3, Chunked Prefill) and for checking the
+    tokens proposed by a draft model in one pass ([SC] "7. Practical
+    applications", item 3, Speculative Decoding).  A query with p < 0 (a
+    context shorter than q_len) attends nothing and yields zeros, as an empty
+    context does for decode.
+
+    q_bits        uint16 [B, q_len, H_q, D]
+    other arguments as decode_attention; units: optional (b, h_kv) subset
+    Returns float64 [B, q_len, H_q, D].
+    """
+    q = bf16_bits_to_f64(q_bits)
+    B, QL, H_q, D = q.shape
+    NB, H_kv, bs, D2 = k_cache.shape
+    assert D2 == D and H_q % H_kv == 0
+    G = H_q // H_kv
+    out = np.full((B, QL, H_q, D), np.nan)
+    if units is None:
+        units = [(b, h) for b in range(B) for h in range(H_kv)]
+    for b, h in units:
+        ctx = int(context_lens[b])
+        row = block_tables[b]
+        ks = None if k_scale is None else k_scale[b, h]
+        vs = None if v_scale is None else v_scale[b, h]
+        K = dequantize(gather_sequence(k_cache, row, ctx, h, bs), cache_dtype, ks)
+        V = dequantize(gather_sequence(v_cache, row, ctx, h, bs), cache_dtype, vs)
+        for i in range(QL):
+            n = max(ctx - QL + i + 1, 0)
+            out[b, i, h * G:(h + 1) * G] = attend(q[b, i, h * G:(h + 1) * G], K[:n], V[:n], float(scale))
+    return out
+
+
 def encode_rows(x, src_dtype, cache_dtype, scale_rows=None):
     """Encode new K or V rows [n, H_kv, D] into cache words.
 

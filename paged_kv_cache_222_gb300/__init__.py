@@ -15,6 +15,7 @@ Cache tensors are [num_blocks, H_kv, block_size, head_dim], bf16 or E4M3
 
 import ctypes
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -22,10 +23,10 @@ from ._lib import (PKV_BF16, PKV_E4M3, PKV_F32, CacheDesc, DecodePlan, PkvError,
                    TraceEntry)
 
 __all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slots_for_positions",
-           "cascade_plan", "cascade_decode_attention",
+           "cascade_plan", "cascade_decode_attention", "BlockManager", "OutOfBlocks", "copy_blocks",
            "device_error", "trace_enable", "trace_read", "library", "PkvError"]
 
-KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix"}
+KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix", 4: "block_copy"}
 
 
 def library():
@@ -268,3 +269,113 @@ def trace_read():
     if n < 0:
         raise RuntimeError("pkv_trace_read failed")
     return {KERNEL_KINDS[buf[i].kind]: (buf[i].launches, buf[i].total_ms) for i in range(n)}
+
+
+# ---------------------------------------------------------------- block manager
+
+class OutOfBlocks(PkvError):
+    """The free pool cannot cover an append (PKV_ERR_OUT_OF_BLOCKS): preempt a
+    sequence (free it or swap it out) and retry."""
+
+
+def _bm_check(status, where):
+    if status == _lib.PKV_ERR_OUT_OF_BLOCKS:
+        raise OutOfBlocks(status, where)
+    _lib.check(status, where)
+
+
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data) if a.size else ctypes.c_void_p(0)
+
+
+class BlockManager:
+    """Host block manager of one paged pool (include/pkv_blocks.h): free pool,
+    reference counts, per-sequence tables, copy-on-write, all-or-nothing
+    appends.  Host memory only; pair it with `copy_blocks` and `append`."""
+
+    def __init__(self, num_blocks, block_size):
+        h = ctypes.c_void_p()
+        _bm_check(library().pkv_bm_create(int(num_blocks), int(block_size), ctypes.byref(h)),
+                  "pkv_bm_create")
+        self._h = h
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if self._h:
+            library().pkv_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self):
+        return library().pkv_bm_num_free(self._h)
+
+    def num_sequences(self):
+        return library().pkv_bm_num_sequences(self._h)
+
+    def ref_count(self, block):
+        return library().pkv_bm_ref_count(self._h, int(block))
+
+    def seq_len(self, seq_id):
+        return library().pkv_bm_seq_len(self._h, int(seq_id))
+
+    def add_sequence(self, seq_id):
+        _bm_check(library().pkv_bm_add_sequence(self._h, int(seq_id)), "pkv_bm_add_sequence")
+
+    def fork(self, parent_id, child_id):
+        _bm_check(library().pkv_bm_fork(self._h, int(parent_id), int(child_id)), "pkv_bm_fork")
+
+    def free_sequence(self, seq_id):
+        _bm_check(library().pkv_bm_free_sequence(self._h, int(seq_id)), "pkv_bm_free_sequence")
+
+    def blocks_needed(self, seq_ids, n_new):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = np.ascontiguousarray(n_new, dtype=np.int32)
+        out = ctypes.c_int64()
+        _bm_check(library().pkv_bm_blocks_needed(self._h, len(ids), _np_ptr(ids), _np_ptr(n),
+                                                 ctypes.byref(out)), "pkv_bm_blocks_needed")
+        return out.value
+
+    def append(self, seq_ids, n_new):
+        """Reserve slots; returns (slots int64 [sum n_new], cow_pairs int32 [k, 2])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = np.ascontiguousarray(n_new, dtype=np.int32)
+        if ids.shape != n.shape:
+            raise ValueError("seq_ids and n_new differ in length")
+        slots = np.empty(int(np.maximum(n, 0).sum()), dtype=np.int64)
+        src = np.empty(max(len(ids), 1), dtype=np.int32)
+        dst = np.empty(max(len(ids), 1), dtype=np.int32)
+        nc = ctypes.c_int32()
+        _bm_check(library().pkv_bm_append(self._h, len(ids), _np_ptr(ids), _np_ptr(n), _np_ptr(slots),
+                                          _np_ptr(src), _np_ptr(dst), len(ids), ctypes.byref(nc)),
+                  "pkv_bm_append")
+        return slots, np.stack([src[:nc.value], dst[:nc.value]], axis=1)
+
+    def block_tables(self, seq_ids, max_blocks_per_seq):
+        """(block_tables int32 [n, max_blocks_per_seq] with -1 past each table, lens int32 [n])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tbl = np.empty((len(ids), int(max_blocks_per_seq)), dtype=np.int32)
+        lens = np.empty(len(ids), dtype=np.int32)
+        _bm_check(library().pkv_bm_block_tables(self._h, len(ids), _np_ptr(ids), int(max_blocks_per_seq),
+                                                _np_ptr(tbl), _np_ptr(lens)), "pkv_bm_block_tables")
+        return tbl, lens
+
+
+def copy_blocks(k_cache, v_cache, src_blocks, dst_blocks):
+    """Device copy-on-write step: block dst[i] := block src[i] in both caches.
+    src/dst: int32 CUDA tensors (or host sequences, copied to the device)."""
+    _check_pair(k_cache, v_cache)
+    dev = k_cache.device
+    src = torch.as_tensor(src_blocks, dtype=torch.int32).to(dev).contiguous()
+    dst = torch.as_tensor(dst_blocks, dtype=torch.int32).to(dev).contiguous()
+    if src.shape != dst.shape or src.dim() != 1:
+        raise ValueError("src_blocks and dst_blocks must be 1-D of equal length")
+    desc = cache_desc(k_cache)
+    with torch.cuda.device(dev):
+        _lib.check(library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(src),
+                                             _ptr(dst), src.numel(), _stream(dev)), "pkv_copy_blocks")

@@ -15,6 +15,7 @@ PKV_ERR_INVALID_ARG = 1
 PKV_ERR_UNSUPPORTED = 2
 PKV_ERR_CUDA = 3
 PKV_ERR_WORKSPACE = 4
+PKV_ERR_OUT_OF_BLOCKS = 5
 
 PKV_BF16 = 0
 PKV_F32 = 1
@@ -60,6 +61,19 @@ SIGNATURES = {
                                 ctypes.POINTER(DecodePlan)]),
     "pkv_cascade_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
                                             _P, _I32, _P, _I32, _F, _P, _P, ctypes.c_size_t, _P]),
+    "pkv_copy_blocks": (_I32, [_P, _P, ctypes.POINTER(CacheDesc), _P, _P, _I32, _P]),
+    "pkv_bm_create": (_I32, [_I64, _I32, ctypes.POINTER(_P)]),
+    "pkv_bm_destroy": (None, [_P]),
+    "pkv_bm_num_free": (_I64, [_P]),
+    "pkv_bm_ref_count": (_I32, [_P, _I64]),
+    "pkv_bm_seq_len": (_I64, [_P, _I64]),
+    "pkv_bm_num_sequences": (_I64, [_P]),
+    "pkv_bm_add_sequence": (_I32, [_P, _I64]),
+    "pkv_bm_fork": (_I32, [_P, _I64, _I64]),
+    "pkv_bm_free_sequence": (_I32, [_P, _I64]),
+    "pkv_bm_append": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _I32, ctypes.POINTER(_I32)]),
+    "pkv_bm_blocks_needed": (_I32, [_P, _I32, _P, _P, ctypes.POINTER(_I64)]),
+    "pkv_bm_block_tables": (_I32, [_P, _I32, _P, _I32, _P, _P]),
     "pkv_get_device_error": (_I32, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_last_error": (ctypes.c_char_p, []),

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libpkv.so")
 
-SOURCES = ["api.cu", "append.cu", "decode.cu"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "cascade.cu", "blocks.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +36,7 @@ def nvcc():
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "pkv.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 
@@ -61,7 +61,7 @@ def build(force=False, verbose=False, ptxas_verbose=False):
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         cmd = [cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "pkv.h"
+#include "pkv_blocks.h"
 #include "pkv_internal.h"
 
 namespace {
@@ -23,6 +24,12 @@ constexpr int kMaxDevices = 64;
 constexpr int kDefaultSms = 152;
 
 thread_local std::string t_last_error;
+
+}  // namespace
+
+void pkv::set_last_error(const char* msg) { t_last_error = msg; }
+
+namespace {
 
 pkv_status fail(pkv_status s, const char* fmt, ...) {
   char buf[512];
@@ -440,6 +447,42 @@ pkv_status pkv_append(const void* k_new, const void* v_new, int32_t src_dtype, i
   return PKV_OK;
 }
 
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                           const int32_t* src_blocks, const int32_t* dst_blocks, int32_t n_pairs,
+                           pkv_stream_t stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  if (n_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "n_pairs %d", n_pairs);
+  if (n_pairs == 0) return PKV_OK;
+  if (k_cache == nullptr || v_cache == nullptr || src_blocks == nullptr || dst_blocks == nullptr)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  if (!aligned(src_blocks, 4) || !aligned(dst_blocks, 4))
+    return fail(PKV_ERR_INVALID_ARG, "block id arrays must be 4-byte aligned");
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  const int64_t esz = cache->dtype == PKV_E4M3 ? 1 : 2;
+  pkv::CopyParams p = {};
+  p.k_src = k_cache;
+  p.v_src = v_cache;
+  p.k_dst = k_cache;
+  p.v_dst = v_cache;
+  p.src = src_blocks;
+  p.dst = dst_blocks;
+  p.n_pairs = n_pairs;
+  p.block_vec = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim * esz / 16;
+  p.src_blocks = cache->num_blocks;
+  p.dst_blocks = cache->num_blocks;
+  p.err = st->err;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(pkv::kKindBlockCopy, cs, [&] { return pkv::launch_copy_blocks(p, cs); });
+  if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
                            int32_t max_context_len, int32_t split_tokens, int32_t num_sms,
                            pkv_decode_plan_t* out) {
@@ -502,13 +545,14 @@ const char* pkv_status_string(int32_t status) {
     case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
     case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+    case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
     default: return "PKV_ERR_UNKNOWN";
   }
 }
 
 const char* pkv_last_error(void) { return t_last_error.c_str(); }
 
-int32_t pkv_abi_version(void) { return 101; }
+int32_t pkv_abi_version(void) { return 102; }
 
 pkv_status pkv_trace_enable(int32_t on) {
   std::lock_guard<std::mutex> lk(g_trace_mu);
@@ -522,7 +566,8 @@ int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity) {
     std::lock_guard<std::mutex> lk(g_trace_mu);
     recs.swap(g_trace);
   }
-  pkv_trace_entry agg[4] = {{0, 0, 0.0}, {1, 0, 0.0}, {2, 0, 0.0}, {3, 0, 0.0}};
+  pkv_trace_entry agg[pkv::kNumKernelKinds];
+  for (int k = 0; k < pkv::kNumKernelKinds; ++k) agg[k] = {k, 0, 0.0};
   int bad = 0;
   for (const TraceRec& r : recs) {
     float ms = 0.f;
@@ -538,7 +583,7 @@ int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity) {
   }
   if (bad) return -1;
   int n = 0;
-  for (int k = 0; k < 4 && n < capacity; ++k) {
+  for (int k = 0; k < pkv::kNumKernelKinds && n < capacity; ++k) {
     if (agg[k].launches > 0 && entries != nullptr) entries[n++] = agg[k];
   }
   return n;

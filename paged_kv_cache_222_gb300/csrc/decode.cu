@@ -38,41 +38,12 @@
 
 #include <utility>
 
+#include "decode_common.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
-
-constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kE4M3 = 2;
-
-template <int D, bool FP8>
-struct Layout {
-  static constexpr int ESZ = FP8 ? 1 : 2;
-  static constexpr int ROWB = D * ESZ;                    // bytes of one token row
-  static constexpr int BOXB = ROWB < 128 ? ROWB : 128;    // row bytes per TMA box
-  static constexpr int NBOX = ROWB / BOXB;                // boxes per tile
-  static constexpr int BOX_ELEMS = BOXB / ESZ;
-  static constexpr int CPB = BOXB / 16;                   // 16-byte chunks per box row
-  static constexpr int BOX_BYTES = kTileTokens * BOXB;
-  static constexpr int TILEB = kTileTokens * ROWB;        // K (or V) bytes of one tile
-  static constexpr int STAGEB = 2 * TILEB;                // K + V
-  // 16 KB of stages per warp: 64 KB per 4-warp CTA, three CTAs per SM, so one
-  // CTA's ramp-up and merge overlap the other two CTAs' streaming
-  static constexpr int NS = (16384 / STAGEB) > 8 ? 8 : (16384 / STAGEB);
-  static constexpr int PIPE_BYTES = kDecodeWarps * NS * STAGEB;
-
-  // Byte offset, inside a tile, of 16-byte chunk c of token row t as the TMA
-  // unit stores it: 128-byte rows swizzled by XOR of the chunk with (t mod 8),
-  // 64-byte rows by XOR with ((t / 2) mod 4).
-  __device__ static __forceinline__ uint32_t off(int t, int c) {
-    const int box = c / CPB;
-    const int cc = c % CPB;
-    const int sw = (BOXB == 128) ? (t & 7) : ((t >> 1) & 3);
-    return static_cast<uint32_t>(box * BOX_BYTES + t * BOXB + ((cc ^ sw) << 4));
-  }
-};
 
 template <int D, bool FP8, int NT>
 struct Smem {
@@ -256,23 +227,6 @@ __device__ __forceinline__ void process_tile(uint32_t stage, int valid, float qk
 // ----------------------------------------------------------------------------
 // Pieces shared by the two decode kernels.
 // ----------------------------------------------------------------------------
-
-// Context length as every kernel sees it: clamped to what the grid, the
-// workspace and the block table can hold (the violation is recorded once).
-__device__ __forceinline__ int clamp_ctx(const DecodeParams& p, int ctx) {
-  const int64_t table_cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
-  const int lim = static_cast<int>(table_cap < p.max_ctx ? table_cap : p.max_ctx);
-  return ctx < 0 ? 0 : (ctx > lim ? lim : ctx);
-}
-
-// Wait for the kernel that precedes this one in the stream (programmatic
-// dependent launch); a no-op when launched without that attribute.
-__device__ __forceinline__ void wait_prior_grid() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void allow_next_grid() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Warps the stream-K split uses for T flat tiles: at most the grid's warps,
 // and never fewer than kMinTilesPerWorker tiles per warp, so no range is empty.
@@ -1075,533 +1029,6 @@ __global__ void __launch_bounds__(128) streamk_fixup_kernel(const DecodeParams p
   }
 }
 
-// ----------------------------------------------------------------------------
-// Cascade prefix kernel.  When every sequence of the batch starts with the same
-// `prefix_len` tokens (the same physical blocks, shared by reference), the
-// prefix part of decode attention is one dense product per KV head:
-//   S = Q_h K_prefix^T,  Q_h = the B*G query rows (b, g) of KV head h,
-// followed by the online softmax and P V_prefix.  Each CTA takes 64 query rows
-// (4 warps x 16) of one KV head over one range of prefix tokens, streams the
-// range in 64-token K/V tiles (TMA, 3 stages, full/empty mbarriers), and
-// writes (acc, m, l) per row into the workspace slot reserved for its range;
-// the combine kernel merges those with the private-suffix splits.
-// Fragments: S^T of the decode kernel becomes S = Q . K^T here (rows: queries,
-// cols: 8-token n-tiles), P re-enters as the A operand of P . V straight from
-// the S accumulators (two n-tiles make one 16-token k-step), as bf16 hi + lo.
-// ----------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128, 2)
-    cascade_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  using L = Layout<D, false>;
-  constexpr int KS = D / 16;
-  constexpr int NSUB = kCascadeTile / kTileTokens;
-  constexpr int STAGE = NSUB * L::STAGEB;     // K and V of 64 tokens
-  constexpr int NS = 3;
-  constexpr int kMaxPrefixBlocks = 1024;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 2, j = lane & 3;
-  const int h = blockIdx.y, ps = blockIdx.z;
-  const int G = p.group;
-  const int rows = p.batch * G;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
-  uint64_t* empty = full + NS;
-  int* s_blk = reinterpret_cast<int*>(empty + NS);  // this CTA's prefix block ids
-  const uint32_t stage0 = smem_u32(smem);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 4);
-    }
-    fence_mbar_init();
-    prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_v);
-  }
-  wait_prior_grid();
-
-  const int t0 = ps * p.prefix_split_tokens;
-  const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
-  const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
-  for (int i = threadIdx.x; i < nblk && i < kMaxPrefixBlocks; i += blockDim.x) {
-    int phys = p.prefix_blocks[t0 / p.block_size + i];
-    if (phys < 0 || phys >= p.num_blocks) {
-      record_error(p.err, kDevErrBlockId);
-      phys = -1;
-    }
-    s_blk[i] = phys;
-  }
-  __syncthreads();
-  const int ntile = (t1 - t0 + kCascadeTile - 1) / kCascadeTile;
-
-  auto issue = [&](int k) {  // thread 0: the four 16-token sub-tiles of tile k
-    const int s = k % NS;
-    const uint32_t dst = stage0 + s * STAGE;
-    const uint32_t bar = smem_u32(full + s);
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int i = 0; i < NSUB; ++i) {
-      const int t = t0 + k * kCascadeTile + i * kTileTokens;
-      // sub-tiles past the prefix end read as zeros (block -1 lies outside the map)
-      const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;
-      const int tok0 = t % p.block_size;
-#pragma unroll
-      for (int bx = 0; bx < L::NBOX; ++bx) {
-        tma_load_4d(dst + i * L::STAGEB + bx * L::BOX_BYTES, &tmap_k, bar, bx * L::BOX_ELEMS, tok0, h, phys);
-        tma_load_4d(dst + i * L::STAGEB + L::TILEB + bx * L::BOX_BYTES, &tmap_v, bar, bx * L::BOX_ELEMS,
-                    tok0, h, phys);
-      }
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int k = 0; k < ntile && k < NS; ++k) issue(k);
-
-  // query fragments (A operand of S = Q K^T): rows ra = base + r and rb = ra + 8
-  const int ra = blockIdx.x * kCascadeRows + warp * 16 + r, rb = ra + 8;
-  uint32_t qa[KS][4];
-  {
-    const uint16_t* q = static_cast<const uint16_t*>(p.q);
-    const uint16_t* qra = ra < rows ? q + (static_cast<int64_t>(ra / G) * p.num_q_heads + h * G + ra % G) * D : nullptr;
-    const uint16_t* qrb = rb < rows ? q + (static_cast<int64_t>(rb / G) * p.num_q_heads + h * G + rb % G) * D : nullptr;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int d0 = 16 * ks + 2 * j;
-      qa[ks][0] = qra ? *reinterpret_cast<const uint32_t*>(qra + d0) : 0u;
-      qa[ks][1] = qrb ? *reinterpret_cast<const uint32_t*>(qrb + d0) : 0u;
-      qa[ks][2] = qra ? *reinterpret_cast<const uint32_t*>(qra + d0 + 8) : 0u;
-      qa[ks][3] = qrb ? *reinterpret_cast<const uint32_t*>(qrb + d0 + 8) : 0u;
-    }
-  }
-
-  const float qk_mult = p.qk_log2_scale;
-  float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F, l_a = 0.f, l_b = 0.f;
-  float o[D / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  // ldmatrix lanes: K (tok 0-7,c)(tok 0-7,c+1)(tok 8-15,c)(tok 8-15,c+1);
-  //                 V (tok 0-7,c)(tok 8-15,c)(tok 0-7,c+1)(tok 8-15,c+1)
-  const int mq = lane >> 3;
-  const int tok_k = (lane & 7) + (mq >> 1) * 8, ch_k = mq & 1;
-  const int tok_v = (lane & 7) + (mq & 1) * 8, ch_v = mq >> 1;
-
-  bool healthy = true;
-  for (int k = 0; k < ntile; ++k) {
-    const int s = k % NS;
-    const uint32_t par = static_cast<uint32_t>((k / NS) & 1);
-    const bool arrived = mbar_wait(smem_u32(full + s), par, p.err);
-    if (!__all_sync(kFull, arrived)) healthy = false;
-    const uint32_t base = stage0 + s * STAGE;
-    if (healthy) {
-      // ---- S = Q K^T over the tile's 64 tokens: 8 n-tiles of 8 tokens
-      float sc[8][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-      for (int sub = 0; sub < NSUB; ++sub) {
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t R[4];
-          ldsm_x4(base + sub * L::STAGEB + L::off(tok_k, 2 * ks + ch_k), R);
-          mma_bf16_16816(sc[2 * sub], qa[ks], R[0], R[1]);
-          mma_bf16_16816(sc[2 * sub + 1], qa[ks], R[2], R[3]);
-        }
-      }
-      // ---- online softmax, rows a (cols e = 0, 1) and b (e = 2, 3)
-      const int valid = t1 - (t0 + k * kCascadeTile);
-      float mx_a = -CUDART_INF_F, mx_b = -CUDART_INF_F;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x = sc[nt][e] * qk_mult;
-          if (nt * 8 + 2 * j + (e & 1) >= valid) x = -CUDART_INF_F;
-          sc[nt][e] = x;
-        }
-        mx_a = fmaxf(mx_a, fmaxf(sc[nt][0], sc[nt][1]));
-        mx_b = fmaxf(mx_b, fmaxf(sc[nt][2], sc[nt][3]));
-      }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFull, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFull, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFull, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFull, mx_b, 2));
-      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-      const float mu_a = (mn_a == -CUDART_INF_F) ? 0.f : mn_a;
-      const float mu_b = (mn_b == -CUDART_INF_F) ? 0.f : mn_b;
-      const float al_a = fast_exp2(m_a - mu_a), al_b = fast_exp2(m_b - mu_b);
-      m_a = mn_a;
-      m_b = mn_b;
-      float sum_a = 0.f, sum_b = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        sc[nt][0] = fast_exp2(sc[nt][0] - mu_a);
-        sc[nt][1] = fast_exp2(sc[nt][1] - mu_a);
-        sc[nt][2] = fast_exp2(sc[nt][2] - mu_b);
-        sc[nt][3] = fast_exp2(sc[nt][3] - mu_b);
-        sum_a += sc[nt][0] + sc[nt][1];
-        sum_b += sc[nt][2] + sc[nt][3];
-      }
-      l_a = l_a * al_a + sum_a;
-      l_b = l_b * al_b + sum_b;
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        o[nt][0] *= al_a;
-        o[nt][1] *= al_a;
-        o[nt][2] *= al_b;
-        o[nt][3] *= al_b;
-      }
-      // ---- O += P V, one 16-token k-step per sub-tile
-#pragma unroll
-      for (int sub = 0; sub < NSUB; ++sub) {
-        uint32_t ph[4], pl[4];
-        const float* c0 = sc[2 * sub];
-        const float* c1 = sc[2 * sub + 1];
-        ph[0] = pack_bf16x2(c0[0], c0[1]);
-        ph[1] = pack_bf16x2(c0[2], c0[3]);
-        ph[2] = pack_bf16x2(c1[0], c1[1]);
-        ph[3] = pack_bf16x2(c1[2], c1[3]);
-        pl[0] = pack_bf16x2(c0[0] - bf16lo_to_f32(ph[0]), c0[1] - bf16hi_to_f32(ph[0]));
-        pl[1] = pack_bf16x2(c0[2] - bf16lo_to_f32(ph[1]), c0[3] - bf16hi_to_f32(ph[1]));
-        pl[2] = pack_bf16x2(c1[0] - bf16lo_to_f32(ph[2]), c1[1] - bf16hi_to_f32(ph[2]));
-        pl[3] = pack_bf16x2(c1[2] - bf16lo_to_f32(ph[3]), c1[3] - bf16hi_to_f32(ph[3]));
-        const uint32_t vt = base + sub * L::STAGEB + L::TILEB;
-#pragma unroll
-        for (int dp = 0; dp < KS; ++dp) {
-          uint32_t R[4];
-          ldsm_x4_trans(vt + L::off(tok_v, 2 * dp + ch_v), R);
-          mma_bf16_16816(o[2 * dp], ph, R[0], R[1]);
-          mma_bf16_16816(o[2 * dp], pl, R[0], R[1]);
-          mma_bf16_16816(o[2 * dp + 1], ph, R[2], R[3]);
-          mma_bf16_16816(o[2 * dp + 1], pl, R[2], R[3]);
-        }
-      }
-    }
-    // ---- release the stage; thread 0 refills it once all four warps are done
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(empty + s));
-    if (threadIdx.x == 0 && healthy && k + NS < ntile) {
-      if (mbar_wait(smem_u32(empty + s), par, p.err)) issue(k + NS);
-    }
-    __syncwarp();
-  }
-  if (!healthy && threadIdx.x == 0) {
-    for (int s = 0; s < NS && s < ntile; ++s) {
-      const int klast = s + ((ntile - 1 - s) / NS) * NS;
-      mbar_wait(smem_u32(full + s), static_cast<uint32_t>((klast / NS) & 1), nullptr);
-    }
-  }
-  allow_next_grid();
-
-  // ---- row sums over the 4 lanes of each row; write this range's piece
-  l_a += __shfl_xor_sync(kFull, l_a, 1);
-  l_a += __shfl_xor_sync(kFull, l_a, 2);
-  l_b += __shfl_xor_sync(kFull, l_b, 1);
-  l_b += __shfl_xor_sync(kFull, l_b, 2);
-  const int64_t S_row = p.slots_per_row;
-  const int slot = p.extra_slot + ps;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int rr = half ? rb : ra;
-    if (rr >= rows) continue;
-    const int64_t orow = static_cast<int64_t>(rr / G) * p.num_q_heads + h * G + rr % G;
-    const int64_t piece = orow * S_row + slot;
-    float* dst = p.ws_o + piece * D;
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt)
-      *reinterpret_cast<float2*>(dst + 8 * nt + 2 * j) =
-          half ? make_float2(o[nt][2], o[nt][3]) : make_float2(o[nt][0], o[nt][1]);
-    if (j == 0) {
-      p.ws_ml[piece * 2] = half ? m_b : m_a;
-      p.ws_ml[piece * 2 + 1] = half ? l_b : l_a;
-    }
-  }
-}
-
-// ----------------------------------------------------------------------------
-// Cascade prefix kernel on the 5th-generation tensor cores (tcgen05 + TMEM).
-// Same contract as the mma.sync version above, 128 query rows per CTA, one row
-// per thread (= one TMEM lane):
-//   TMEM columns   [0, D/2)   Q rows, bf16 pairs (A operand of S = Q K^T)
-//                  [64, 128)  S (fp32), then P = 2^(s - m) as bf16 hi | lo
-//                             (A operand of O += P V; P aliases S)
-//                  [128, 128 + D)  O (fp32 accumulator)
-//   shared memory  3 stages of 64-token K and V tiles, TMA-loaded with the
-//                  128-byte swizzle: K read as a K-major B operand, V as an
-//                  MN-major B operand, through sm_100 matrix descriptors.
-// Thread 0 issues the MMAs and commits them to mbarriers; every thread reads
-// its S row, keeps a lazy running max (O in TMEM is rescaled only when the
-// max grows by more than 2^8, so P stays <= 256) and writes its P row back.
-// ----------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128, 2)
-    cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  using L = Layout<D, false>;
-  constexpr int M = 128;
-  constexpr int NKEY = kCascadeTile;
-  constexpr int NSUB = NKEY / kTileTokens;
-  constexpr int HALVES = D / 64;                 // 128-byte d-halves of a row
-  constexpr int HALF_BYTES = NKEY * 128;         // one d-half of a 64-key tile
-  constexpr int KREG = HALVES * HALF_BYTES;      // K (or V) tile
-  constexpr int STAGE = 2 * KREG;
-  constexpr int NS = 3;
-  constexpr int kMaxPrefixBlocks = 1024;
-  constexpr uint32_t TCOLS = 256;
-  constexpr uint32_t COL_Q = 0, COL_S = 64, COL_PHI = 64, COL_PLO = 96, COL_O = 128;
-  constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
-  constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
-  static_assert(D == 64 || D == 128, "head_dim");
-
-  const int warp = threadIdx.x >> 5;
-  const int h = blockIdx.y, ps = blockIdx.z;
-  const int G = p.group;
-  const int rows = p.batch * G;
-  const int row = blockIdx.x * M + threadIdx.x;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
-  uint64_t* bar_s = full + NS;
-  uint64_t* bar_pv = bar_s + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_pv + 1);
-  int* s_blk = reinterpret_cast<int*>(s_tmem + 2);
-  const uint32_t stage0 = smem_u32(smem);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(full + s), 1);
-    mbar_init(smem_u32(bar_s), 1);
-    mbar_init(smem_u32(bar_pv), 1);
-    fence_mbar_init();
-    prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_v);
-  }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(s_tmem), TCOLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *s_tmem;
-  const uint32_t tlane = tbase + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
-
-  wait_prior_grid();
-  const int t0 = ps * p.prefix_split_tokens;
-  const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
-  const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
-  for (int i = threadIdx.x; i < nblk && i < kMaxPrefixBlocks; i += blockDim.x) {
-    int phys = p.prefix_blocks[t0 / p.block_size + i];
-    if (phys < 0 || phys >= p.num_blocks) {
-      record_error(p.err, kDevErrBlockId);
-      phys = -1;
-    }
-    s_blk[i] = phys;
-  }
-  __syncthreads();
-  const int ntile = (t1 - t0 + NKEY - 1) / NKEY;
-
-  auto issue = [&](int k) {  // thread 0: tile k -> stage k % NS, laid out [K|V][d-half][key][128 B]
-    const int s = k % NS;
-    const uint32_t dst = stage0 + s * STAGE;
-    const uint32_t bar = smem_u32(full + s);
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int i = 0; i < NSUB; ++i) {
-      const int t = t0 + k * NKEY + i * kTileTokens;
-      const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;   // past the end: zeros
-      const int tok0 = t % p.block_size;
-#pragma unroll
-      for (int bx = 0; bx < HALVES; ++bx) {
-        const uint32_t off = bx * HALF_BYTES + i * kTileTokens * 128;
-        tma_load_4d(dst + off, &tmap_k, bar, bx * L::BOX_ELEMS, tok0, h, phys);
-        tma_load_4d(dst + KREG + off, &tmap_v, bar, bx * L::BOX_ELEMS, tok0, h, phys);
-      }
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int k = 0; k < ntile && k < NS; ++k) issue(k);
-
-  // ---- this thread's query row into TMEM (zeros for padding rows)
-  {
-    const uint16_t* q = static_cast<const uint16_t*>(p.q);
-    const uint16_t* qr = row < rows ? q + (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) * D
-                                    : nullptr;
-#pragma unroll
-    for (int c0 = 0; c0 < D / 2; c0 += 16) {
-      uint32_t v[16];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 w = qr ? *reinterpret_cast<const uint4*>(qr + 2 * c0 + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * i] = w.x;
-        v[4 * i + 1] = w.y;
-        v[4 * i + 2] = w.z;
-        v[4 * i + 3] = w.w;
-      }
-      tmem_st16(tlane + COL_Q + c0, v);
-    }
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  __syncthreads();
-
-  const float qk_mult = p.qk_log2_scale;
-  float m_used = -CUDART_INF_F, lsum = 0.f;
-  bool healthy = true;
-  int k = 0;
-  for (; k < ntile; ++k) {
-    const int s = k % NS;
-    const uint32_t kbase = stage0 + s * STAGE, vbase = kbase + KREG;
-    // ---- S = Q K^T, issued by thread 0 once the tile has landed and the
-    // previous tile's P.V has completed: S shares TMEM columns with the P that
-    // P.V reads, and tcgen05 orders MMAs only on the same accumulator.  When
-    // bar_s flips, O is stable, P may be overwritten and the previous stage
-    // is free.
-    bool ok = true;
-    if (threadIdx.x == 0) {
-      ok = mbar_wait(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err);
-      if (ok && k > 0) ok = mbar_wait(smem_u32(bar_pv), static_cast<uint32_t>((k - 1) & 1), p.err);
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t kd = smem_desc_sw128(kbase + (ks / 4) * HALF_BYTES + (ks % 4) * 32, 0, 1024);
-          tc_mma_ts(tbase + COL_S, tbase + COL_Q + ks * 8, kd, IDESC_S, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(smem_u32(bar_s));
-      }
-    }
-    if (!__syncthreads_and(ok)) {
-      healthy = false;
-      break;
-    }
-    if (!mbar_wait(smem_u32(bar_s), static_cast<uint32_t>(k & 1), p.err)) ok = false;
-    tc_fence_after();
-    if (threadIdx.x == 0 && ok && k > 0 && k - 1 + NS < ntile) issue(k - 1 + NS);
-    float x[NKEY];
-    {
-      uint32_t v[NKEY / 16][16];
-#pragma unroll
-      for (int c = 0; c < NKEY / 16; ++c) tmem_ld16(tlane + COL_S + 16 * c, v[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < NKEY / 16; ++c)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]);
-    }
-    const int valid = t1 - (t0 + k * NKEY);
-    float mt = -CUDART_INF_F;
-#pragma unroll
-    for (int i = 0; i < NKEY; ++i) {
-      x[i] = i < valid ? x[i] * qk_mult : -CUDART_INF_F;
-      mt = fmaxf(mt, x[i]);
-    }
-    float alpha = 1.f;
-    bool resc = false;
-    if (k == 0) {
-      m_used = mt;
-    } else if (mt > m_used + 8.f) {
-      alpha = fast_exp2(m_used - mt);
-      m_used = mt;
-      resc = true;
-    }
-    if (__any_sync(kFull, resc)) {
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[2][16];
-        tmem_ld16(tlane + COL_O + c0, v[0]);
-        tmem_ld16(tlane + COL_O + c0 + 16, v[1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[hh][i] = __float_as_uint(__uint_as_float(v[hh][i]) * alpha);
-        tmem_st16(tlane + COL_O + c0, v[0]);
-        tmem_st16(tlane + COL_O + c0 + 16, v[1]);
-      }
-    }
-    lsum *= alpha;
-#pragma unroll
-    for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p0 = fast_exp2(x[2 * (c0 + i)] - m_used);
-        const float p1 = fast_exp2(x[2 * (c0 + i) + 1] - m_used);
-        lsum += p0 + p1;
-        hi[i] = pack_bf16x2(p0, p1);
-        lo[i] = pack_bf16x2(p0 - bf16lo_to_f32(hi[i]), p1 - bf16hi_to_f32(hi[i]));
-      }
-      tmem_st16(tlane + COL_PHI + c0, hi);
-      tmem_st16(tlane + COL_PLO + c0, lo);
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    if (!__syncthreads_and(ok)) {
-      healthy = false;
-      break;
-    }
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < NKEY / 16; ++kk) {
-        // MN-major V: 8-key groups 1024 B apart, the two 64-wide d-halves
-        // HALF_BYTES apart (a single half for D = 64)
-        const uint64_t vd = smem_desc_sw128(vbase + kk * 2048, HALVES > 1 ? HALF_BYTES : 0, 1024);
-        tc_mma_ts(tbase + COL_O, tbase + COL_PHI + kk * 8, vd, IDESC_PV, (k > 0 || kk > 0) ? 1u : 0u);
-        tc_mma_ts(tbase + COL_O, tbase + COL_PLO + kk * 8, vd, IDESC_PV, 1u);
-      }
-      tc_commit(smem_u32(bar_pv));
-    }
-  }
-  if (healthy && ntile > 0) {
-    const bool pv_done = mbar_wait(smem_u32(bar_pv), static_cast<uint32_t>((ntile - 1) & 1), p.err);
-    healthy = __syncthreads_and(pv_done);
-  }
-  if (healthy && ntile > 0) {
-    tc_fence_after();
-    const int64_t S_row = p.slots_per_row;
-    const int64_t piece = (row < rows ? (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) : 0) *
-                              S_row + p.extra_slot + ps;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t v[2][16];
-      tmem_ld16(tlane + COL_O + c0, v[0]);
-      tmem_ld16(tlane + COL_O + c0 + 16, v[1]);
-      tmem_wait_ld();
-      if (row < rows) {
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + piece * D + c0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]), __uint_as_float(v[i / 4][4 * (i % 4) + 1]),
-                               __uint_as_float(v[i / 4][4 * (i % 4) + 2]), __uint_as_float(v[i / 4][4 * (i % 4) + 3]));
-      }
-    }
-    if (row < rows) {
-      p.ws_ml[piece * 2] = m_used;
-      p.ws_ml[piece * 2 + 1] = lsum;
-    }
-  } else if (!healthy && threadIdx.x == 0) {
-    // let whatever is still in flight land before the memory is released
-    for (int s = 0; s < NS && s < ntile; ++s) mbar_wait(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), nullptr);
-    mbar_wait(smem_u32(bar_s), static_cast<uint32_t>(k & 1), nullptr);
-    if (k > 0) mbar_wait(smem_u32(bar_pv), static_cast<uint32_t>((k - 1) & 1), nullptr);
-  }
-  allow_next_grid();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tbase, TCOLS);
-  }
-}
-
 // Persistent-grid shape of the stream-K kernel per (D, dtype): warps per CTA,
 // pipeline stages per warp, CTAs per SM.
 template <int D, bool FP8>
@@ -1617,25 +1044,6 @@ int streamk_smem_bytes_t(int batch) {
   using L = Layout<D, FP8>;
   using Shape = StreamKShape<D, FP8>;
   return Shape::NW * Shape::NS * L::STAGEB + Shape::NW * Shape::NS * 8 + 4 * (batch + 1) + 1024;
-}
-
-// Launch with programmatic dependent launch allowed: the kernel may be
-// scheduled while its predecessor in the stream drains; it waits for the
-// predecessor's completion (griddepcontrol.wait) before touching its data.
-template <class... KArgs, class... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t stream,
-                       Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 template <int D, bool FP8, int NT>
@@ -1723,38 +1131,6 @@ cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tk, co
                           : launch_split_t<64, true, 2>(p, tk, tv, stream);
   return nt == 1 ? launch_split_t<64, false, 1>(p, tk, tv, stream)
                  : launch_split_t<64, false, 2>(p, tk, tv, stream);
-}
-
-int cascade_smem_bytes(int head_dim) {
-  const int stage = (kCascadeTile / kTileTokens) * 2 * kTileTokens * head_dim * 2;
-  return 3 * stage + 6 * 8 + 1024 * 4 + 1024;
-}
-
-template <int D>
-cudaError_t launch_cascade_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                             cudaStream_t stream) {
-  auto kern = cascade_prefix_tc_kernel<D>;
-  const int smem = cascade_smem_bytes(D);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  static bool configured[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  const int rows = p.batch * p.group;
-  const int nps = (p.prefix_len + p.prefix_split_tokens - 1) / p.prefix_split_tokens;
-  const dim3 grid((rows + kCascadeRowsTc - 1) / kCascadeRowsTc, p.num_kv_heads, nps);
-  return launch_pdl(kern, grid, dim3(128), smem, stream, tk, tv, p);
-}
-
-cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                  cudaStream_t stream) {
-  if (p.head_dim == 128) return launch_cascade_t<128>(p, tk, tv, stream);
-  return launch_cascade_t<64>(p, tk, tv, stream);
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {

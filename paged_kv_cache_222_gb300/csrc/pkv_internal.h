@@ -19,7 +19,14 @@ constexpr int kTileTokens = 16;
 // Consumer warps per decode CTA.
 constexpr int kDecodeWarps = 4;
 
-enum KernelKind { kKindAppend = 0, kKindDecodeSplit = 1, kKindCombine = 2, kKindCascadePrefix = 3 };
+enum KernelKind {
+  kKindAppend = 0,
+  kKindDecodeSplit = 1,
+  kKindCombine = 2,
+  kKindCascadePrefix = 3,
+  kKindBlockCopy = 4,
+  kNumKernelKinds = 8  // room for later kinds; the trace aggregates by kind
+};
 
 // Decode work split: balanced stream-K ranges over the flattened
 // (sequence, head, tile) space, or fixed `split_tokens` chunks per sequence.
@@ -86,7 +93,27 @@ struct DecodeParams {
   int* err;
 };
 
+// Whole-block copies between (or within) block pools: pair i copies block
+// src[i] of the K and V caches to block dst[i].
+struct CopyParams {
+  const void* k_src;      // K cache the sources live in
+  const void* v_src;
+  void* k_dst;            // K cache the destinations live in
+  void* v_dst;
+  const int32_t* src;     // [n_pairs] source block ids
+  const int32_t* dst;     // [n_pairs] destination block ids
+  int64_t n_pairs;
+  int64_t block_vec;      // 16-byte words per block of one cache
+  int64_t src_blocks;     // valid source ids: [0, src_blocks)
+  int64_t dst_blocks;     // valid destination ids: [0, dst_blocks)
+  int* err;
+};
+
+// Message returned by pkv_last_error() on this host thread.
+void set_last_error(const char* msg);
+
 // Launchers (return the launch's cudaError_t; nothing is synchronised).
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tmap_k,
                                 const CUtensorMap& tmap_v, cudaStream_t stream);

@@ -1,4 +1,4 @@
-"""C-ABI library: loads, exports what include/pkv.h declares, and rejects bad
+"""C-ABI library: loads, exports what include/*.h declare, and rejects bad
 arguments on the host before touching the GPU (CPU only, no compute calls)."""
 
 import ctypes
@@ -22,9 +22,14 @@ def lib():
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_documented_entry_points():
@@ -43,10 +48,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.pkv_abi_version() == 101
+    assert lib.pkv_abi_version() == 102
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(1) == b"PKV_ERR_INVALID_ARG"
     assert lib.pkv_status_string(4) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(5) == b"PKV_ERR_OUT_OF_BLOCKS"
     assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
 
 
@@ -229,3 +235,23 @@ def test_cascade_plan_shapes(lib):
 def test_cascade_plan_rejects(lib, desc_kw, prefix, max_ctx, code):
     st, _ = _cplan(lib, _desc(**desc_kw), 4, 64, prefix, max_ctx)
     assert st == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_pairs=-1), L.PKV_ERR_INVALID_ARG),
+    (dict(src=None), L.PKV_ERR_INVALID_ARG),
+    (dict(cache_ptr=8), L.PKV_ERR_INVALID_ARG),
+    (dict(desc=dict(block_size=8)), L.PKV_ERR_UNSUPPORTED),
+])
+def test_copy_blocks_rejects_bad_arguments_on_host(lib, kw, code):
+    desc = _desc(**kw.get("desc", {}))
+    cp = ctypes.c_void_p(kw.get("cache_ptr", 256))
+    src = None if "src" in kw else ctypes.c_void_p(1024)
+    st = lib.pkv_copy_blocks(cp, cp, ctypes.byref(desc), src, ctypes.c_void_p(2048),
+                             kw.get("n_pairs", 4), None)
+    assert st == code
+
+
+def test_copy_of_no_pairs_is_a_noop(lib):
+    desc = _desc()
+    assert lib.pkv_copy_blocks(None, None, ctypes.byref(desc), None, None, 0, None) == L.PKV_OK
