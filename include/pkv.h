@@ -267,6 +267,46 @@ pkv_status pkv_cascade_decode_attention(const void* q, int32_t batch, int32_t nu
                                         void* workspace, size_t workspace_bytes,
                                         pkv_stream_t stream);
 
+/*
+ * Multi-token query attention — q_len new tokens per sequence attend the
+ * sequence's paged K/V causally: the chunk of a chunked prefill that runs
+ * next to decode steps ([SC] "9. Failure modes and limitations", item 3,
+ * Chunked Prefill) or the tokens a draft model proposed, verified in one
+ * parallel pass ([SC] "7. Practical applications", item 3, Speculative
+ * Decoding).
+ *
+ *   q              bf16 [batch, q_len, num_q_heads, head_dim], 16-byte aligned;
+ *                  1 <= q_len <= 16.
+ *   context_lens   int32 [batch]: tokens of sequence b, its q_len new tokens
+ *                  included (they must already be appended).  Query i sits at
+ *                  position context_lens[b] - q_len + i and attends tokens
+ *                  0 .. that position; a query before position 0 (a context
+ *                  shorter than q_len) gives zeros.
+ *   out            float32 [batch, q_len, num_q_heads, head_dim].
+ *   split_tokens   0 = automatic, else tokens per split: a multiple of 64, at
+ *                  most 1024 * block_size.
+ *   workspace      device scratch of at least plan.workspace_bytes from
+ *                  pkv_multi_query_plan with the same arguments (256-byte
+ *                  aligned; may be NULL when that is 0).
+ *   Other arguments as pkv_decode_attention; bf16 caches only (E4M3:
+ *   PKV_ERR_UNSUPPORTED).  q_len = 1 computes decode attention.
+ *
+ * pkv_multi_query_plan (host only): mode 3; split_tokens / max_splits as for
+ * decode, workers = warps per CTA that share each 16 query rows (4, 2 or 1).
+ */
+pkv_status pkv_multi_query_plan(int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                const pkv_cache_desc* cache, int32_t max_context_len,
+                                int32_t split_tokens, int32_t num_sms, pkv_decode_plan_t* plan);
+
+pkv_status pkv_multi_query_attention(const void* q, int32_t batch, int32_t q_len,
+                                     int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                     const pkv_cache_desc* cache,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t max_context_len,
+                                     float scale, float* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t split_tokens, pkv_stream_t stream);
+
 /* Device error codes (first one recorded wins). */
 enum {
   PKV_DEVERR_NONE = 0,
@@ -298,7 +338,7 @@ int32_t pkv_abi_version(void);
  * pkv_trace_read synchronises those events and returns, per kernel kind,
  * the number of launches and their summed device time; it then clears the
  * buffer.  Kinds: 0 append, 1 decode split, 2 combine, 3 cascade prefix,
- * 4 block copy.
+ * 4 block copy, 5 multi-token query.
  */
 typedef struct {
   int32_t kind;

@@ -23,10 +23,12 @@ from ._lib import (PKV_BF16, PKV_E4M3, PKV_F32, CacheDesc, DecodePlan, PkvError,
                    TraceEntry)
 
 __all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slots_for_positions",
-           "cascade_plan", "cascade_decode_attention", "BlockManager", "OutOfBlocks", "copy_blocks",
+           "cascade_plan", "cascade_decode_attention", "multi_query_plan", "multi_query_attention",
+           "BlockManager", "OutOfBlocks", "copy_blocks",
            "device_error", "trace_enable", "trace_read", "library", "PkvError"]
 
-KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix", 4: "block_copy"}
+KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix", 4: "block_copy",
+                5: "multi_query"}
 
 
 def library():
@@ -237,6 +239,48 @@ def cascade_decode_attention(q, k_cache, v_cache, prefix_blocks, prefix_len, blo
         int(max_context_len), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
         _stream(dev))
     _lib.check(st, "pkv_cascade_decode_attention")
+    return out
+
+
+def multi_query_plan(batch, q_len, num_q_heads, k_cache_or_desc, max_context_len, split_tokens=0,
+                     num_sms=0):
+    desc = k_cache_or_desc if isinstance(k_cache_or_desc, CacheDesc) else cache_desc(k_cache_or_desc)
+    plan = DecodePlan()
+    _lib.check(library().pkv_multi_query_plan(batch, q_len, num_q_heads, ctypes.byref(desc), max_context_len,
+                                              split_tokens, num_sms, ctypes.byref(plan)),
+               "pkv_multi_query_plan")
+    return plan
+
+
+def multi_query_attention(q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                          split_tokens=0, out=None, workspace=None):
+    """q_len new tokens per sequence attending causally: q [B, q_len, H_q, D]
+    bf16, context_lens counting the new tokens; returns out [B, q_len, H_q, D]
+    float32."""
+    _check_pair(k_cache, v_cache)
+    dev = k_cache.device
+    if q.dim() != 4:
+        raise ValueError("q must be [B, q_len, H_q, D]")
+    B, ql, hq, d = q.shape
+    _contig(q, torch.bfloat16, "q", dev)
+    _contig(block_tables, torch.int32, "block_tables", dev)
+    _contig(context_lens, torch.int32, "context_lens", dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    desc = cache_desc(k_cache)
+    if out is None:
+        out = torch.empty((B, ql, hq, d), dtype=torch.float32, device=dev)
+    _contig(out, torch.float32, "out", dev)
+    with torch.cuda.device(dev):
+        plan = multi_query_plan(B, ql, hq, desc, int(max_context_len), split_tokens,
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
+        if plan.workspace_bytes > 0 and (workspace is None or workspace.numel() < plan.workspace_bytes):
+            workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        _lib.check(library().pkv_multi_query_attention(
+            _ptr(q), B, ql, hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+            _ptr(workspace), workspace.numel() if workspace is not None else 0, split_tokens,
+            _stream(dev)), "pkv_multi_query_attention")
     return out
 
 

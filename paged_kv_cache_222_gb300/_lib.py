@@ -61,6 +61,10 @@ SIGNATURES = {
                                 ctypes.POINTER(DecodePlan)]),
     "pkv_cascade_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
                                             _P, _I32, _P, _I32, _F, _P, _P, ctypes.c_size_t, _P]),
+    "pkv_multi_query_plan": (_I32, [_I32, _I32, _I32, ctypes.POINTER(CacheDesc), _I32, _I32, _I32,
+                                    ctypes.POINTER(DecodePlan)]),
+    "pkv_multi_query_attention": (_I32, [_P, _I32, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
+                                         _P, _I32, _F, _P, _P, ctypes.c_size_t, _I32, _P]),
     "pkv_copy_blocks": (_I32, [_P, _P, ctypes.POINTER(CacheDesc), _P, _P, _I32, _P]),
     "pkv_bm_create": (_I32, [_I64, _I32, ctypes.POINTER(_P)]),
     "pkv_bm_destroy": (None, [_P]),

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libpkv.so")
 
-SOURCES = ["api.cu", "append.cu", "decode.cu", "cascade.cu", "blocks.cu", "block_manager.cpp"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "cascade.cu", "multi_query.cu", "blocks.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

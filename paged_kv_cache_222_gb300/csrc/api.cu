@@ -740,6 +740,139 @@ extern "C" pkv_status pkv_cascade_decode_attention(
 }
 
 // ---------------------------------------------------------------------------
+// Multi-token query attention (q_len new tokens per sequence, causal).
+// ---------------------------------------------------------------------------
+
+namespace {
+
+pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_cache_desc* c,
+                   int32_t max_ctx, int32_t split_tokens, int32_t sms, pkv_decode_plan_t* out) {
+  pkv_status s = check_cache(c);
+  if (s != PKV_OK) return s;
+  if (c->dtype != PKV_BF16) return fail(PKV_ERR_UNSUPPORTED, "multi-token attention takes bf16 caches");
+  if (batch < 0 || batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch %d", batch);
+  if (q_len < 1 || q_len > 16) return fail(PKV_ERR_UNSUPPORTED, "q_len %d (1..16)", q_len);
+  if (num_q_heads < 1 || num_q_heads % c->num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads,
+                c->num_kv_heads);
+  if (num_q_heads / c->num_kv_heads > 16)
+    return fail(PKV_ERR_UNSUPPORTED, "group size %d > 16", num_q_heads / c->num_kv_heads);
+  if (max_ctx < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d", max_ctx);
+  const int64_t max_st = static_cast<int64_t>(pkv::kMultiQueryMaxSplitBlocks) * c->block_size;
+  if (split_tokens < 0 || (split_tokens > 0 && (split_tokens % pkv::kMultiQueryTile != 0 || split_tokens > max_st)))
+    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (0, or a multiple of 64 up to %lld)", split_tokens,
+                static_cast<long long>(max_st));
+  if (sms <= 0) sms = kDefaultSms;
+  const int32_t rows = q_len * (num_q_heads / c->num_kv_heads);
+  const int32_t lanes = pkv::multi_query_lanes(rows);
+  const int64_t nrb = ceil_div(rows, 16 * (4 / lanes));
+  const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * nrb;
+  int32_t st = split_tokens;
+  if (st == 0) {
+    // largest power of two (256..4096) that still gives about four waves of
+    // two CTAs per SM when every sequence is as long as the bound
+    const int64_t want = static_cast<int64_t>(sms) * 2 * 4;
+    st = 4096;
+    while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
+  }
+  const int64_t splits = max_ctx > 0 ? ceil_div(max_ctx, st) : 1;
+  if (splits > 0x7FFFFFFFll) return fail(PKV_ERR_INVALID_ARG, "too many splits");
+  if (static_cast<int64_t>(c->num_kv_heads) * nrb > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads x row blocks beyond the grid");
+  *out = pkv_decode_plan_t{};
+  out->mode = 3;
+  out->split_tokens = st;
+  out->max_splits = static_cast<int32_t>(splits);
+  out->workers = lanes;
+  if (splits > 1) {
+    const int64_t n = static_cast<int64_t>(batch) * q_len * num_q_heads * splits;
+    out->workspace_bytes = align256(n * c->head_dim * 4) + n * 2 * 4;
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_multi_query_plan(int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                           const pkv_cache_desc* cache, int32_t max_context_len,
+                                           int32_t split_tokens, int32_t num_sms, pkv_decode_plan_t* plan) {
+  if (plan == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan output is NULL");
+  return mq_plan(batch, q_len, num_q_heads, cache, max_context_len, split_tokens, num_sms, plan);
+}
+
+extern "C" pkv_status pkv_multi_query_attention(
+    const void* q, int32_t batch, int32_t q_len, int32_t num_q_heads, const void* k_cache,
+    const void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len, float scale,
+    float* out, void* workspace, size_t workspace_bytes, int32_t split_tokens, pkv_stream_t stream) {
+  DecodeArgs a = {q, batch, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                  context_lens, max_context_len, scale, out, nullptr, nullptr, 0};
+  pkv_status s = check_decode(a);
+  if (s != PKV_OK) return s;
+  pkv_decode_plan_t pl;
+  s = mq_plan(batch, q_len, num_q_heads, cache, max_context_len, split_tokens, kDefaultSms, &pl);
+  if (s != PKV_OK) return s;
+  if (batch == 0) return PKV_OK;
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  if (split_tokens == 0) {
+    s = mq_plan(batch, q_len, num_q_heads, cache, max_context_len, 0, st->sms, &pl);
+    if (s != PKV_OK) return s;
+  }
+  if (pl.workspace_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < static_cast<size_t>(pl.workspace_bytes))
+      return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes, need %lld", workspace_bytes,
+                  static_cast<long long>(pl.workspace_bytes));
+    if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  const pkv_cache_desc& c = *cache;
+  CUtensorMap tk, tv;
+  s = make_cache_tmap(&tk, k_cache, c);
+  if (s != PKV_OK) return s;
+  s = make_cache_tmap(&tv, v_cache, c);
+  if (s != PKV_OK) return s;
+  const int64_t n = static_cast<int64_t>(batch) * q_len * num_q_heads * pl.max_splits;
+  DecodeParams p = {};
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_ml = pl.workspace_bytes > 0
+                ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(n * c.head_dim * 4))
+                : nullptr;
+  p.num_blocks = c.num_blocks;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.group = num_q_heads / c.num_kv_heads;
+  p.head_dim = c.head_dim;
+  p.block_size = c.block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_ctx = max_context_len;
+  p.split_tokens = pl.split_tokens;
+  p.max_splits = pl.max_splits;
+  p.qk_log2_scale = scale * 1.4426950408889634f;
+  p.cache_dtype = c.dtype;
+  p.mode = pkv::kModeFixedSplit;
+  p.extra_slot = -1;
+  p.slots_per_row = pl.max_splits;
+  p.q_len = q_len;
+  p.err = st->err;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(pkv::kKindMultiQuery, cs, [&] { return pkv::launch_multi_query(p, tk, tv, cs); });
+  if (e == cudaSuccess && pl.max_splits > 1) {
+    DecodeParams pc = p;            // rows (b, i, hq) flatten to b * (q_len * H_q) + i * H_q + hq
+    pc.num_q_heads = q_len * num_q_heads;
+    e = traced(pkv::kKindCombine, cs, [&] { return pkv::launch_decode_combine(pc, cs); });
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------------------------
 // Decode attention that allocates nothing.
 //
 // The split-KV partials live in a fixed array in device memory that belongs to

@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(128) combine_rows_kernel(const DecodeParams p)
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] += w * x[u][v];
   }
-  const float inv = 1.f / L;
+  const float inv = L > 0.f ? 1.f / L : 0.f;  // a row with nothing to attend gives zeros
   float* dst = p.out + row * D + lane * V;
   if constexpr (V == 4) {
     *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
     wt[w] = (s_ml[w][0] == -CUDART_INF_F) ? 0.f : fast_exp2(s_ml[w][0] - Mt);
     Lt += wt[w] * s_ml[w][1];
   }
-  const float inv = 1.f / Lt;
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
   for (int d = threadIdx.x; d < D; d += blockDim.x)
     p.out[row * D + d] =
         (wt[0] * s_acc[0][d] + wt[1] * s_acc[1][d] + wt[2] * s_acc[2][d] + wt[3] * s_acc[3][d]) * inv;

@@ -25,6 +25,7 @@ enum KernelKind {
   kKindCombine = 2,
   kKindCascadePrefix = 3,
   kKindBlockCopy = 4,
+  kKindMultiQuery = 5,
   kNumKernelKinds = 8  // room for later kinds; the trace aggregates by kind
 };
 
@@ -90,6 +91,8 @@ struct DecodeParams {
   const int32_t* prefix_blocks;  // [prefix_len / block_size] physical blocks
   int32_t prefix_len;
   int32_t prefix_split_tokens;   // prefix tokens per prefix CTA (multiple of 64)
+  // multi-token queries: q_len new tokens per sequence (1 for decode)
+  int32_t q_len;
   int* err;
 };
 
@@ -120,6 +123,17 @@ cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tmap_k
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tmap_k,
                                   const CUtensorMap& tmap_v, cudaStream_t stream);
+cudaError_t launch_multi_query(const DecodeParams& p, const CUtensorMap& tmap_k,
+                               const CUtensorMap& tmap_v, cudaStream_t stream);
+
+// Multi-token query kernel: 64-token tiles, rows of (query token, head) pairs
+// in 16-row warp groups; the block ids of one split staged in shared memory.
+constexpr int kMultiQueryTile = 64;
+constexpr int kMultiQueryMaxSplitBlocks = 1024;
+// Dynamic shared memory of the multi-token query kernel.
+int multi_query_smem_bytes(int head_dim);
+// Token lanes (warps sharing the same 16 rows) for R rows per (sequence, head).
+inline int multi_query_lanes(int rows) { return rows <= 16 ? 4 : (rows <= 32 ? 2 : 1); }
 
 // Rows of query heads one cascade prefix CTA covers: 4 warps x 16 (mma.sync
 // kernel), one TMEM lane per thread (tcgen05 kernel).

@@ -255,3 +255,38 @@ def test_copy_blocks_rejects_bad_arguments_on_host(lib, kw, code):
 def test_copy_of_no_pairs_is_a_noop(lib):
     desc = _desc()
     assert lib.pkv_copy_blocks(None, None, ctypes.byref(desc), None, None, 0, None) == L.PKV_OK
+
+
+def _mqplan(lib, desc, batch, q_len, hq, max_ctx, st=0, sms=152):
+    p = L.DecodePlan()
+    r = lib.pkv_multi_query_plan(batch, q_len, hq, ctypes.byref(desc), max_ctx, st, sms, ctypes.byref(p))
+    return r, p
+
+
+def test_multi_query_plan_shapes(lib):
+    desc = _desc()
+    r, p = _mqplan(lib, desc, 64, 4, 64, 8192)
+    assert r == L.PKV_OK and p.mode == 3 and p.workers == 2          # 32 rows: two lanes
+    assert p.split_tokens % 64 == 0 and p.max_splits == -(-8192 // p.split_tokens)
+    n = 64 * 4 * 64 * p.max_splits
+    assert p.workspace_bytes == -(-n * 128 * 4 // 256) * 256 + n * 8
+    r, p = _mqplan(lib, desc, 2, 16, 64, 100, st=128)
+    assert r == L.PKV_OK and p.workers == 1 and p.max_splits == 1 and p.workspace_bytes == 0
+    r, p = _mqplan(lib, desc, 2, 2, 64, 100)
+    assert r == L.PKV_OK and p.workers == 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q_len=0), L.PKV_ERR_UNSUPPORTED),
+    (dict(q_len=17), L.PKV_ERR_UNSUPPORTED),
+    (dict(st=100), L.PKV_ERR_INVALID_ARG),
+    (dict(st=16 * 1024 + 64), L.PKV_ERR_INVALID_ARG),
+    (dict(max_ctx=-1), L.PKV_ERR_INVALID_ARG),
+    (dict(desc=dict(dtype=L.PKV_E4M3)), L.PKV_ERR_UNSUPPORTED),
+    (dict(hq=60), L.PKV_ERR_INVALID_ARG),
+])
+def test_multi_query_plan_rejects(lib, kw, code):
+    desc = _desc(**kw.get("desc", {}))
+    r, _ = _mqplan(lib, desc, 4, kw.get("q_len", 4), kw.get("hq", 64), kw.get("max_ctx", 1000),
+                   st=kw.get("st", 0))
+    assert r == code

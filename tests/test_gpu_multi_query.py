@@ -1,0 +1,153 @@
+"""GPU parity of multi-token (causal) query attention against the oracle:
+small ragged cases over every warp arrangement and split size, the edge cases
+(contexts shorter than q_len, empty contexts, q_len = 1), and sampled units
+of the full-size GQA workload with four new tokens per sequence appended
+through the library first."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_222_gb300 as pkv
+import workloads as W
+from oracle import paged_attention as PA
+
+from .gpu_support import BF16_NAN, bits16
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def _small_case(ctxs, q_len, H_q, H_kv, D, bs, seed):
+    """Paged bf16 caches holding each sequence's ctx tokens (new ones included),
+    tables over a shuffled pool, NaN in every slot no sequence holds."""
+    gen = torch.Generator().manual_seed(seed)
+    B = len(ctxs)
+    nblk = [-(-c // bs) for c in ctxs]
+    mb = max(max(nblk), 1)
+    pool = sum(nblk) + 5
+    perm = torch.randperm(pool, generator=gen).tolist()
+    table = np.full((B, mb), -1, dtype=np.int32)
+    k = 0
+    for b in range(B):
+        table[b, :nblk[b]] = perm[k:k + nblk[b]]
+        k += nblk[b]
+    kc = torch.randn((pool, H_kv, bs, D), generator=gen).to(torch.bfloat16)
+    vc = torch.randn((pool, H_kv, bs, D), generator=gen).to(torch.bfloat16)
+    kb, vb = kc.view(torch.int16), vc.view(torch.int16)
+    used = np.zeros(pool, dtype=bool)
+    for b in range(B):
+        used[table[b, :nblk[b]]] = True
+        for pos in range(ctxs[b], nblk[b] * bs):
+            blk = int(table[b, pos // bs])
+            kb[blk, :, pos % bs] = BF16_NAN
+            vb[blk, :, pos % bs] = BF16_NAN
+    for blk in np.nonzero(~used)[0]:
+        kb[int(blk)] = BF16_NAN
+        vb[int(blk)] = BF16_NAN
+    q = torch.randn((B, q_len, H_q, D), generator=gen).to(torch.bfloat16)
+    return dict(kc=kc, vc=vc, table=table, ctx=np.array(ctxs, dtype=np.int32), q=q, scale=D ** -0.5)
+
+
+def _run(case, split_tokens=0):
+    lens = torch.from_numpy(case["ctx"]).to(DEV)
+    out = pkv.multi_query_attention(case["q"].to(DEV), case["kc"].to(DEV), case["vc"].to(DEV),
+                                    torch.from_numpy(case["table"]).to(DEV), lens, case["scale"],
+                                    max_context_len=max(int(case["ctx"].max()), 1),
+                                    split_tokens=split_tokens)
+    assert pkv.device_error(DEV) == 0
+    return out.cpu().numpy()
+
+
+def _oracle(case):
+    return PA.multi_query_attention(bits16(case["q"]), bits16(case["kc"]), bits16(case["vc"]), PA.BF16,
+                                    case["table"], case["ctx"], case["scale"])
+
+
+@pytest.mark.parametrize("q_len,H_q,H_kv,D,bs", [
+    (1, 8, 1, 128, 16),     # 8 rows: four token lanes
+    (2, 8, 1, 128, 16),     # 16 rows
+    (3, 10, 2, 64, 16),     # 15 rows, G = 5
+    (4, 8, 1, 128, 32),     # 32 rows: two lanes
+    (8, 4, 1, 64, 32),      # 32 rows
+    (6, 8, 1, 128, 16),     # 48 rows: one lane, one partial row block
+    (16, 8, 2, 128, 16),    # 128 rows: two row blocks per head
+    (16, 16, 1, 64, 16),    # 256 rows
+])
+@pytest.mark.parametrize("split_tokens", [0, 64, 192])
+def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, bs, split_tokens):
+    ctxs = [q_len, 17 + q_len, 64, 65, 300, 1000 + q_len]
+    case = _small_case(ctxs, q_len, H_q, H_kv, D, bs, seed=20260200 + q_len * 7 + D + split_tokens)
+    out = _run(case, split_tokens)
+    want = _oracle(case)
+    assert np.isfinite(out).all()
+    assert np.abs(out - want).max() <= 2e-3
+
+
+def test_short_and_empty_contexts_give_zeros_for_unplaced_queries():
+    q_len = 8
+    case = _small_case([0, 3, 8, 9], q_len, 8, 2, 128, 16, seed=20260301)
+    for st in (0, 64):
+        out = _run(case, st)
+        want = _oracle(case)
+        assert np.isfinite(out).all()
+        assert np.all(out[0] == 0.0) and np.all(out[1, :5] == 0.0)
+        assert np.abs(out - want).max() <= 2e-3
+
+
+def test_single_query_equals_decode():
+    case = _small_case([1, 40, 700, 2049], 1, 16, 2, 128, 16, seed=20260302)
+    out = _run(case)
+    lens = torch.from_numpy(case["ctx"]).to(DEV)
+    dec = pkv.decode_attention(case["q"][:, 0].contiguous().to(DEV), case["kc"].to(DEV), case["vc"].to(DEV),
+                               torch.from_numpy(case["table"]).to(DEV), lens, case["scale"],
+                               max_context_len=2049)
+    assert np.abs(out[:, 0] - dec.cpu().numpy()).max() <= 1e-4
+
+
+def test_split_count_does_not_change_the_result():
+    case = _small_case([5000, 333, 4096], 4, 32, 4, 128, 16, seed=20260303)
+    outs = [_run(case, st) for st in (64, 256, 1024, 4096, 16384)]
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 1e-5
+
+
+@pytest.mark.parametrize("q_len", [4, 16])
+def test_full_size_gqa_workload_sampled(q_len):
+    """B=64, H_q=64, H_kv=8, D=128, bs=16, contexts U[512, 8192]: the q_len
+    new tokens of every sequence are appended by pkv.append, then attended
+    causally; 24 sampled (sequence, KV head) units are checked."""
+    case = W.make_case("gqa_bf16", device=DEV, steps=q_len)
+    B, bs, G = case["B"], case["bs"], case["H_q"] // case["H_kv"]
+    rng = np.random.default_rng(q_len)
+    units = [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 24), rng.integers(0, case["H_kv"], 24))]
+    bt = case["block_tables"].to(DEV)
+    snap = {}
+    for b, h in units:
+        n = case["blocks_needed"][b]
+        ids = case["block_tables"][b, :n].to(torch.int64).to(DEV)
+        snap[(b, h)] = (bits16(case["k_cache"][ids][:, h:h + 1]), bits16(case["v_cache"][ids][:, h:h + 1]))
+    ctx = case["ctx"].to(DEV).to(torch.int64)
+    for s in range(q_len):
+        slots = pkv.slots_for_positions(bt, torch.arange(B, device=DEV), ctx + s, bs)
+        pkv.append(case["k_new"][s].contiguous(), case["v_new"][s].contiguous(), slots,
+                   case["k_cache"], case["v_cache"])
+    lens = (ctx + q_len).to(torch.int32)
+    q = case["q"].permute(1, 0, 2, 3).contiguous()                          # [B, q_len, H_q, D]
+    out = pkv.multi_query_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"],
+                                    max_context_len=int(lens.max()))
+    assert pkv.device_error(DEV) == 0
+    out = out.cpu().numpy()
+    for b, h in units:
+        n = case["blocks_needed"][b]
+        kc, vc = (a.copy() for a in snap[(b, h)])
+        table = np.arange(n, dtype=np.int32)[None, :]
+        c0 = int(case["ctx"][b])
+        for s in range(q_len):
+            slot = np.array([PA.slot_of(table[0], c0 + s, bs)])
+            kc, vc = PA.append(bits16(case["k_new"][s, b, h:h + 1])[None], bits16(case["v_new"][s, b, h:h + 1])[None],
+                               PA.BF16, slot, kc, vc, PA.BF16)
+        qq = bits16(q[b:b + 1, :, h * G:(h + 1) * G])
+        want = PA.multi_query_attention(qq, kc, vc, PA.BF16, table, np.array([c0 + q_len]), case["scale"])
+        got = out[b, :, h * G:(h + 1) * G]
+        assert np.abs(got - want[0]).max() <= 2e-3, (b, h)
