@@ -119,6 +119,85 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
                            const int32_t* src_blocks, const int32_t* dst_blocks,
                            int32_t n_pairs, pkv_stream_t stream);
 
+/* ------------------------------------------------------------ host tier
+ *
+ * A second pool of blocks in host memory, for swapping preempted sequences
+ * out of HBM ([SC] "9. Failure modes and limitations", item 2, Swap to CPU)
+ * and for moving single blocks between the tiers ([UI] "Architecting
+ * Multi-Tier Disaggregated KV-Cache Hierarchies...", "C++ Block Scheduler
+ * and Asynchronous Fetch Kernel": promote a block from Tier-2 host memory to
+ * Tier-1 HBM, demote it back; "Tier-1 / Tier-2 Double Buffering": fetch the
+ * blocks needed a few steps ahead while the current step runs).
+ *
+ * Every table entry is either a device block id or a host block id.  A
+ * sequence with any host entry cannot be appended to, forked or attended
+ * (pkv_bm_append / pkv_bm_fork / pkv_bm_block_tables return
+ * PKV_ERR_INVALID_ARG) until its entries are staged back.  Host blocks are
+ * never shared: demoting a shared device block gives this sequence its own
+ * host copy and drops one device reference.
+ */
+
+/* Give the manager a host pool of num_host_blocks (once).  The host free
+ * pool is a stack like the device one (block num_host_blocks - 1 first). */
+pkv_status pkv_bm_set_host_blocks(pkv_block_manager* bm, int64_t num_host_blocks);
+int64_t pkv_bm_num_free_host(pkv_block_manager* bm);
+/* Host entries of a sequence; -1 for an unknown sequence. */
+int64_t pkv_bm_host_entries(pkv_block_manager* bm, int64_t seq_id);
+
+/*
+ * Demote (evict) / promote (stage) entries `logical[0..n)` of a sequence
+ * (distinct indices inside its table).  Entries already in the target tier
+ * are skipped.  The (from, to) block pairs to copy are written to the two
+ * arrays (n entries suffice) and their count to *n_pairs; copy them with
+ * pkv_copy_blocks_between before the freed blocks are reused.  All or
+ * nothing: PKV_ERR_OUT_OF_BLOCKS when the target pool is short.
+ */
+pkv_status pkv_bm_evict(pkv_block_manager* bm, int64_t seq_id, int32_t n, const int32_t* logical,
+                        int32_t* dev_src, int32_t* host_dst, int32_t* n_pairs);
+pkv_status pkv_bm_stage(pkv_block_manager* bm, int64_t seq_id, int32_t n, const int32_t* logical,
+                        int32_t* host_src, int32_t* dev_dst, int32_t* n_pairs);
+
+/* The raw table of a sequence: ids[j] and on_host[j] (0 / 1) for each entry. */
+pkv_status pkv_bm_table_entries(pkv_block_manager* bm, int64_t seq_id, int32_t capacity,
+                                int32_t* ids, int32_t* on_host, int32_t* n_entries);
+
+/*
+ * Salience-driven eviction candidates ([UI] "Predictive Prefetching and
+ * Attention-Salience Eviction Policy"): the device entries j of a sequence
+ * with salience[j] < threshold, excluding logical block 0 (it holds the sink
+ * tokens, positions < 4) and every block holding one of the last
+ * `local_window` tokens; ordered by salience, ties by index.
+ *   salience  float [entries of the sequence], host memory.
+ */
+pkv_status pkv_bm_eviction_candidates(pkv_block_manager* bm, int64_t seq_id, const float* salience,
+                                      float threshold, int32_t local_window, int32_t capacity,
+                                      int32_t* logical, int32_t* n_out);
+
+/*
+ * pkv_copy_blocks_between — pair i copies block src_blocks[i] of the source
+ * pool (src_k, src_v; src_num_blocks blocks) to block dst_blocks[i] of the
+ * destination pool; both pools have the block geometry and dtype of `cache`
+ * (its num_blocks is not used).  Pools and id arrays may be device memory or
+ * host memory the GPU can address (pinned with pkv_host_alloc): one kernel
+ * moves every block of the call through the GPU's own loads and stores.
+ * Ids outside a pool are recorded (PKV_DEVERR_BLOCK_ID) and skipped.
+ *   max_ctas  upper bound on the copy's thread blocks; 0 = automatic: 64
+ *             when a pool is in host memory, else no bound.  A copy across
+ *             the host link saturates the link with a few dozen; bounding it
+ *             leaves the other SMs to attention kernels running at the same
+ *             time on other streams.
+ */
+pkv_status pkv_copy_blocks_between(const void* src_k, const void* src_v, int64_t src_num_blocks,
+                                   void* dst_k, void* dst_v, int64_t dst_num_blocks,
+                                   const pkv_cache_desc* cache, const int32_t* src_blocks,
+                                   const int32_t* dst_blocks, int32_t n_pairs, int32_t max_ctas,
+                                   pkv_stream_t stream);
+
+/* Page-locked host memory mapped into the GPU's address space (the same
+ * pointer works on host and device); pkv_host_free releases it. */
+pkv_status pkv_host_alloc(size_t bytes, void** ptr);
+pkv_status pkv_host_free(void* ptr);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,8 +42,29 @@ Readings where the pages leave a step open (also listed in the design notes):
 5. One append call over several sequences is all or nothing: if the pool
    runs out anywhere in it, the call fails with nothing changed.
 
-The model mutates plain Python lists and dicts; it is the specification the
-native block manager is compared against operation by operation.
+Host tier (swap / stage / evict), from [UI] "Architecting Multi-Tier
+Disaggregated KV-Cache Hierarchies...", "C++ Block Scheduler and Asynchronous
+Fetch Kernel" (promote a block from host memory to HBM, demote it back; an
+already resident block is left alone, a pinned one is never demoted) and
+"Predictive Prefetching and Attention-Salience Eviction Policy" (sink blocks
+and the local recency window stay in HBM; other blocks whose salience is below
+a threshold are demoted), and [SC] "9. Failure modes and limitations", item 2
+(swap a preempted request's blocks to host memory):
+
+6. A second pool of host blocks with its own free stack (same order rule).
+   Every table entry is (tier, id).  Evicting entry j of a sequence takes a
+   host block, reports (device id, host id) for the copy and drops the
+   sequence's reference to the device block (freed when it was the last).
+   Staging takes a device block, reports (host id, device id) and frees the
+   host block.  Both are all or nothing over the entries of one call;
+   entries already in the target tier are skipped.
+7. A sequence with any host entry cannot be appended to, forked or attended
+   (its block table is not handed out) until it is staged back.
+8. Pinned entries for the salience policy: logical block 0 (it holds the
+   sink tokens, positions < 4) and every block that holds a position in the
+   last `local_window` tokens.  Candidates for eviction are the other device
+   entries whose salience is below the threshold, lowest salience first (ties
+   by logical index).
 """
 
 import copy
@@ -54,7 +75,7 @@ class OutOfBlocks(Exception):
 
 
 class BlockManagerModel:
-    def __init__(self, num_blocks, block_size):
+    def __init__(self, num_blocks, block_size, num_host_blocks=0):
         if num_blocks < 1 or block_size < 1:
             raise ValueError("num_blocks and block_size must be positive")
         self.block_size = block_size
@@ -62,6 +83,8 @@ class BlockManagerModel:
         self.free = list(range(num_blocks))   # top of the stack = end of list
         self.tables = {}                      # seq_id -> [physical block ids]
         self.lens = {}                        # seq_id -> tokens held
+        self.host_free = list(range(num_host_blocks))
+        self.on_host = {}                     # seq_id -> set of logical indices held on the host
 
     # -------------------------------------------------------------- queries
     @property
@@ -93,21 +116,93 @@ class BlockManagerModel:
             raise KeyError(f"sequence {seq_id} exists")
         self.tables[seq_id] = []
         self.lens[seq_id] = 0
+        self.on_host[seq_id] = set()
+
+    def _resident(self, seq_id):
+        if self.on_host[seq_id]:
+            raise KeyError(f"sequence {seq_id} has blocks on the host")
 
     def fork(self, parent, child):
         if parent not in self.tables or child in self.tables:
             raise KeyError("fork needs an existing parent and a new child")
+        self._resident(parent)
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
+        self.on_host[child] = set()
         for b in self.tables[child]:
             self.ref[b] += 1
 
     def free_sequence(self, seq_id):
-        for b in self.tables.pop(seq_id):
+        host = self.on_host.pop(seq_id)
+        for j, b in enumerate(self.tables.pop(seq_id)):
+            if j in host:
+                self.host_free.append(b)
+                continue
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 self.free.append(b)
         del self.lens[seq_id]
+
+    # ------------------------------------------------------------ host tier
+    def evict(self, seq_id, logical):
+        """Demote entries `logical` of a sequence; returns [(device, host)]."""
+        tbl, host = self.tables[seq_id], self.on_host[seq_id]
+        logical = list(logical)
+        if len(set(logical)) != len(logical) or any(not 0 <= j < len(tbl) for j in logical):
+            raise KeyError("bad logical block list")
+        todo = [j for j in logical if j not in host]
+        if len(todo) > len(self.host_free):
+            raise OutOfBlocks("host pool exhausted")
+        pairs = []
+        for j in todo:
+            hb = self.host_free.pop()
+            d = tbl[j]
+            pairs.append((d, hb))
+            self.ref[d] -= 1
+            if self.ref[d] == 0:
+                self.free.append(d)
+            tbl[j] = hb
+            host.add(j)
+        return pairs
+
+    def stage(self, seq_id, logical):
+        """Promote entries `logical` of a sequence; returns [(host, device)]."""
+        tbl, host = self.tables[seq_id], self.on_host[seq_id]
+        logical = list(logical)
+        if len(set(logical)) != len(logical) or any(not 0 <= j < len(tbl) for j in logical):
+            raise KeyError("bad logical block list")
+        todo = [j for j in logical if j in host]
+        if len(todo) > len(self.free):
+            raise OutOfBlocks("device pool exhausted")
+        pairs = []
+        for j in todo:
+            d = self._take()
+            hb = tbl[j]
+            pairs.append((hb, d))
+            self.host_free.append(hb)
+            tbl[j] = d
+            host.discard(j)
+        return pairs
+
+    def swap_out(self, seq_id):
+        return self.evict(seq_id, range(len(self.tables[seq_id])))
+
+    def swap_in(self, seq_id):
+        return self.stage(seq_id, range(len(self.tables[seq_id])))
+
+    def pinned(self, seq_id, local_window):
+        n, bs, L = len(self.tables[seq_id]), self.block_size, self.lens[seq_id]
+        pin = {0} if n else set()
+        if local_window > 0:                  # blocks holding positions L-W .. L-1
+            pin |= set(range(max(L - local_window, 0) // bs, n))
+        return pin
+
+    def eviction_candidates(self, seq_id, salience, threshold, local_window):
+        pin = self.pinned(seq_id, local_window)
+        host = self.on_host[seq_id]
+        c = [j for j in range(len(self.tables[seq_id]))
+             if j not in pin and j not in host and salience[j] < threshold]
+        return sorted(c, key=lambda j: (salience[j], j))
 
     def _append_one(self, seq_id, n_new, slots, cows):
         bs = self.block_size
@@ -137,6 +232,7 @@ class BlockManagerModel:
         for s in seq_ids:
             if s not in self.tables:
                 raise KeyError(f"unknown sequence {s}")
+            self._resident(s)
         saved = (copy.deepcopy(self.ref), list(self.free), copy.deepcopy(self.tables),
                  dict(self.lens))
         slots, cows = [], []
@@ -152,6 +248,7 @@ class BlockManagerModel:
         """[n, max_blocks] table rows (-1 past each sequence's blocks) and lengths."""
         rows, lens = [], []
         for s in seq_ids:
+            self._resident(s)
             t = self.tables[s]
             if len(t) > max_blocks:
                 raise ValueError("table longer than max_blocks")
@@ -163,7 +260,8 @@ class BlockManagerModel:
         """Everything observable, for comparisons."""
         return {"ref": list(self.ref), "free": list(self.free),
                 "tables": {k: list(v) for k, v in self.tables.items()},
-                "lens": dict(self.lens)}
+                "lens": dict(self.lens), "host_free": list(self.host_free),
+                "on_host": {k: sorted(v) for k, v in self.on_host.items()}}
 
 
 def copy_blocks(cache, pairs):

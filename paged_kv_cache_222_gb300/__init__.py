@@ -25,6 +25,7 @@ from ._lib import (PKV_BF16, PKV_E4M3, PKV_F32, CacheDesc, DecodePlan, PkvError,
 __all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slots_for_positions",
            "cascade_plan", "cascade_decode_attention", "multi_query_plan", "multi_query_attention",
            "BlockManager", "OutOfBlocks", "copy_blocks",
+           "host_pool_like", "copy_blocks_between",
            "device_error", "trace_enable", "trace_read", "library", "PkvError"]
 
 KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix", 4: "block_copy",
@@ -400,6 +401,57 @@ class BlockManager:
                   "pkv_bm_append")
         return slots, np.stack([src[:nc.value], dst[:nc.value]], axis=1)
 
+    # ---- host tier
+    def set_host_blocks(self, num_host_blocks):
+        _bm_check(library().pkv_bm_set_host_blocks(self._h, int(num_host_blocks)), "pkv_bm_set_host_blocks")
+
+    def num_free_host(self):
+        return library().pkv_bm_num_free_host(self._h)
+
+    def host_entries(self, seq_id):
+        return library().pkv_bm_host_entries(self._h, int(seq_id))
+
+    def table_entries(self, seq_id):
+        """(ids int32 [n], on_host int32 [n]) of a sequence's table."""
+        cap = max(self.num_blocks, 1) + 1
+        ids = np.empty(cap, dtype=np.int32)
+        host = np.empty(cap, dtype=np.int32)
+        n = ctypes.c_int32()
+        _bm_check(library().pkv_bm_table_entries(self._h, int(seq_id), cap, _np_ptr(ids), _np_ptr(host),
+                                                 ctypes.byref(n)), "pkv_bm_table_entries")
+        return ids[:n.value].copy(), host[:n.value].copy()
+
+    def _move(self, fn, name, seq_id, logical):
+        lg = np.ascontiguousarray(logical, dtype=np.int32)
+        a = np.empty(max(len(lg), 1), dtype=np.int32)
+        b = np.empty(max(len(lg), 1), dtype=np.int32)
+        n = ctypes.c_int32()
+        _bm_check(fn(self._h, int(seq_id), len(lg), _np_ptr(lg), _np_ptr(a), _np_ptr(b), ctypes.byref(n)), name)
+        return np.stack([a[:n.value], b[:n.value]], axis=1)
+
+    def evict(self, seq_id, logical):
+        """Demote table entries to the host pool; returns (device, host) pairs [k, 2]."""
+        return self._move(library().pkv_bm_evict, "pkv_bm_evict", seq_id, logical)
+
+    def stage(self, seq_id, logical):
+        """Promote table entries to the device pool; returns (host, device) pairs [k, 2]."""
+        return self._move(library().pkv_bm_stage, "pkv_bm_stage", seq_id, logical)
+
+    def swap_out(self, seq_id):
+        return self.evict(seq_id, np.arange(len(self.table_entries(seq_id)[0])))
+
+    def swap_in(self, seq_id):
+        return self.stage(seq_id, np.arange(len(self.table_entries(seq_id)[0])))
+
+    def eviction_candidates(self, seq_id, salience, threshold, local_window):
+        sal = np.ascontiguousarray(salience, dtype=np.float32)
+        out = np.empty(max(len(sal), 1), dtype=np.int32)
+        n = ctypes.c_int32()
+        _bm_check(library().pkv_bm_eviction_candidates(self._h, int(seq_id), _np_ptr(sal), float(threshold),
+                                                       int(local_window), len(out), _np_ptr(out),
+                                                       ctypes.byref(n)), "pkv_bm_eviction_candidates")
+        return out[:n.value].copy()
+
     def block_tables(self, seq_ids, max_blocks_per_seq):
         """(block_tables int32 [n, max_blocks_per_seq] with -1 past each table, lens int32 [n])."""
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
@@ -423,3 +475,33 @@ def copy_blocks(k_cache, v_cache, src_blocks, dst_blocks):
     with torch.cuda.device(dev):
         _lib.check(library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(src),
                                              _ptr(dst), src.numel(), _stream(dev)), "pkv_copy_blocks")
+
+
+def host_pool_like(k_cache, num_blocks):
+    """(k, v) block pools in page-locked host memory with the block geometry
+    and dtype of `k_cache`; the GPU addresses them directly."""
+    shape = (int(num_blocks),) + tuple(k_cache.shape[1:])
+    k = torch.empty(shape, dtype=k_cache.dtype, pin_memory=True)
+    v = torch.empty(shape, dtype=k_cache.dtype, pin_memory=True)
+    return k, v
+
+
+def copy_blocks_between(src_k, src_v, dst_k, dst_v, src_blocks, dst_blocks, max_ctas=0,
+                        stream_device=None):
+    """Block dst_blocks[i] of (dst_k, dst_v) := block src_blocks[i] of (src_k, src_v),
+    through one kernel on the current stream; the pools may live in device or
+    pinned host memory.  max_ctas bounds the SMs the copy occupies (0: no bound)."""
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype:
+        raise ValueError("pools differ in block geometry or dtype")
+    for t in (src_k, src_v, dst_k, dst_v):
+        if not t.is_contiguous() or (t.device.type == "cpu" and not t.is_pinned()):
+            raise ValueError("pools must be contiguous, and pinned when in host memory")
+    dev = stream_device or next(t.device for t in (src_k, dst_k) if t.device.type == "cuda")
+    src = torch.as_tensor(src_blocks, dtype=torch.int32).to(dev).contiguous()
+    dst = torch.as_tensor(dst_blocks, dtype=torch.int32).to(dev).contiguous()
+    desc = cache_desc(src_k)
+    with torch.cuda.device(dev):
+        _lib.check(library().pkv_copy_blocks_between(
+            _ptr(src_k), _ptr(src_v), src_k.shape[0], _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
+            ctypes.byref(desc), _ptr(src), _ptr(dst), src.numel(), int(max_ctas), _stream(dev)),
+            "pkv_copy_blocks_between")

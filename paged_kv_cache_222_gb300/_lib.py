@@ -78,6 +78,17 @@ SIGNATURES = {
     "pkv_bm_append": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _I32, ctypes.POINTER(_I32)]),
     "pkv_bm_blocks_needed": (_I32, [_P, _I32, _P, _P, ctypes.POINTER(_I64)]),
     "pkv_bm_block_tables": (_I32, [_P, _I32, _P, _I32, _P, _P]),
+    "pkv_bm_set_host_blocks": (_I32, [_P, _I64]),
+    "pkv_bm_num_free_host": (_I64, [_P]),
+    "pkv_bm_host_entries": (_I64, [_P, _I64]),
+    "pkv_bm_evict": (_I32, [_P, _I64, _I32, _P, _P, _P, ctypes.POINTER(_I32)]),
+    "pkv_bm_stage": (_I32, [_P, _I64, _I32, _P, _P, _P, ctypes.POINTER(_I32)]),
+    "pkv_bm_table_entries": (_I32, [_P, _I64, _I32, _P, _P, ctypes.POINTER(_I32)]),
+    "pkv_bm_eviction_candidates": (_I32, [_P, _I64, _P, _F, _I32, _I32, _P, ctypes.POINTER(_I32)]),
+    "pkv_copy_blocks_between": (_I32, [_P, _P, _I64, _P, _P, _I64, ctypes.POINTER(CacheDesc), _P, _P, _I32, _I32,
+                                       _P]),
+    "pkv_host_alloc": (_I32, [ctypes.c_size_t, ctypes.POINTER(_P)]),
+    "pkv_host_free": (_I32, [_P]),
     "pkv_get_device_error": (_I32, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_last_error": (ctypes.c_char_p, []),

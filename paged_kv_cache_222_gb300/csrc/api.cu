@@ -22,6 +22,9 @@ using pkv::DecodeParams;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSms = 152;
+// Thread blocks of a block copy that crosses the host link (it reaches the
+// link's bandwidth with about 32 on GB300).
+constexpr int kHostLinkCopyCtas = 64;
 
 thread_local std::string t_last_error;
 
@@ -480,6 +483,78 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = traced(pkv::kKindBlockCopy, cs, [&] { return pkv::launch_copy_blocks(p, cs); });
   if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_copy_blocks_between(const void* src_k, const void* src_v, int64_t src_num_blocks,
+                                   void* dst_k, void* dst_v, int64_t dst_num_blocks,
+                                   const pkv_cache_desc* cache, const int32_t* src_blocks,
+                                   const int32_t* dst_blocks, int32_t n_pairs, int32_t max_ctas,
+                                   pkv_stream_t stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  if (n_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "n_pairs %d", n_pairs);
+  if (max_ctas < 0) return fail(PKV_ERR_INVALID_ARG, "max_ctas %d", max_ctas);
+  if (src_num_blocks < 1 || dst_num_blocks < 1)
+    return fail(PKV_ERR_INVALID_ARG, "pool sizes %lld, %lld", static_cast<long long>(src_num_blocks),
+                static_cast<long long>(dst_num_blocks));
+  if (n_pairs == 0) return PKV_OK;
+  if (src_k == nullptr || src_v == nullptr || dst_k == nullptr || dst_v == nullptr || src_blocks == nullptr ||
+      dst_blocks == nullptr)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) || !aligned(dst_v, 16))
+    return fail(PKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+  if (!aligned(src_blocks, 4) || !aligned(dst_blocks, 4))
+    return fail(PKV_ERR_INVALID_ARG, "block id arrays must be 4-byte aligned");
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  const int64_t esz = cache->dtype == PKV_E4M3 ? 1 : 2;
+  pkv::CopyParams p = {};
+  p.k_src = src_k;
+  p.v_src = src_v;
+  p.k_dst = dst_k;
+  p.v_dst = dst_v;
+  p.src = src_blocks;
+  p.dst = dst_blocks;
+  p.n_pairs = n_pairs;
+  p.block_vec = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim * esz / 16;
+  p.src_blocks = src_num_blocks;
+  p.dst_blocks = dst_num_blocks;
+  if (max_ctas == 0) {
+    // a copy across the host link saturates it with a few dozen CTAs; keep
+    // the other SMs free for attention running beside it
+    bool host_side = false;
+    const void* pools[2] = {src_k, dst_k};
+    for (const void* ptr : pools) {
+      cudaPointerAttributes attr;
+      if (cudaPointerGetAttributes(&attr, ptr) == cudaSuccess && attr.type == cudaMemoryTypeHost) host_side = true;
+    }
+    cudaGetLastError();  // a pointer the runtime does not know is not an error here
+    max_ctas = host_side ? kHostLinkCopyCtas : 0;
+  }
+  p.max_ctas = max_ctas;
+  p.err = st->err;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(pkv::kKindBlockCopy, cs, [&] { return pkv::launch_copy_blocks(p, cs); });
+  if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_host_alloc(size_t bytes, void** ptr) {
+  if (ptr == nullptr) return fail(PKV_ERR_INVALID_ARG, "ptr is NULL");
+  *ptr = nullptr;
+  if (bytes == 0) return fail(PKV_ERR_INVALID_ARG, "zero bytes");
+  cudaError_t e = cudaHostAlloc(ptr, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+  return PKV_OK;
+}
+
+pkv_status pkv_host_free(void* ptr) {
+  if (ptr == nullptr) return PKV_OK;
+  cudaError_t e = cudaFreeHost(ptr);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeHost");
   return PKV_OK;
 }
 

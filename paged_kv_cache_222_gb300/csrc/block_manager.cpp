@@ -16,6 +16,7 @@
 // lookup per sequence.
 
 #include <cstdarg>
+#include <algorithm>
 #include <cstdio>
 #include <limits>
 #include <mutex>
@@ -28,13 +29,17 @@
 
 struct pkv_block_manager {
   struct Seq {
-    std::vector<int32_t> blocks;
+    std::vector<int32_t> blocks;  // device id, or host id where on_host[j]
+    std::vector<uint8_t> on_host;
     int64_t len = 0;
+    int64_t host_entries = 0;
   };
   std::mutex mu;
   int32_t block_size = 0;
   std::vector<int32_t> ref;
   std::vector<int32_t> free_stack;  // top = back()
+  bool host_tier = false;
+  std::vector<int32_t> host_free;   // host pool, same stack rule
   std::unordered_map<int64_t, Seq> seqs;
 };
 
@@ -94,6 +99,8 @@ pkv_status check_batch(Manager* m, int32_t n_seqs, const int64_t* ids, const int
       return fail(PKV_ERR_INVALID_ARG, "unknown sequence %lld", static_cast<long long>(ids[i]));
     if (!seen.emplace(ids[i], i).second)
       return fail(PKV_ERR_INVALID_ARG, "sequence %lld appears twice", static_cast<long long>(ids[i]));
+    if (it->second.host_entries != 0)
+      return fail(PKV_ERR_INVALID_ARG, "sequence %lld has blocks on the host", static_cast<long long>(ids[i]));
     out[static_cast<size_t>(i)] = &it->second;
   }
   return PKV_OK;
@@ -170,6 +177,8 @@ pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_i
     return fail(PKV_ERR_INVALID_ARG, "unknown parent %lld", static_cast<long long>(parent_id));
   if (bm->seqs.count(child_id) != 0)
     return fail(PKV_ERR_INVALID_ARG, "sequence %lld exists", static_cast<long long>(child_id));
+  if (p->second.host_entries != 0)
+    return fail(PKV_ERR_INVALID_ARG, "parent %lld has blocks on the host", static_cast<long long>(parent_id));
   Manager::Seq child = p->second;  // copy before the map may rehash
   for (int32_t b : child.blocks) bm->ref[static_cast<size_t>(b)] += 1;
   bm->seqs.emplace(child_id, std::move(child));
@@ -182,7 +191,13 @@ pkv_status pkv_bm_free_sequence(pkv_block_manager* bm, int64_t seq_id) {
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end())
     return fail(PKV_ERR_INVALID_ARG, "unknown sequence %lld", static_cast<long long>(seq_id));
-  for (int32_t b : it->second.blocks) {
+  const Manager::Seq& sq = it->second;
+  for (size_t j = 0; j < sq.blocks.size(); ++j) {
+    const int32_t b = sq.blocks[j];
+    if (sq.on_host[j]) {
+      bm->host_free.push_back(b);
+      continue;
+    }
     int32_t& r = bm->ref[static_cast<size_t>(b)];
     r -= 1;
     if (r == 0) bm->free_stack.push_back(b);
@@ -243,6 +258,7 @@ pkv_status pkv_bm_append(pkv_block_manager* bm, int32_t n_seqs, const int64_t* s
       const size_t lb = static_cast<size_t>(pos / bs);
       if (pos % bs == 0) {
         sq.blocks.push_back(take(*bm));
+        sq.on_host.push_back(0);
       } else {
         const int32_t last = sq.blocks[lb];
         if (bm->ref[static_cast<size_t>(last)] > 1) {
@@ -280,6 +296,9 @@ pkv_status pkv_bm_block_tables(pkv_block_manager* bm, int32_t n_seqs, const int6
                   static_cast<long long>(seq_ids[i]), it->second.blocks.size(), max_blocks_per_seq);
     if (it->second.len > std::numeric_limits<int32_t>::max())
       return fail(PKV_ERR_INVALID_ARG, "sequence length beyond int32");
+    if (it->second.host_entries != 0)
+      return fail(PKV_ERR_INVALID_ARG, "sequence %lld has blocks on the host",
+                  static_cast<long long>(seq_ids[i]));
   }
   for (int32_t i = 0; i < n_seqs; ++i) {
     const Manager::Seq& sq = bm->seqs.find(seq_ids[i])->second;
@@ -289,6 +308,165 @@ pkv_status pkv_bm_block_tables(pkv_block_manager* bm, int32_t n_seqs, const int6
       row[j] = j < n ? sq.blocks[j] : -1;
     if (context_lens != nullptr) context_lens[i] = static_cast<int32_t>(sq.len);
   }
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------ host tier
+
+namespace {
+
+// Logical indices of one call: distinct and inside the table.
+pkv_status check_logical(const Manager::Seq& sq, int32_t n, const int32_t* logical) {
+  if (n < 0 || (n > 0 && logical == nullptr)) return fail(PKV_ERR_INVALID_ARG, "bad logical list");
+  std::vector<uint8_t> seen(sq.blocks.size(), 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t j = logical[i];
+    if (j < 0 || static_cast<size_t>(j) >= sq.blocks.size())
+      return fail(PKV_ERR_INVALID_ARG, "logical block %d outside the table (%zu)", j, sq.blocks.size());
+    if (seen[static_cast<size_t>(j)]) return fail(PKV_ERR_INVALID_ARG, "logical block %d repeated", j);
+    seen[static_cast<size_t>(j)] = 1;
+  }
+  return PKV_OK;
+}
+
+pkv_status find_seq(Manager* bm, int64_t seq_id, Manager::Seq** out) {
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return fail(PKV_ERR_INVALID_ARG, "unknown sequence %lld", static_cast<long long>(seq_id));
+  *out = &it->second;
+  return PKV_OK;
+}
+
+// Demote (to_host) or promote entries; pairs are (from id, to id).
+pkv_status move_entries(Manager* bm, Manager::Seq& sq, int32_t n, const int32_t* logical, bool to_host,
+                        int32_t* from, int32_t* to, int32_t* n_pairs) {
+  if (!bm->host_tier) return fail(PKV_ERR_INVALID_ARG, "no host tier (pkv_bm_set_host_blocks)");
+  if (n_pairs == nullptr) return fail(PKV_ERR_INVALID_ARG, "n_pairs is NULL");
+  pkv_status s = check_logical(sq, n, logical);
+  if (s != PKV_OK) return s;
+  int64_t todo = 0;
+  for (int32_t i = 0; i < n; ++i) todo += (sq.on_host[static_cast<size_t>(logical[i])] != 0) != to_host;
+  if (todo > 0 && (from == nullptr || to == nullptr)) return fail(PKV_ERR_INVALID_ARG, "NULL pair arrays");
+  const size_t avail = to_host ? bm->host_free.size() : bm->free_stack.size();
+  if (todo > static_cast<int64_t>(avail))
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "%s pool: %lld blocks needed, %zu free", to_host ? "host" : "device",
+                static_cast<long long>(todo), avail);
+  int32_t k = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const size_t j = static_cast<size_t>(logical[i]);
+    if ((sq.on_host[j] != 0) == to_host) continue;  // already in the target tier
+    const int32_t old = sq.blocks[j];
+    int32_t nb;
+    if (to_host) {
+      nb = bm->host_free.back();
+      bm->host_free.pop_back();
+      int32_t& r = bm->ref[static_cast<size_t>(old)];
+      r -= 1;
+      if (r == 0) bm->free_stack.push_back(old);
+      sq.host_entries += 1;
+    } else {
+      nb = take(*bm);
+      bm->host_free.push_back(old);
+      sq.host_entries -= 1;
+    }
+    from[k] = old;
+    to[k] = nb;
+    ++k;
+    sq.blocks[j] = nb;
+    sq.on_host[j] = to_host ? 1 : 0;
+  }
+  *n_pairs = k;
+  return PKV_OK;
+}
+
+}  // namespace
+
+pkv_status pkv_bm_set_host_blocks(pkv_block_manager* bm, int64_t num_host_blocks) {
+  if (bm == nullptr) return fail(PKV_ERR_INVALID_ARG, "manager is NULL");
+  if (num_host_blocks < 1 || num_host_blocks > std::numeric_limits<int32_t>::max())
+    return fail(PKV_ERR_INVALID_ARG, "num_host_blocks %lld", static_cast<long long>(num_host_blocks));
+  std::lock_guard<std::mutex> lk(bm->mu);
+  if (bm->host_tier) return fail(PKV_ERR_INVALID_ARG, "host tier already set");
+  bm->host_free.resize(static_cast<size_t>(num_host_blocks));
+  for (int64_t i = 0; i < num_host_blocks; ++i) bm->host_free[static_cast<size_t>(i)] = static_cast<int32_t>(i);
+  bm->host_tier = true;
+  return PKV_OK;
+}
+
+int64_t pkv_bm_num_free_host(pkv_block_manager* bm) {
+  if (bm == nullptr) return -1;
+  std::lock_guard<std::mutex> lk(bm->mu);
+  return static_cast<int64_t>(bm->host_free.size());
+}
+
+int64_t pkv_bm_host_entries(pkv_block_manager* bm, int64_t seq_id) {
+  if (bm == nullptr) return -1;
+  std::lock_guard<std::mutex> lk(bm->mu);
+  auto it = bm->seqs.find(seq_id);
+  return it == bm->seqs.end() ? -1 : it->second.host_entries;
+}
+
+pkv_status pkv_bm_evict(pkv_block_manager* bm, int64_t seq_id, int32_t n, const int32_t* logical,
+                        int32_t* dev_src, int32_t* host_dst, int32_t* n_pairs) {
+  if (bm == nullptr) return fail(PKV_ERR_INVALID_ARG, "manager is NULL");
+  std::lock_guard<std::mutex> lk(bm->mu);
+  Manager::Seq* sq;
+  pkv_status s = find_seq(bm, seq_id, &sq);
+  if (s != PKV_OK) return s;
+  return move_entries(bm, *sq, n, logical, true, dev_src, host_dst, n_pairs);
+}
+
+pkv_status pkv_bm_stage(pkv_block_manager* bm, int64_t seq_id, int32_t n, const int32_t* logical,
+                        int32_t* host_src, int32_t* dev_dst, int32_t* n_pairs) {
+  if (bm == nullptr) return fail(PKV_ERR_INVALID_ARG, "manager is NULL");
+  std::lock_guard<std::mutex> lk(bm->mu);
+  Manager::Seq* sq;
+  pkv_status s = find_seq(bm, seq_id, &sq);
+  if (s != PKV_OK) return s;
+  return move_entries(bm, *sq, n, logical, false, host_src, dev_dst, n_pairs);
+}
+
+pkv_status pkv_bm_table_entries(pkv_block_manager* bm, int64_t seq_id, int32_t capacity, int32_t* ids,
+                                int32_t* on_host, int32_t* n_entries) {
+  if (bm == nullptr || n_entries == nullptr) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  std::lock_guard<std::mutex> lk(bm->mu);
+  Manager::Seq* sq;
+  pkv_status s = find_seq(bm, seq_id, &sq);
+  if (s != PKV_OK) return s;
+  const size_t n = sq->blocks.size();
+  if (static_cast<int64_t>(n) > capacity || (n > 0 && (ids == nullptr || on_host == nullptr)))
+    return fail(PKV_ERR_INVALID_ARG, "table of %zu entries, capacity %d", n, capacity);
+  for (size_t j = 0; j < n; ++j) {
+    ids[j] = sq->blocks[j];
+    on_host[j] = sq->on_host[j];
+  }
+  *n_entries = static_cast<int32_t>(n);
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_eviction_candidates(pkv_block_manager* bm, int64_t seq_id, const float* salience,
+                                      float threshold, int32_t local_window, int32_t capacity,
+                                      int32_t* logical, int32_t* n_out) {
+  if (bm == nullptr || n_out == nullptr) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (local_window < 0) return fail(PKV_ERR_INVALID_ARG, "local_window %d", local_window);
+  std::lock_guard<std::mutex> lk(bm->mu);
+  Manager::Seq* sq;
+  pkv_status s = find_seq(bm, seq_id, &sq);
+  if (s != PKV_OK) return s;
+  const int64_t n = static_cast<int64_t>(sq->blocks.size());
+  if (n > 0 && salience == nullptr) return fail(PKV_ERR_INVALID_ARG, "salience is NULL");
+  // pinned: block 0 (sink tokens) and the blocks of the last local_window tokens
+  const int64_t first_local =
+      local_window > 0 ? (sq->len > local_window ? sq->len - local_window : 0) / bm->block_size : n;
+  std::vector<int32_t> c;
+  for (int64_t j = 1; j < n && j < first_local; ++j) {
+    if (sq->on_host[static_cast<size_t>(j)]) continue;
+    if (salience[j] < threshold) c.push_back(static_cast<int32_t>(j));
+  }
+  std::stable_sort(c.begin(), c.end(), [&](int32_t a, int32_t b) { return salience[a] < salience[b]; });
+  if (static_cast<int64_t>(c.size()) > capacity || (!c.empty() && logical == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "%zu candidates, capacity %d", c.size(), capacity);
+  for (size_t i = 0; i < c.size(); ++i) logical[i] = c[i];
+  *n_out = static_cast<int32_t>(c.size());
   return PKV_OK;
 }
 

@@ -67,7 +67,8 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream) {
   if (words == 0) return cudaSuccess;
   // enough threads for one pass of four words each, at most 8 CTAs per SM
   const int64_t want = (words + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
-  const int blocks = static_cast<int>(want < 152 * 8 ? want : 152 * 8);
+  const int64_t cap = p.max_ctas > 0 ? p.max_ctas : 152 * 8;
+  const int blocks = static_cast<int>(want < cap ? want : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
   cfg.blockDim = dim3(kCopyThreads);

@@ -109,6 +109,7 @@ struct CopyParams {
   int64_t block_vec;      // 16-byte words per block of one cache
   int64_t src_blocks;     // valid source ids: [0, src_blocks)
   int64_t dst_blocks;     // valid destination ids: [0, dst_blocks)
+  int32_t max_ctas;       // grid bound (0: as many as the copy can use)
   int* err;
 };
 

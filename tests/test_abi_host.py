@@ -290,3 +290,20 @@ def test_multi_query_plan_rejects(lib, kw, code):
     r, _ = _mqplan(lib, desc, 4, kw.get("q_len", 4), kw.get("hq", 64), kw.get("max_ctx", 1000),
                    st=kw.get("st", 0))
     assert r == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_pairs=-1), L.PKV_ERR_INVALID_ARG),
+    (dict(max_ctas=-1), L.PKV_ERR_INVALID_ARG),
+    (dict(src_nb=0), L.PKV_ERR_INVALID_ARG),
+    (dict(dst_ptr=8), L.PKV_ERR_INVALID_ARG),
+    (dict(desc=dict(head_dim=96)), L.PKV_ERR_UNSUPPORTED),
+])
+def test_copy_between_pools_rejects_bad_arguments_on_host(lib, kw, code):
+    desc = _desc(**kw.get("desc", {}))
+    sp = ctypes.c_void_p(256)
+    dp = ctypes.c_void_p(kw.get("dst_ptr", 512))
+    st = lib.pkv_copy_blocks_between(sp, sp, kw.get("src_nb", 4), dp, dp, 4, ctypes.byref(desc),
+                                     ctypes.c_void_p(1024), ctypes.c_void_p(2048), kw.get("n_pairs", 2),
+                                     kw.get("max_ctas", 0), None)
+    assert st == code

@@ -143,3 +143,109 @@ def test_large_pool_serving_churn_is_fast():
             nxt += 8
     dt = (time.perf_counter() - t0) / 200
     assert dt < 0.05, f"{dt * 1e3:.2f} ms per step"
+
+
+def _same_tier_state(native, model):
+    assert native.num_free() == model.num_free()
+    assert native.num_free_host() == len(model.host_free)
+    for b in range(model.num_blocks):
+        assert native.ref_count(b) == model.ref_count(b)
+    for s in model.tables:
+        ids, host = native.table_entries(s)
+        assert ids.tolist() == model.table(s)
+        assert [j for j in range(len(host)) if host[j]] == sorted(model.on_host[s])
+        assert native.host_entries(s) == len(model.on_host[s])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_native_host_tier_matches_the_model(seed):
+    rng = random.Random(2000 + seed)
+    nb, nh, bs = rng.choice([8, 32]), rng.choice([4, 24]), rng.choice([4, 16])
+    native = pkv.BlockManager(nb, bs)
+    native.set_host_blocks(nh)
+    model = BlockManagerModel(nb, bs, num_host_blocks=nh)
+    nxt = 0
+    for _ in range(300):
+        live = sorted(model.tables)
+        op = rng.random()
+        if op < 0.15 or not live:
+            native.add_sequence(nxt)
+            model.add_sequence(nxt)
+            nxt += 1
+        elif op < 0.22:
+            s = rng.choice(live)
+            native.free_sequence(s)
+            model.free_sequence(s)
+        elif op < 0.3:
+            s, c = rng.choice(live), nxt
+            if model.on_host[s]:
+                with pytest.raises(pkv.PkvError):
+                    native.fork(s, c)
+                continue
+            native.fork(s, c)
+            model.fork(s, c)
+            nxt += 1
+        elif op < 0.55:
+            s = rng.choice(live)
+            n = len(model.table(s))
+            lg = rng.sample(range(n), rng.randint(0, n)) if n else []
+            evict = rng.random() < 0.5
+            try:
+                want = model.evict(s, lg) if evict else model.stage(s, lg)
+            except OutOfBlocks:
+                want = None
+            fn = native.evict if evict else native.stage
+            if want is None:
+                with pytest.raises(pkv.OutOfBlocks):
+                    fn(s, lg)
+            else:
+                assert [tuple(p) for p in fn(s, lg).tolist()] == want
+        elif op < 0.62:
+            s = rng.choice(live)
+            n = len(model.table(s))
+            sal = [rng.choice([0.0, 0.01, 0.2, 0.5, 0.05]) for _ in range(n)]
+            w = rng.choice([0, 1, bs, 3 * bs])
+            assert native.eviction_candidates(s, sal, 0.1, w).tolist() == \
+                model.eviction_candidates(s, sal, 0.1, w)
+        else:
+            s = rng.choice(live)
+            k = rng.randint(1, 2 * bs)
+            if model.on_host[s]:
+                with pytest.raises(pkv.PkvError):
+                    native.append([s], [k])
+                continue
+            try:
+                want = model.append([s], [k])
+            except OutOfBlocks:
+                want = None
+            if want is None:
+                with pytest.raises(pkv.OutOfBlocks):
+                    native.append([s], [k])
+            else:
+                slots, cows = native.append([s], [k])
+                assert slots.tolist() == want[0] and [tuple(c) for c in cows.tolist()] == want[1]
+        _same_tier_state(native, model)
+
+
+def test_host_tier_rejections():
+    bm = pkv.BlockManager(8, 4)
+    bm.add_sequence(0)
+    bm.append([0], [6])
+    with pytest.raises(pkv.PkvError):
+        bm.evict(0, [0])                      # no host tier yet
+    bm.set_host_blocks(4)
+    with pytest.raises(pkv.PkvError):
+        bm.set_host_blocks(4)                 # once
+    with pytest.raises(pkv.PkvError):
+        bm.evict(0, [2])                      # outside the table
+    with pytest.raises(pkv.PkvError):
+        bm.evict(0, [1, 1])                   # repeated
+    bm.evict(0, [1])
+    with pytest.raises(pkv.PkvError):
+        bm.block_tables([0], 4)               # not resident
+    with pytest.raises(pkv.PkvError):
+        bm.blocks_needed([0], [1])
+    assert bm.stage(0, [0]).shape == (0, 2)   # already on the device: nothing to do
+    bm.stage(0, [1])
+    tbl, lens = bm.block_tables([0], 4)
+    assert lens.tolist() == [6] and bm.num_free_host() == 4

@@ -186,3 +186,136 @@ def test_copy_blocks_reads_the_cache_before_the_call():
     out = copy_blocks(cache, [(1, 4), (2, 5)])
     assert np.array_equal(out[4], cache[1]) and np.array_equal(out[5], cache[2])
     assert np.array_equal(out[:4], cache[:4])
+
+
+# ------------------------------------------------------------ host tier
+
+def test_swap_out_frees_device_blocks_and_swap_in_restores_the_view():
+    m = BlockManagerModel(6, 4, num_host_blocks=5)
+    m.add_sequence(0)
+    m.append([0], [10])                       # device 5, 4, 3
+    pairs = m.swap_out(0)
+    assert pairs == [(5, 4), (4, 3), (3, 2)]  # host stack top first
+    assert m.num_free() == 6 and m.on_host[0] == {0, 1, 2}
+    with pytest.raises(KeyError):
+        m.append([0], [1])                    # not resident
+    with pytest.raises(KeyError):
+        m.block_tables([0], 4)
+    back = m.swap_in(0)
+    assert back == [(4, 3), (3, 4), (2, 5)]   # device stack: 3, 4, 5 were pushed in that order
+    assert m.on_host[0] == set() and m.num_free() == 3
+
+
+def test_evicting_a_shared_block_gives_a_private_host_copy():
+    m = BlockManagerModel(6, 4, num_host_blocks=4)
+    m.add_sequence(0)
+    m.append([0], [8])
+    m.fork(0, 1)
+    pairs = m.evict(1, [0])
+    assert pairs == [(5, 3)] and m.ref_count(5) == 1 and m.table(0) == [5, 4]
+    m.free_sequence(1)
+    assert m.num_free() == 4 and len(m.host_free) == 4
+
+
+def test_tier_moves_are_all_or_nothing():
+    m = BlockManagerModel(4, 4, num_host_blocks=2)
+    m.add_sequence(0)
+    m.append([0], [12])
+    before = m.snapshot()
+    with pytest.raises(OutOfBlocks):
+        m.swap_out(0)                         # 3 blocks, 2 host blocks
+    assert m.snapshot() == before
+    m.evict(0, [1, 2])
+    m.add_sequence(1)
+    m.append([1], [12])                       # takes the 3 freed device blocks
+    with pytest.raises(OutOfBlocks):
+        m.stage(0, [1, 2])
+    assert m.on_host[0] == {1, 2}
+
+
+def test_eviction_candidates_keep_sinks_and_the_local_window():
+    # [UI] "Predictive Prefetching and Attention-Salience Eviction Policy":
+    # blocks with tokens j < 4 are never evicted, nor the local window; the
+    # others go when their salience is under the threshold.
+    m = BlockManagerModel(32, 16)
+    m.add_sequence(0)
+    m.append([0], [16 * 10 + 3])              # 11 blocks, last one partial
+    sal = [0.0, 0.3, 0.01, 0.5, 0.02, 0.02, 0.9, 0.0, 0.0, 0.0, 0.0]
+    got = m.eviction_candidates(0, sal, 0.1, local_window=40)
+    # local window: positions 123..162 -> blocks 7..10
+    assert got == [2, 4, 5]
+    assert m.eviction_candidates(0, sal, 0.1, local_window=0) == [7, 8, 9, 10, 2, 4, 5]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_tier_moves_keep_every_sequence_view(seed):
+    rng = random.Random(100 + seed)
+    bs = rng.choice([2, 4])
+    m = BlockManagerModel(rng.choice([8, 20]), bs, num_host_blocks=rng.choice([4, 16]))
+    dev, host = {}, {}                        # slot -> token id, per tier
+    expect = {}
+    nxt, tok = 0, 0
+
+    def read(s):
+        t = m.table(s)
+        out = []
+        for i in range(m.seq_len(s)):
+            j = i // bs
+            src = host if j in m.on_host[s] else dev
+            out.append(src[t[j] * bs + i % bs])
+        return out
+
+    for _ in range(300):
+        live = list(m.tables)
+        op = rng.random()
+        if op < 0.15 or not live:
+            m.add_sequence(nxt)
+            expect[nxt] = []
+            nxt += 1
+        elif op < 0.25:
+            s = rng.choice(live)
+            m.free_sequence(s)
+            del expect[s]
+        elif op < 0.45:
+            s = rng.choice(live)
+            n = len(m.table(s))
+            lg = rng.sample(range(n), rng.randint(0, n)) if n else []
+            to_host = rng.random() < 0.5
+            try:
+                pairs = m.evict(s, lg) if to_host else m.stage(s, lg)
+            except OutOfBlocks:
+                continue
+            src, dst = (dev, host) if to_host else (host, dev)
+            for a, b in pairs:
+                for o in range(bs):
+                    if a * bs + o in src:
+                        dst[b * bs + o] = src[a * bs + o]
+        else:
+            res = [s for s in live if not m.on_host[s]]
+            if not res:
+                continue
+            s = rng.choice(res)
+            try:
+                slots, cows = m.append([s], [rng.randint(1, 2 * bs)])
+            except OutOfBlocks:
+                continue
+            for a, b in cows:
+                for o in range(bs):
+                    if a * bs + o in dev:
+                        dev[b * bs + o] = dev[a * bs + o]
+            for sl in slots:
+                dev[sl] = tok
+                expect[s].append(tok)
+                tok += 1
+        # invariants: device refs count device entries; host ids distinct
+        used, hused = {}, []
+        for s, t in m.tables.items():
+            for j, b in enumerate(t):
+                if j in m.on_host[s]:
+                    hused.append(b)
+                else:
+                    used[b] = used.get(b, 0) + 1
+        assert all(m.ref_count(b) == used.get(b, 0) for b in range(m.num_blocks))
+        assert sorted(hused + m.host_free) == sorted(set(hused + m.host_free))
+        for s in expect:
+            assert read(s) == expect[s]
