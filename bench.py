@@ -216,7 +216,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("decode.cu", "pkv_device.cuh", "pkv_internal.h"):
+    for name in ("decode.cu", "decode_common.cuh", "pkv_device.cuh", "pkv_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_222_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
