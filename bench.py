@@ -18,6 +18,14 @@ exchange step); value sums the ranks' bytes over the slowest rank's time.
 
 --impl reference times the float64 CPU oracle (the reference of this
 library) on the host cores over a bounded sample of the same workload.
+
+--op cascade | multi_query | block_copy | host_swap times one of the other
+hot-path operations instead of the decode step (one JSON line with "op"):
+cascade decode on the shared-prefix workload (prefix kernel against the bf16
+tensor peak), multi-token query attention on the GQA workload (--q-len new
+tokens per sequence), the copy-on-write block copy (HBM), and block moves
+between HBM and pinned host memory (against a contiguous copy over the same
+link).
 """
 
 import argparse
@@ -38,6 +46,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attention KV GB/s & seqs/s at 1 GB300; fraction of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse_args():
@@ -46,11 +55,19 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_bf16")
+    ap.add_argument("--workload", default=None,
+                    help="default: gqa_bf16 (shared_prefix for --op cascade)")
+    ap.add_argument("--op", default="decode",
+                    choices=["decode", "cascade", "multi_query", "block_copy", "host_swap"],
+                    help="decode (the headline step) or one of the other hot-path operations")
+    ap.add_argument("--q-len", type=int, default=4, help="new tokens per sequence for --op multi_query")
     ap.add_argument("--split-tokens", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.workload is None:
+        args.workload = "shared_prefix" if args.op == "cascade" else "gqa_bf16"
+    return args
 
 
 # ---------------------------------------------------------------- oracle leg
@@ -212,6 +229,17 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 tensor peak (burst: kernels timed on their own)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash():
@@ -439,8 +467,180 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- other operations
+
+def _time_on_stream(fn, steps, warmup, stream, sync):
+    import torch
+    for _ in range(max(3, warmup)):
+        fn()
+    sync()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    sync()
+    return e0.elapsed_time(e1) / steps
+
+
+def _traced(pkv, fn, steps, sync):
+    pkv.trace_read()
+    pkv.trace_enable(True)
+    for _ in range(steps):
+        fn()
+    sync()
+    pkv.trace_enable(False)
+    return {k: (n, t) for k, (n, t) in pkv.trace_read().items()}
+
+
+def run_op(args, local_rank):
+    """One JSON line for a hot-path operation other than the decode step
+    (cascade decode, multi-token query, block copy, host swap); device-timed
+    with CUDA events on the launching stream, per-kernel times from the
+    library's trace."""
+    import torch
+    import paged_kv_cache_222_gb300 as pkv
+    import workloads as W
+    from paged_kv_cache_222_gb300 import build
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sync = lambda: torch.cuda.synchronize(dev)
+    hbm, hbm_kind = measured_peaks()
+    tf_peak, tf_kind = measured_bf16_tflops()
+    steps, warm = args.steps, args.warmup
+    line = {"op": args.op, "n_gpus": 1, "steps": steps, "warmup": warm, "data": "synthetic"}
+
+    if args.op == "cascade":
+        case = W.make_case(args.workload, device=dev)
+        B, bs, prefix = case["B"], case["bs"], case["prefix"]
+        bt = case["block_tables"].to(dev)
+        lens = (case["ctx"] + 1).to(dev).to(torch.int32)
+        mx = int(lens.max())
+        q = case["q"][0].contiguous()
+        out = torch.empty((B, case["H_q"], case["D"]), device=dev)
+        pblocks = bt[0, :prefix // bs].contiguous()
+        plan = pkv.cascade_plan(B, case["H_q"], case["k_cache"], prefix, mx)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.cascade_decode_attention(q, case["k_cache"], case["v_cache"], pblocks, prefix, bt, lens,
+                                                  case["scale"], mx, out=out, workspace=ws)
+        plain = lambda: pkv.decode_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"],
+                                             max_context_len=mx, out=out)
+        ms = _time_on_stream(fn, steps, warm, stream, sync)
+        ms_plain = _time_on_stream(plain, steps, warm, stream, sync)
+        tr = _traced(pkv, fn, steps, sync)
+        logical = float((case["ctx"].double() + 1).sum()) * case["H_kv"] * case["D"] * 4
+        unique = (prefix + float((case["ctx"].double() + 1 - prefix).sum())) * case["H_kv"] * case["D"] * 4
+        n, t = tr.get("cascade_prefix", (0, 0.0))
+        pf_ms = t / n if n else float("nan")
+        flops = 4.0 * B * case["H_q"] * prefix * case["D"]
+        achieved = flops / (pf_ms / 1e3) / 1e12
+        line.update({"metric": "cascade decode KV GB/s (logical bytes: every sequence's whole context)",
+                     "value": logical / ms / 1e6, "unit": "GB/s", "ms_per_step": ms, "higher_is_better": True,
+                     "dtype": "bf16", "unique_GBs": unique / ms / 1e6, "plain_decode_ms": ms_plain,
+                     "config": {"workload": args.workload, "B": B, "H_q": case["H_q"], "H_kv": case["H_kv"],
+                                "d_head": case["D"], "block_size": bs, "shared_prefix": prefix,
+                                "prefix_ranges": plan.workers, "prefix_range_tokens": plan.prefix_split_tokens,
+                                "suffix_split_tokens": plan.split_tokens},
+                     "roofline": {"bound": "tensor", "kernel": "cascade_prefix", "achieved": achieved,
+                                  "peak": tf_peak, "unit": "TFLOP/s", "frac": achieved / tf_peak,
+                                  "peak_source": f"{tf_kind} (bf16_tflops, burst)",
+                                  "algorithmic_flops_per_launch": flops, "avg_launch_ms": pf_ms, "traffic": None}})
+    elif args.op == "multi_query":
+        ql = args.q_len
+        case = W.make_case(args.workload, device=dev, steps=ql)
+        B = case["B"]
+        bt = case["block_tables"].to(dev)
+        lens = (case["ctx"] + ql).to(dev).to(torch.int32)
+        mx = int(lens.max())
+        q = case["q"].permute(1, 0, 2, 3).contiguous()
+        out = torch.empty((B, ql, case["H_q"], case["D"]), device=dev)
+        plan = pkv.multi_query_plan(B, ql, case["H_q"], case["k_cache"], mx, 0,
+                                    torch.cuda.get_device_properties(dev).multi_processor_count)
+        ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.multi_query_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"], mx,
+                                               out=out, workspace=ws)
+        ms = _time_on_stream(fn, steps, warm, stream, sync)
+        tr = _traced(pkv, fn, steps, sync)
+        L = lens.double().cpu()
+        kv = float(L.sum()) * case["H_kv"] * case["D"] * 4
+        att = sum(float((L - ql + i + 1).clamp(min=0).sum()) for i in range(ql))
+        flops = 4.0 * att * case["H_q"] * case["D"]
+        n, t = tr.get("multi_query", (0, 0.0))
+        k_ms = t / n if n else float("nan")
+        achieved = kv / (k_ms / 1e3) / 1e9
+        line.update({"metric": "multi-token query attention KV GB/s", "value": kv / ms / 1e6, "unit": "GB/s",
+                     "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+                     "TFLOPs": flops / ms / 1e9,
+                     "config": {"workload": args.workload, "q_len": ql, "B": B, "H_q": case["H_q"],
+                                "H_kv": case["H_kv"], "d_head": case["D"], "block_size": case["bs"],
+                                "split_tokens": plan.split_tokens, "splits": plan.max_splits,
+                                "token_lanes": plan.workers},
+                     "roofline": {"bound": "hbm", "kernel": "multi_query", "achieved": achieved, "peak": hbm,
+                                  "unit": "GB/s", "frac": achieved / hbm,
+                                  "peak_source": f"{hbm_kind} (hbm_gbs, copy bandwidth)",
+                                  "algorithmic_bytes_per_launch": kv, "avg_launch_ms": k_ms,
+                                  "tensor_TFLOPs": flops / (k_ms / 1e3) / 1e12, "traffic": None}})
+    else:
+        nb, hkv, bs, d = 40000, 8, 16, 128
+        kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        blk = hkv * bs * d * 2
+        g = torch.Generator().manual_seed(20260500)
+        if args.op == "block_copy":
+            npairs = 8192
+            perm = torch.randperm(nb, generator=g)
+            src = perm[:npairs].to(torch.int32).to(dev)
+            dst = perm[npairs:2 * npairs].to(torch.int32).to(dev)
+            fn = lambda: pkv.copy_blocks(kc, vc, src, dst)
+            ms = _time_on_stream(fn, steps, warm, stream, sync)
+            byts = npairs * blk * 2 * 2
+            gbs = byts / ms / 1e6
+            line.update({"metric": "copy-on-write block copy GB/s (read + write)", "value": gbs, "unit": "GB/s",
+                         "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+                         "config": {"pairs": npairs, "block_bytes_per_cache": blk, "pool_blocks": nb},
+                         "roofline": {"bound": "hbm", "kernel": "block_copy", "achieved": gbs, "peak": hbm,
+                                      "unit": "GB/s", "frac": gbs / hbm,
+                                      "peak_source": f"{hbm_kind} (hbm_gbs, copy bandwidth)",
+                                      "algorithmic_bytes_per_launch": byts, "avg_launch_ms": ms, "traffic": None}})
+        else:
+            nh = 8192
+            hk, hv = pkv.host_pool_like(kc, nh)
+            src = torch.randperm(nb, generator=g)[:nh].to(torch.int32).to(dev)
+            hdst = torch.randperm(nh, generator=g).to(torch.int32).to(dev)
+            out_ms = _time_on_stream(lambda: pkv.copy_blocks_between(kc, vc, hk, hv, src, hdst), steps, warm,
+                                     stream, sync)
+            in_ms = _time_on_stream(lambda: pkv.copy_blocks_between(hk, hv, kc, vc, hdst, src), steps, warm,
+                                    stream, sync)
+            n = 2048
+            ref_out = _time_on_stream(lambda: hk[:n].copy_(kc[:n], non_blocking=True), steps, warm, stream, sync)
+            ref_in = _time_on_stream(lambda: kc[:n].copy_(hk[:n], non_blocking=True), steps, warm, stream, sync)
+            byts = nh * blk * 2
+            link_out = n * blk / ref_out / 1e6
+            link_in = n * blk / ref_in / 1e6
+            line.update({"metric": "host swap GB/s (device -> pinned host, host -> device)",
+                         "value": byts / out_ms / 1e6, "unit": "GB/s", "stage_GBs": byts / in_ms / 1e6,
+                         "ms_per_step": out_ms + in_ms, "higher_is_better": True, "dtype": "bf16",
+                         "config": {"blocks": nh, "block_bytes_per_cache": blk},
+                         "roofline": {"bound": "host link", "kernel": "block_copy",
+                                      "achieved": byts / out_ms / 1e6, "peak": link_out, "unit": "GB/s",
+                                      "frac": byts / out_ms / 1e6 / link_out,
+                                      "peak_source": "one contiguous cudaMemcpyAsync of 64 MB each way, "
+                                                     f"same run ({link_out:.0f} out, {link_in:.0f} in)",
+                                      "traffic": None}})
+    if pkv.device_error(dev) != 0:
+        raise RuntimeError("device error")
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.op != "decode":
+        run_op(args, int(os.environ.get("LOCAL_RANK", "0")))
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
