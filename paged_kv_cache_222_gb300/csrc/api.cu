@@ -105,8 +105,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // 4-D view (d, token-in-block, kv-head, block) of one cache tensor; a box is
-// one 16-token tile of up to 128 bytes per row, swizzled for ldmatrix.
-pkv_status make_cache_tmap(CUtensorMap* tm, const void* base, const pkv_cache_desc& c) {
+// `box_tokens` token rows (16 by default: one decode tile) of up to 128 bytes,
+// 128B- or 64B-swizzled.
+pkv_status make_cache_tmap(CUtensorMap* tm, const void* base, const pkv_cache_desc& c,
+                           int box_tokens = pkv::kTileTokens) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   const uint64_t esz = c.dtype == PKV_E4M3 ? 1 : 2;
@@ -116,8 +118,7 @@ pkv_status make_cache_tmap(CUtensorMap* tm, const void* base, const pkv_cache_de
                         static_cast<cuuint64_t>(c.num_kv_heads),
                         static_cast<cuuint64_t>(c.num_blocks)};
   cuuint64_t strides[3] = {row, row * c.block_size, row * c.block_size * c.num_kv_heads};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(boxb / esz), static_cast<cuuint32_t>(pkv::kTileTokens),
-                       1, 1};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(boxb / esz), static_cast<cuuint32_t>(box_tokens), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(tm, c.dtype == PKV_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   4, const_cast<void*>(base), dims, strides, box, estr,
@@ -709,14 +710,20 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
   const int32_t suffix = max_ctx - prefix_len;
   const int32_t st = auto_split_tokens(batch, c->num_kv_heads, suffix > 0 ? suffix : 1, sms);
   const int64_t splits = suffix > 0 ? ceil_div(suffix, st) : 1;
-  // prefix ranges: enough CTAs for two per SM, each at least one 64-token tile
-  // and at most 1024 blocks
+  // prefix ranges: the prefix kernel runs one CTA per SM; pick the number of
+  // ranges that minimises (waves of CTAs) x (tiles per range + two tiles of
+  // per-CTA overhead); fewer ranges on ties (fewer pieces to combine)
   const int64_t rows = static_cast<int64_t>(batch) * (num_q_heads / c->num_kv_heads);
   const int64_t row_blocks = ceil_div(rows, pkv::kCascadeRowsTc) * c->num_kv_heads;
-  int64_t nps = ceil_div(2LL * sms, row_blocks);
   const int64_t tiles = ceil_div(prefix_len, pkv::kCascadeTile);
-  if (nps > tiles) nps = tiles;
-  if (nps < 1) nps = 1;
+  int64_t nps = 1, best = -1;
+  for (int64_t n = 1; n <= tiles && n <= 64; ++n) {
+    const int64_t est = ceil_div(row_blocks * n, sms) * (ceil_div(tiles, n) + 2);
+    if (best < 0 || est < best) {
+      best = est;
+      nps = n;
+    }
+  }
   int64_t pst = ceil_div(ceil_div(prefix_len, nps), pkv::kCascadeTile) * pkv::kCascadeTile;
   const int64_t max_pst = 1024LL * c->block_size / pkv::kCascadeTile * pkv::kCascadeTile;
   if (pst > max_pst) pst = max_pst;
@@ -771,6 +778,13 @@ extern "C" pkv_status pkv_cascade_decode_attention(
   if (s != PKV_OK) return s;
   s = make_cache_tmap(&tv, v_cache, c);
   if (s != PKV_OK) return s;
+  // the prefix kernel reads whole blocks (up to 64 tokens) per TMA box
+  const int box = c.block_size < pkv::kCascadeTile ? c.block_size : pkv::kCascadeTile;
+  CUtensorMap tkb, tvb;
+  s = make_cache_tmap(&tkb, k_cache, c, box);
+  if (s != PKV_OK) return s;
+  s = make_cache_tmap(&tvb, v_cache, c, box);
+  if (s != PKV_OK) return s;
 
   const int64_t slots = pl.max_splits + pl.workers;
   const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * slots;
@@ -805,7 +819,7 @@ extern "C" pkv_status pkv_cascade_decode_attention(
   p.prefix_split_tokens = pl.prefix_split_tokens;
   p.err = st->err;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = traced(pkv::kKindCascadePrefix, cs, [&] { return pkv::launch_cascade_prefix(p, tk, tv, cs); });
+  cudaError_t e = traced(pkv::kKindCascadePrefix, cs, [&] { return pkv::launch_cascade_prefix(p, tkb, tvb, cs); });
   if (e == cudaSuccess)
     e = traced(pkv::kKindDecodeSplit, cs, [&] { return pkv::launch_decode_split(p, tk, tv, cs); });
   if (e == cudaSuccess)

@@ -9,9 +9,9 @@
 //
 // A block of one cache is num_kv_heads * block_size * head_dim elements,
 // contiguous.  The kernel walks the flat space of 16-byte words of all pairs
-// (K words, then V words, pair after pair) with a grid-stride loop; each
-// thread issues four independent 16-byte loads before its four stores, so a
-// warp keeps 2 KB in flight.  Source and destination ids are range-checked;
+// (K words, then V words, pair after pair) with a grid-stride loop over one
+// wave of resident CTAs; each thread issues four independent 16-byte loads
+// before its four stores, so a warp keeps 2 KB in flight.  Source and destination ids are range-checked;
 // a bad pair is skipped and recorded in the device error word.
 
 #include "pkv_device.cuh"
@@ -65,9 +65,24 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyPar
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream) {
   const int64_t words = p.n_pairs * 2 * p.block_vec;
   if (words == 0) return cudaSuccess;
-  // enough threads for one pass of four words each, at most 8 CTAs per SM
+  // one full wave of resident CTAs (a partial second wave leaves SMs idle at
+  // the end), fewer when the copy is small or the caller bounds it
+  static int resident[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, copy_blocks_kernel, kCopyThreads, 0);
+    if (e != cudaSuccess) return e;
+    resident[dev] = sms * (per_sm > 0 ? per_sm : 1);
+  }
   const int64_t want = (words + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
-  const int64_t cap = p.max_ctas > 0 ? p.max_ctas : 152 * 8;
+  int64_t cap = resident[dev];
+  if (p.max_ctas > 0 && p.max_ctas < cap) cap = p.max_ctas;
   const int blocks = static_cast<int>(want < cap ? want : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);

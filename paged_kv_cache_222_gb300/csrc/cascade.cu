@@ -16,59 +16,125 @@ namespace pkv {
 namespace {
 
 // ----------------------------------------------------------------------------
-// Cascade prefix kernel on the 5th-generation tensor cores (tcgen05 + TMEM).
-// 128 query rows per CTA, one row per thread (= one TMEM lane):
-//   TMEM columns   [0, D/2)   Q rows, bf16 pairs (A operand of S = Q K^T)
-//                  [64, 128)  S (fp32), then P = 2^(s - m) as bf16 hi | lo
-//                             (A operand of O += P V; P aliases S)
-//                  [128, 128 + D)  O (fp32 accumulator)
-//   shared memory  3 stages of 64-token K and V tiles, TMA-loaded with the
-//                  128-byte swizzle: K read as a K-major B operand, V as an
-//                  MN-major B operand, through sm_100 matrix descriptors.
-// Thread 0 issues the MMAs and commits them to mbarriers; every thread reads
-// its S row, keeps a lazy running max (O in TMEM is rescaled only when the
-// max grows by more than 2^8, so P stays <= 256) and writes its P row back.
+// Cascade prefix kernel on the 5th-generation tensor cores (tcgen05 + TMEM),
+// pipelined.  One CTA per SM owns 256 query rows of one KV head — two groups
+// of 128 rows that share every K/V tile — over one range of prefix tokens.
+// Its eleven warps have fixed roles:
+//   warps 0-7  softmax: group g = warp / 4; thread t of the group is its
+//              query row t (= TMEM lane t, in the group's half of the columns)
+//   warp 8     TMA producer: 64-token K and V tiles into a ring of four
+//              128B-swizzled stages, one box per lane
+//   warps 9-10 MMA issuers, one per group (one lane each):
+//              S_g(k) = Q_g K(k)^T, then O_g += P_g(k-1) V(k-1)
+// TMEM (512 columns): group g owns [256 g, 256 g + 256): O [0, D) fp32 and a
+// double buffer of S [D, D + 128) fp32, each buffer overwritten in place by
+// its P = 2^(s - m) as bf16 hi | lo pairs.  Q sits in shared memory in the
+// K-major 128B-swizzled layout (A operand of S through a matrix descriptor);
+// K is a K-major and V an MN-major B operand.  While one group's softmax
+// turns S(k) into P(k), the tensor core works on the other group and on
+// S(k+1) and O += P(k-1) V.  S_g(k) goes into the buffer that P_g(k-2)
+// occupied only after P_g(k-2).V has completed (tcgen05 orders MMAs only on
+// one accumulator).  Hand-offs are mbarriers: full / empty per stage (TMA
+// bytes; one commit per group after the stage's P.V), and per group and
+// buffer sfull / pfree (MMA commits) and pfull (one arrive per softmax warp).
+// The softmax keeps a lazy running max: O in TMEM is rescaled only when the
+// max grows by more than 2^8 (then after the previous P.V has completed), so
+// P stays <= 256.  The CTAs of one KV head read the same prefix tiles; each
+// starts at a different tile of its range (the online softmax takes tiles in
+// any order) so that they do not all ask L2 for the same lines at once.
+// Every wait is bounded; a time-out records the error, raises a shared abort
+// flag that ends every role's loop, and the CTA drains its copies and MMAs
+// before it frees TMEM.
 // ----------------------------------------------------------------------------
+
+// Wait for a barrier phase; false once the CTA aborts (or on time-out, which
+// records the error and raises the abort flag).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (n % 16 == 0 && *abort) return false;
+    if (n % kWaitTriesPerClockRead == 0) {
+      const uint64_t t = global_timer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kWaitLimitNs) {
+        record_error(err, kDevErrWaitTimeout);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(128, 2)
+struct CascadeShape {
+  static constexpr int GROUPS = 2;                    // 128-row groups per CTA
+  static constexpr int M = 128;                       // query rows per group
+  static constexpr int NKEY = kCascadeTile;           // keys per tile
+  static constexpr int HALVES = D / 64;               // 128-byte d-halves of a row
+  static constexpr int QHALF = M * 128;               // one d-half of one group's Q
+  static constexpr int HALF_BYTES = NKEY * 128;       // one d-half of a K (or V) tile
+  static constexpr int KREG = HALVES * HALF_BYTES;    // K (or V) tile
+  static constexpr int STAGE = 2 * KREG;
+  static constexpr int QBYTES = GROUPS * HALVES * QHALF;
+  static constexpr int NS = 4;
+  static constexpr int NBARS = 2 * NS + 6 * GROUPS + GROUPS;  // full, empty; sfull, pfull, pfree x2; done
+  static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
+  static constexpr int THREADS = 32 * (4 * GROUPS + 1 + GROUPS);
+};
+
+template <int D>
+__global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using L = Layout<D, false>;
-  constexpr int M = 128;
-  constexpr int NKEY = kCascadeTile;
-  constexpr int NSUB = NKEY / kTileTokens;
-  constexpr int HALVES = D / 64;                 // 128-byte d-halves of a row
-  constexpr int HALF_BYTES = NKEY * 128;         // one d-half of a 64-key tile
-  constexpr int KREG = HALVES * HALF_BYTES;      // K (or V) tile
-  constexpr int STAGE = 2 * KREG;
-  constexpr int NS = 3;
+  using C = CascadeShape<D>;
+  constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS, GROUPS = C::GROUPS;
   constexpr int kMaxPrefixBlocks = 1024;
-  constexpr uint32_t TCOLS = 256;
-  constexpr uint32_t COL_Q = 0, COL_S = 64, COL_PHI = 64, COL_PLO = 96, COL_O = 128;
+  constexpr uint32_t TCOLS = 512;
+  constexpr uint32_t GCOLS = TCOLS / GROUPS;          // TMEM columns of one group
+  constexpr uint32_t COL_O = 0, COL_S = D;            // within a group's columns
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
+  constexpr int PRODUCER = 4 * GROUPS;                // warp index
   static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(COL_S + 2 * NKEY <= GCOLS, "TMEM columns");
 
-  const int warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, ps = blockIdx.z;
   const int G = p.group;
   const int rows = p.batch * G;
-  const int row = blockIdx.x * M + threadIdx.x;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
-  uint64_t* bar_s = full + NS;
-  uint64_t* bar_pv = bar_s + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_pv + 1);
-  int* s_blk = reinterpret_cast<int*>(s_tmem + 2);
-  const uint32_t stage0 = smem_u32(smem);
+  uint8_t* q_sm = smem;                                // group g at g * HALVES * QHALF
+  const uint32_t stage0 = smem_u32(smem + C::QBYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::QBYTES + NS * C::STAGE);
+  uint64_t* full = bars;
+  uint64_t* empty = full + NS;
+  uint64_t* sfull = empty + NS;       // [GROUPS][2]
+  uint64_t* pfull = sfull + 2 * GROUPS;
+  uint64_t* pfree = pfull + 2 * GROUPS;
+  uint64_t* done = pfree + 2 * GROUPS;  // [GROUPS]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + GROUPS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_blk = reinterpret_cast<int*>(s_tmem + 4);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(full + s), 1);
-    mbar_init(smem_u32(bar_s), 1);
-    mbar_init(smem_u32(bar_pv), 1);
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), GROUPS);
+    }
+    for (int i = 0; i < 2 * GROUPS; ++i) {
+      mbar_init(smem_u32(sfull + i), 1);
+      mbar_init(smem_u32(pfull + i), 4);
+      mbar_init(smem_u32(pfree + i), 1);
+    }
+    for (int g = 0; g < GROUPS; ++g) mbar_init(smem_u32(done + g), 1);
+    *s_abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
@@ -77,17 +143,12 @@ __global__ void __launch_bounds__(128, 2)
     tmem_alloc(smem_u32(s_tmem), TCOLS);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *s_tmem;
-  const uint32_t tlane = tbase + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
-
   wait_prior_grid();
+
   const int t0 = ps * p.prefix_split_tokens;
   const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
   const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
-  for (int i = threadIdx.x; i < nblk && i < kMaxPrefixBlocks; i += blockDim.x) {
+  for (int i = tid; i < nblk && i < kMaxPrefixBlocks; i += blockDim.x) {
     int phys = p.prefix_blocks[t0 / p.block_size + i];
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.err, kDevErrBlockId);
@@ -95,195 +156,239 @@ __global__ void __launch_bounds__(128, 2)
     }
     s_blk[i] = phys;
   }
-  __syncthreads();
   const int ntile = (t1 - t0 + NKEY - 1) / NKEY;
+  // k-th tile processed = tile (k + first) % ntile of the range
+  const int first = ntile > 0 ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * ntile) / gridDim.x) : 0;
 
-  auto issue = [&](int k) {  // thread 0: tile k -> stage k % NS, laid out [K|V][d-half][key][128 B]
-    const int s = k % NS;
-    const uint32_t dst = stage0 + s * STAGE;
-    const uint32_t bar = smem_u32(full + s);
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int i = 0; i < NSUB; ++i) {
-      const int t = t0 + k * NKEY + i * kTileTokens;
-      const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;   // past the end: zeros
-      const int tok0 = t % p.block_size;
-#pragma unroll
-      for (int bx = 0; bx < HALVES; ++bx) {
-        const uint32_t off = bx * HALF_BYTES + i * kTileTokens * 128;
-        tma_load_4d(dst + off, &tmap_k, bar, bx * L::BOX_ELEMS, tok0, h, phys);
-        tma_load_4d(dst + KREG + off, &tmap_v, bar, bx * L::BOX_ELEMS, tok0, h, phys);
-      }
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int k = 0; k < ntile && k < NS; ++k) issue(k);
-
-  // ---- this thread's query row into TMEM (zeros for padding rows)
-  {
+  // ---- Q rows into shared memory: group g, row r, 16-byte chunk c of d-half
+  // hf at g * HALVES * QHALF + hf * QHALF + r * 128 + ((c ^ (r % 8)) * 16)
+  // (the 128-byte swizzle)
+  const int grp = warp / 4;                            // softmax warps only
+  const int r_in = (warp % 4) * 32 + lane;             // row within the group
+  const int row = blockIdx.x * (GROUPS * M) + grp * M + r_in;
+  if (warp < PRODUCER) {
     const uint16_t* q = static_cast<const uint16_t*>(p.q);
     const uint16_t* qr = row < rows ? q + (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) * D
                                     : nullptr;
+    uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
 #pragma unroll
-    for (int c0 = 0; c0 < D / 2; c0 += 16) {
-      uint32_t v[16];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 w = qr ? *reinterpret_cast<const uint4*>(qr + 2 * c0 + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * i] = w.x;
-        v[4 * i + 1] = w.y;
-        v[4 * i + 2] = w.z;
-        v[4 * i + 3] = w.w;
-      }
-      tmem_st16(tlane + COL_Q + c0, v);
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 w = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+      const int hf = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w;
     }
-    tmem_wait_st();
+    fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
   }
   tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_tmem;
 
-  const float qk_mult = p.qk_log2_scale;
-  float m_used = -CUDART_INF_F, lsum = 0.f;
-  bool healthy = true;
-  int k = 0;
-  for (; k < ntile; ++k) {
-    const int s = k % NS;
-    const uint32_t kbase = stage0 + s * STAGE, vbase = kbase + KREG;
-    // ---- S = Q K^T, issued by thread 0 once the tile has landed and the
-    // previous tile's P.V has completed: S shares TMEM columns with the P that
-    // P.V reads, and tcgen05 orders MMAs only on the same accumulator.  When
-    // bar_s flips, O is stable, P may be overwritten and the previous stage
-    // is free.
+  if (warp == PRODUCER) {
+    // ------------------------------------------------------------ producer
+    // Every lane of the warp issues one TMA box of each tile: one thread
+    // issuing all of a tile's boxes back to back was measured to hold a tile
+    // to about 16 bytes per cycle.
+    const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
+    const int per_half = NKEY / box;
+    const int nbox = 2 * C::HALVES * per_half;                   // K and V boxes of a tile (<= 32)
+    int issued = 0;
+    for (int k = 0; k < ntile; ++k) {
+      const int s = k % NS;
+      bool go = true;
+      if (lane == 0 && k >= NS)
+        go = wait_or_abort(smem_u32(empty + s), static_cast<uint32_t>((k / NS - 1) & 1), p.err, s_abort);
+      if (!__shfl_sync(kFull, go ? 1 : 0, 0)) break;
+      const uint32_t dst = stage0 + s * C::STAGE;
+      const uint32_t bar = smem_u32(full + s);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, C::STAGE);
+      }
+      __syncwarp();
+      if (lane < nbox) {
+        const int v = lane / (C::HALVES * per_half);          // 0: K, 1: V
+        const int bx = (lane / per_half) % C::HALVES;          // d-half
+        const int i = lane % per_half;                         // box within the tile
+        const int t = t0 + ((k + first) % ntile) * NKEY + i * box;
+        const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;  // past the end: zeros
+        const uint32_t off = v * C::KREG + bx * C::HALF_BYTES + i * box * 128;
+        tma_load_4d(dst + off, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, h, phys);
+      }
+      issued = k + 1;
+    }
+    if (lane == 0 && *s_abort) {  // the copies in flight land before the stages are released
+      for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
+        mbar_wait(smem_u32(full + k % NS), static_cast<uint32_t>((k / NS) & 1), nullptr);
+    }
+  } else if (warp > PRODUCER) {
+    // ------------------------------------------------------------ MMA issuers
+    const int g = warp - PRODUCER - 1;
+    if (lane == 0) {
+      const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
+      const uint32_t tg = tbase + g * GCOLS;
+      for (int k = 0; k <= ntile; ++k) {
+        if (k < ntile) {
+          const int s = k % NS, b = k & 1;
+          if (!wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort)) break;
+          // buffer b still holds P(k-2) until P(k-2).V has completed
+          if (k >= 2 && !wait_or_abort(smem_u32(pfree + 2 * g + b), static_cast<uint32_t>(((k - 2) >> 1) & 1),
+                                       p.err, s_abort))
+            break;
+          tc_fence_after();
+          const uint32_t kst = stage0 + s * C::STAGE;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t ad = smem_desc_sw128(qa + (ks / 4) * C::QHALF + (ks % 4) * 32, 0, 1024);
+            const uint64_t bd = smem_desc_sw128(kst + (ks / 4) * C::HALF_BYTES + (ks % 4) * 32, 0, 1024);
+            tc_mma_ss(tg + COL_S + b * NKEY, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(sfull + 2 * g + b));
+        }
+        if (k >= 1) {
+          const int j = k - 1, sj = j % NS, bj = j & 1;
+          if (!wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort))
+            break;
+          tc_fence_after();
+          const uint32_t vst = stage0 + sj * C::STAGE + C::KREG;
+          const uint32_t pa = tg + COL_S + bj * NKEY;
+#pragma unroll
+          for (int kk = 0; kk < NKEY / 16; ++kk) {
+            // MN-major V: 8-key groups 1024 B apart, d-halves HALF_BYTES apart
+            const uint64_t vd = smem_desc_sw128(vst + kk * 2048, C::HALVES > 1 ? C::HALF_BYTES : 0, 1024);
+            tc_mma_ts(tg + COL_O, pa + kk * 8, vd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(tg + COL_O, pa + NKEY / 2 + kk * 8, vd, IDESC_PV, 1u);
+          }
+          tc_commit(smem_u32(pfree + 2 * g + bj));
+          tc_commit(smem_u32(empty + sj));
+        }
+      }
+      // nothing of this thread's may still be running when TMEM is freed
+      tc_commit(smem_u32(done + g));
+      mbar_wait(smem_u32(done + g), 0u, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const uint32_t tl = tbase + grp * GCOLS + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    uint64_t* g_sfull = sfull + 2 * grp;
+    uint64_t* g_pfull = pfull + 2 * grp;
+    uint64_t* g_pfree = pfree + 2 * grp;
+    const float qk_mult = p.qk_log2_scale;
+    float m_used = -CUDART_INF_F, lsum = 0.f;
     bool ok = true;
-    if (threadIdx.x == 0) {
-      ok = mbar_wait(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err);
-      if (ok && k > 0) ok = mbar_wait(smem_u32(bar_pv), static_cast<uint32_t>((k - 1) & 1), p.err);
-      if (ok) {
+    for (int k = 0; k < ntile && ok; ++k) {
+      const int b = k & 1;
+      ok = __all_sync(kFull, wait_or_abort(smem_u32(g_sfull + b), static_cast<uint32_t>((k >> 1) & 1), p.err,
+                                           s_abort));
+      if (!ok) break;
+      tc_fence_after();
+      float x[NKEY];
+      {
+        uint32_t v[NKEY / 16][16];
+#pragma unroll
+        for (int c = 0; c < NKEY / 16; ++c) tmem_ld16(tl + COL_S + b * NKEY + 16 * c, v[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < NKEY / 16; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]) * qk_mult;
+      }
+      const int valid = t1 - (t0 + ((k + first) % ntile) * NKEY);
+      if (valid < NKEY) {
+#pragma unroll
+        for (int i = 0; i < NKEY; ++i)
+          if (i >= valid) x[i] = -CUDART_INF_F;
+      }
+      float mt;
+      {  // tree of partial maxima: a short dependency chain
+        float mp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mp[i] = x[i];
+#pragma unroll
+        for (int i = 8; i < NKEY; ++i) mp[i & 7] = fmaxf(mp[i & 7], x[i]);
+        mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      }
+      float alpha = 1.f;
+      bool resc = false;
+      if (m_used == -CUDART_INF_F) {
+        m_used = mt;  // nothing accumulated yet for this row
+      } else if (mt > m_used + 8.f) {
+        alpha = fast_exp2(m_used - mt);
+        m_used = mt;
+        resc = true;
+      }
+      if (__any_sync(kFull, resc)) {
+        // O holds tiles 0..k-1 once P(k-1).V has completed
+        ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + ((k - 1) & 1)),
+                                             static_cast<uint32_t>(((k - 1) >> 1) & 1), p.err, s_abort));
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t kd = smem_desc_sw128(kbase + (ks / 4) * HALF_BYTES + (ks % 4) * 32, 0, 1024);
-          tc_mma_ts(tbase + COL_S, tbase + COL_Q + ks * 8, kd, IDESC_S, ks > 0 ? 1u : 0u);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[2][16];
+          tmem_ld16(tl + COL_O + c0, v[0]);
+          tmem_ld16(tl + COL_O + c0 + 16, v[1]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[hh][i] = __float_as_uint(__uint_as_float(v[hh][i]) * alpha);
+          tmem_st16(tl + COL_O + c0, v[0]);
+          tmem_st16(tl + COL_O + c0 + 16, v[1]);
         }
-        tc_commit(smem_u32(bar_s));
+        tmem_wait_st();
       }
-    }
-    if (!__syncthreads_and(ok)) {
-      healthy = false;
-      break;
-    }
-    if (!mbar_wait(smem_u32(bar_s), static_cast<uint32_t>(k & 1), p.err)) ok = false;
-    tc_fence_after();
-    if (threadIdx.x == 0 && ok && k > 0 && k - 1 + NS < ntile) issue(k - 1 + NS);
-    float x[NKEY];
-    {
-      uint32_t v[NKEY / 16][16];
+      lsum *= alpha;
+      const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < NKEY / 16; ++c) tmem_ld16(tlane + COL_S + 16 * c, v[c]);
-      tmem_wait_ld();
+      for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int c = 0; c < NKEY / 16; ++c)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]);
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = fast_exp2(x[2 * (c0 + i)] - mu);
+          const float p1 = fast_exp2(x[2 * (c0 + i) + 1] - mu);
+          ls[i & 3] += p0 + p1;
+          hi[i] = pack_bf16x2(p0, p1);
+          lo[i] = pack_bf16x2(p0 - bf16lo_to_f32(hi[i]), p1 - bf16hi_to_f32(hi[i]));
+        }
+        tmem_st16(tl + COL_S + b * NKEY + c0, hi);          // P(k) over S(k)
+        tmem_st16(tl + COL_S + b * NKEY + NKEY / 2 + c0, lo);
+      }
+      lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(g_pfull + b));   // P(k) is in TMEM
     }
-    const int valid = t1 - (t0 + k * NKEY);
-    float mt = -CUDART_INF_F;
-#pragma unroll
-    for (int i = 0; i < NKEY; ++i) {
-      x[i] = i < valid ? x[i] * qk_mult : -CUDART_INF_F;
-      mt = fmaxf(mt, x[i]);
-    }
-    float alpha = 1.f;
-    bool resc = false;
-    if (k == 0) {
-      m_used = mt;
-    } else if (mt > m_used + 8.f) {
-      alpha = fast_exp2(m_used - mt);
-      m_used = mt;
-      resc = true;
-    }
-    if (__any_sync(kFull, resc)) {
+    if (ok && ntile > 0)
+      ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + ((ntile - 1) & 1)),
+                                           static_cast<uint32_t>(((ntile - 1) >> 1) & 1), p.err, s_abort));
+    if (ok && ntile > 0) {
+      tc_fence_after();
+      const int64_t S_row = p.slots_per_row;
+      const int64_t piece = (row < rows ? (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) : 0) *
+                                S_row + p.extra_slot + ps;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[2][16];
-        tmem_ld16(tlane + COL_O + c0, v[0]);
-        tmem_ld16(tlane + COL_O + c0 + 16, v[1]);
+        tmem_ld16(tl + COL_O + c0, v[0]);
+        tmem_ld16(tl + COL_O + c0 + 16, v[1]);
         tmem_wait_ld();
+        if (row < rows) {
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + piece * D + c0);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[hh][i] = __float_as_uint(__uint_as_float(v[hh][i]) * alpha);
-        tmem_st16(tlane + COL_O + c0, v[0]);
-        tmem_st16(tlane + COL_O + c0 + 16, v[1]);
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]), __uint_as_float(v[i / 4][4 * (i % 4) + 1]),
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 2]),
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 3]));
+        }
       }
-    }
-    lsum *= alpha;
-#pragma unroll
-    for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p0 = fast_exp2(x[2 * (c0 + i)] - m_used);
-        const float p1 = fast_exp2(x[2 * (c0 + i) + 1] - m_used);
-        lsum += p0 + p1;
-        hi[i] = pack_bf16x2(p0, p1);
-        lo[i] = pack_bf16x2(p0 - bf16lo_to_f32(hi[i]), p1 - bf16hi_to_f32(hi[i]));
-      }
-      tmem_st16(tlane + COL_PHI + c0, hi);
-      tmem_st16(tlane + COL_PLO + c0, lo);
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    if (!__syncthreads_and(ok)) {
-      healthy = false;
-      break;
-    }
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < NKEY / 16; ++kk) {
-        // MN-major V: 8-key groups 1024 B apart, the two 64-wide d-halves
-        // HALF_BYTES apart (a single half for D = 64)
-        const uint64_t vd = smem_desc_sw128(vbase + kk * 2048, HALVES > 1 ? HALF_BYTES : 0, 1024);
-        tc_mma_ts(tbase + COL_O, tbase + COL_PHI + kk * 8, vd, IDESC_PV, (k > 0 || kk > 0) ? 1u : 0u);
-        tc_mma_ts(tbase + COL_O, tbase + COL_PLO + kk * 8, vd, IDESC_PV, 1u);
-      }
-      tc_commit(smem_u32(bar_pv));
-    }
-  }
-  if (healthy && ntile > 0) {
-    const bool pv_done = mbar_wait(smem_u32(bar_pv), static_cast<uint32_t>((ntile - 1) & 1), p.err);
-    healthy = __syncthreads_and(pv_done);
-  }
-  if (healthy && ntile > 0) {
-    tc_fence_after();
-    const int64_t S_row = p.slots_per_row;
-    const int64_t piece = (row < rows ? (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) : 0) *
-                              S_row + p.extra_slot + ps;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t v[2][16];
-      tmem_ld16(tlane + COL_O + c0, v[0]);
-      tmem_ld16(tlane + COL_O + c0 + 16, v[1]);
-      tmem_wait_ld();
       if (row < rows) {
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + piece * D + c0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]), __uint_as_float(v[i / 4][4 * (i % 4) + 1]),
-                               __uint_as_float(v[i / 4][4 * (i % 4) + 2]), __uint_as_float(v[i / 4][4 * (i % 4) + 3]));
+        p.ws_ml[piece * 2] = m_used;
+        p.ws_ml[piece * 2 + 1] = lsum;
       }
     }
-    if (row < rows) {
-      p.ws_ml[piece * 2] = m_used;
-      p.ws_ml[piece * 2 + 1] = lsum;
-    }
-  } else if (!healthy && threadIdx.x == 0) {
-    // let whatever is still in flight land before the memory is released
-    for (int s = 0; s < NS && s < ntile; ++s) mbar_wait(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), nullptr);
-    mbar_wait(smem_u32(bar_s), static_cast<uint32_t>(k & 1), nullptr);
-    if (k > 0) mbar_wait(smem_u32(bar_pv), static_cast<uint32_t>((k - 1) & 1), nullptr);
   }
   allow_next_grid();
   tc_fence_before();
@@ -297,8 +402,9 @@ __global__ void __launch_bounds__(128, 2)
 }  // namespace
 
 int cascade_smem_bytes(int head_dim) {
-  const int stage = (kCascadeTile / kTileTokens) * 2 * kTileTokens * head_dim * 2;
-  return 3 * stage + 6 * 8 + 1024 * 4 + 1024;
+  // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
+  const int need = head_dim == 128 ? CascadeShape<128>::BYTES : CascadeShape<64>::BYTES;
+  return need > 120 * 1024 ? need : 120 * 1024;
 }
 
 namespace {
@@ -320,7 +426,7 @@ cudaError_t launch_cascade_t(const DecodeParams& p, const CUtensorMap& tk, const
   const int rows = p.batch * p.group;
   const int nps = (p.prefix_len + p.prefix_split_tokens - 1) / p.prefix_split_tokens;
   const dim3 grid((rows + kCascadeRowsTc - 1) / kCascadeRowsTc, p.num_kv_heads, nps);
-  return launch_pdl(kern, grid, dim3(128), smem, stream, tk, tv, p);
+  return launch_pdl(kern, grid, dim3(CascadeShape<D>::THREADS), smem, stream, tk, tv, p);
 }
 
 }  // namespace

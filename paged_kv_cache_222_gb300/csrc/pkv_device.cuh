@@ -65,16 +65,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier, at most kWaitLimitNs.  On time-out the
-// error word gets PKV_DEVERR_WAIT_TIMEOUT and false is returned.
+// Try-waits between two reads of the global timer: the timer read is slow,
+// and a phase that completes while the thread reads it would be noticed late.
+constexpr uint32_t kWaitTriesPerClockRead = 256;
+
+// Wait for phase `parity` of the barrier, at most about kWaitLimitNs.  On
+// time-out the error word gets PKV_DEVERR_WAIT_TIMEOUT and false is returned.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      record_error(err, kDevErrWaitTimeout);
-      return false;
+    if (n % kWaitTriesPerClockRead == 0) {
+      const uint64_t t = global_timer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kWaitLimitNs) {
+        record_error(err, kDevErrWaitTimeout);
+        return false;
+      }
     }
   }
 }

@@ -136,10 +136,9 @@ int multi_query_smem_bytes(int head_dim);
 // Token lanes (warps sharing the same 16 rows) for R rows per (sequence, head).
 inline int multi_query_lanes(int rows) { return rows <= 16 ? 4 : (rows <= 32 ? 2 : 1); }
 
-// Rows of query heads one cascade prefix CTA covers: 4 warps x 16 (mma.sync
-// kernel), one TMEM lane per thread (tcgen05 kernel).
-constexpr int kCascadeRows = 64;
-constexpr int kCascadeRowsTc = 128;
+// Rows of query heads one cascade prefix CTA covers: two groups of 128 TMEM
+// lanes.
+constexpr int kCascadeRowsTc = 256;
 // Keys per cascade prefix tile (4 sub-tiles of kTileTokens).
 constexpr int kCascadeTile = 64;
 
