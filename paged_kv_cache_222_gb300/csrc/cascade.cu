@@ -171,11 +171,14 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     const uint16_t* qr = row < rows ? q + (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) * D
                                     : nullptr;
     uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
+    uint4 w[D / 8];  // every load issued before the first store
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+      w[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
-      const uint4 w = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
       const int hf = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w;
+      *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
     }
     fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
   }
