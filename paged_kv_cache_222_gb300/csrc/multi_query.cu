@@ -11,9 +11,9 @@
 //  * Rows are (query token i, head g) pairs of one KV head: R = q_len * G of
 //    them share every K/V byte.  A CTA takes up to 64 rows of one (sequence,
 //    KV head) over one split of `split_tokens` tokens, streamed in 64-token
-//    tiles (four 16-token TMA sub-tiles of K and V, 128B-swizzled, three
-//    stages, full / empty mbarriers, block ids of the split staged in shared
-//    memory).
+//    tiles (four 16-token TMA sub-tiles of K and V, 128B-swizzled, two or
+//    three stages, full / empty mbarriers, block ids of the split staged in
+//    shared memory).
 //  * Warps are arranged as row groups x token lanes: with R <= 16 all four
 //    warps hold the same 16 rows and each takes one sub-tile of every tile;
 //    R <= 32 gives two groups of two lanes; larger R one 16-row group per
@@ -30,18 +30,28 @@
 namespace pkv {
 namespace {
 
+// Shared-memory stages per CTA and CTAs per SM: with two or four token lanes
+// (R <= 32 rows) a CTA is light enough on registers that two stages let three
+// CTAs share an SM.
+template <int TL>
+struct MqShape {
+  static constexpr int NS = TL >= 2 ? 2 : 3;
+  static constexpr int MINB = TL >= 2 ? 3 : 2;
+};
+
 template <int D, int TL>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, MqShape<TL>::MINB)
     multi_query_kernel(const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using L = Layout<D, false>;
   constexpr int KS = D / 16;
   constexpr int NSUB = kMultiQueryTile / kTileTokens;  // sub-tiles per tile
+  static_assert(2 * NSUB * L::NBOX <= 32, "one TMA box per lane");
   constexpr int NSW = NSUB / TL;                       // sub-tiles per warp per tile
   constexpr int RG = 4 / TL;                           // row groups
   constexpr int RPC = 16 * RG;                         // rows per CTA
   constexpr int STAGE = NSUB * L::STAGEB;
-  constexpr int NS = 3;
+  constexpr int NS = MqShape<TL>::NS;
   constexpr int DP = D + 4;
   static_assert(4 * 16 * DP * 4 + 4 * 16 * 2 * 4 <= NS * STAGE, "merge buffer fits the stages");
 
@@ -109,27 +119,31 @@ __global__ void __launch_bounds__(128, 2)
   }
   __syncthreads();
 
-  auto issue = [&](int k) {  // thread 0: the four 16-token sub-tiles of tile k
+  // Warp 0 loads tile k: lane 0 arms the stage's barrier, then every lane
+  // issues one 16-token TMA box (one thread issuing all of a tile's boxes was
+  // measured to hold a stage to about 16 bytes per cycle).
+  constexpr int NBOXES = 2 * NSUB * L::NBOX;  // K and V boxes of a tile (<= 32)
+  auto issue = [&](int k) {
     const int s = k % NS;
     const uint32_t dst = stage0 + s * STAGE;
     const uint32_t bar = smem_u32(full + s);
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int i = 0; i < NSUB; ++i) {
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, STAGE);
+    }
+    __syncwarp();
+    if (lane < NBOXES) {
+      const int v = lane / (NSUB * L::NBOX);
+      const int i = (lane / L::NBOX) % NSUB;
+      const int bx = lane % L::NBOX;
       const int t = t_begin + k * kMultiQueryTile + i * kTileTokens;
       const int bi = (t - t_begin) / p.block_size;
       const int phys = (t < t_stop && bi < kMultiQueryMaxSplitBlocks) ? s_blk[bi] : -1;
-      const int tok0 = t % p.block_size;
-#pragma unroll
-      for (int bx = 0; bx < L::NBOX; ++bx) {
-        tma_load_4d(dst + i * L::STAGEB + bx * L::BOX_BYTES, &tmap_k, bar, bx * L::BOX_ELEMS, tok0, h, phys);
-        tma_load_4d(dst + i * L::STAGEB + L::TILEB + bx * L::BOX_BYTES, &tmap_v, bar, bx * L::BOX_ELEMS,
-                    tok0, h, phys);
-      }
+      tma_load_4d(dst + i * L::STAGEB + v * L::TILEB + bx * L::BOX_BYTES, v ? &tmap_v : &tmap_k, bar,
+                  bx * L::BOX_ELEMS, t % p.block_size, h, phys);
     }
   };
-  if (threadIdx.x == 0)
+  if (warp == 0)
     for (int k = 0; k < ntile && k < NS; ++k) issue(k);
 
   // query fragments (A operand of S = Q K^T): rows ra and rb = ra + 8
@@ -267,11 +281,12 @@ __global__ void __launch_bounds__(128, 2)
         }
       }
     }
-    // ---- release the stage; thread 0 refills it once all four warps are done
+    // ---- release the stage; warp 0 refills it once all four warps are done
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(empty + s));
-    if (threadIdx.x == 0 && healthy && k + NS < ntile) {
-      if (mbar_wait(smem_u32(empty + s), par, p.err)) issue(k + NS);
+    if (warp == 0 && healthy && k + NS < ntile) {
+      const bool freed = lane == 0 ? mbar_wait(smem_u32(empty + s), par, p.err) : true;
+      if (__shfl_sync(kFull, freed ? 1 : 0, 0)) issue(k + NS);
     }
     __syncwarp();
   }
@@ -346,7 +361,8 @@ template <int D, int TL>
 cudaError_t launch_mq_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                         cudaStream_t stream) {
   auto kern = multi_query_kernel<D, TL>;
-  const int smem = multi_query_smem_bytes(D);
+  const int stage = (kMultiQueryTile / kTileTokens) * 2 * kTileTokens * D * 2;
+  const int smem = MqShape<TL>::NS * stage + 6 * 8 + kMultiQueryMaxSplitBlocks * 4 + 1024;
   static bool configured[64] = {};
   cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
@@ -357,11 +373,6 @@ cudaError_t launch_mq_t(const DecodeParams& p, const CUtensorMap& tk, const CUte
 }
 
 }  // namespace
-
-int multi_query_smem_bytes(int head_dim) {
-  const int stage = (kMultiQueryTile / kTileTokens) * 2 * kTileTokens * head_dim * 2;
-  return 3 * stage + 6 * 8 + kMultiQueryMaxSplitBlocks * 4 + 1024;
-}
 
 cudaError_t launch_multi_query(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {

@@ -131,8 +131,6 @@ cudaError_t launch_multi_query(const DecodeParams& p, const CUtensorMap& tmap_k,
 // in 16-row warp groups; the block ids of one split staged in shared memory.
 constexpr int kMultiQueryTile = 64;
 constexpr int kMultiQueryMaxSplitBlocks = 1024;
-// Dynamic shared memory of the multi-token query kernel.
-int multi_query_smem_bytes(int head_dim);
 // Token lanes (warps sharing the same 16 rows) for R rows per (sequence, head).
 inline int multi_query_lanes(int rows) { return rows <= 16 ? 4 : (rows <= 32 ? 2 : 1); }
 
