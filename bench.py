@@ -558,11 +558,12 @@ def run_op(args, local_rank):
         mx = int(lens.max())
         q = case["q"].permute(1, 0, 2, 3).contiguous()
         out = torch.empty((B, ql, case["H_q"], case["D"]), device=dev)
-        plan = pkv.multi_query_plan(B, ql, case["H_q"], case["k_cache"], mx, 0,
+        st = max(args.split_tokens, 0)
+        plan = pkv.multi_query_plan(B, ql, case["H_q"], case["k_cache"], mx, st,
                                     torch.cuda.get_device_properties(dev).multi_processor_count)
         ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
         fn = lambda: pkv.multi_query_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"], mx,
-                                               out=out, workspace=ws)
+                                               split_tokens=st, out=out, workspace=ws)
         ms = _time_on_stream(fn, steps, warm, stream, sync)
         tr = _traced(pkv, fn, steps, sync)
         L = lens.double().cpu()

@@ -854,7 +854,8 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
   if (sms <= 0) sms = kDefaultSms;
   const int32_t rows = q_len * (num_q_heads / c->num_kv_heads);
   const int32_t lanes = pkv::multi_query_lanes(rows);
-  const int64_t nrb = ceil_div(rows, 16 * (4 / lanes));
+  const bool tc = rows >= pkv::kMultiQueryTcRows;
+  const int64_t nrb = tc ? ceil_div(rows, 128) : ceil_div(rows, 16 * (4 / lanes));
   const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * nrb;
   int32_t st = split_tokens;
   if (st == 0) {
@@ -872,7 +873,7 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
   out->mode = 3;
   out->split_tokens = st;
   out->max_splits = static_cast<int32_t>(splits);
-  out->workers = lanes;
+  out->workers = rows >= pkv::kMultiQueryTcRows ? 0 : lanes;  // 0: the tcgen05 kernel
   if (splits > 1) {
     const int64_t n = static_cast<int64_t>(batch) * q_len * num_q_heads * splits;
     out->workspace_bytes = align256(n * c->head_dim * 4) + n * 2 * 4;
@@ -917,10 +918,13 @@ extern "C" pkv_status pkv_multi_query_attention(
     if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
   const pkv_cache_desc& c = *cache;
+  // q_len * G >= 64 rows: the tcgen05 kernel, which reads whole blocks per TMA box
+  const bool tc = pl.workers == 0;
+  const int box = tc ? (c.block_size < pkv::kCascadeTile ? c.block_size : pkv::kCascadeTile) : pkv::kTileTokens;
   CUtensorMap tk, tv;
-  s = make_cache_tmap(&tk, k_cache, c);
+  s = make_cache_tmap(&tk, k_cache, c, box);
   if (s != PKV_OK) return s;
-  s = make_cache_tmap(&tv, v_cache, c);
+  s = make_cache_tmap(&tv, v_cache, c, box);
   if (s != PKV_OK) return s;
   const int64_t n = static_cast<int64_t>(batch) * q_len * num_q_heads * pl.max_splits;
   DecodeParams p = {};
@@ -951,7 +955,9 @@ extern "C" pkv_status pkv_multi_query_attention(
   p.q_len = q_len;
   p.err = st->err;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = traced(pkv::kKindMultiQuery, cs, [&] { return pkv::launch_multi_query(p, tk, tv, cs); });
+  cudaError_t e = traced(pkv::kKindMultiQuery, cs, [&] {
+    return tc ? pkv::launch_multi_query_tc(p, tk, tv, cs) : pkv::launch_multi_query(p, tk, tv, cs);
+  });
   if (e == cudaSuccess && pl.max_splits > 1) {
     DecodeParams pc = p;            // rows (b, i, hq) flatten to b * (q_len * H_q) + i * H_q + hq
     pc.num_q_heads = q_len * num_q_heads;

@@ -68,9 +68,15 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
   }
 }
 
-template <int D>
-struct CascadeShape {
-  static constexpr int GROUPS = 2;                    // 128-row groups per CTA
+// Shape of a CTA: GROUPS 128-row groups (2 for the cascade prefix, whose
+// rows all read the same prefix; 1 for multi-token queries, whose rows of one
+// (sequence, KV head) are at most 128 per row block), the ring of K/V stages
+// and the threads (4 softmax warps per group, a producer warp, one MMA-issuer
+// warp per group).  Two groups take all 512 TMEM columns (one CTA per SM);
+// one group takes 256, and two such CTAs share an SM.
+template <int D, int GROUPS_>
+struct TcShape {
+  static constexpr int GROUPS = GROUPS_;
   static constexpr int M = 128;                       // query rows per group
   static constexpr int NKEY = kCascadeTile;           // keys per tile
   static constexpr int HALVES = D / 64;               // 128-byte d-halves of a row
@@ -79,33 +85,42 @@ struct CascadeShape {
   static constexpr int KREG = HALVES * HALF_BYTES;    // K (or V) tile
   static constexpr int STAGE = 2 * KREG;
   static constexpr int QBYTES = GROUPS * HALVES * QHALF;
-  static constexpr int NS = 4;
+  static constexpr int NS = GROUPS == 2 ? 4 : 2;
   static constexpr int NBARS = 2 * NS + 6 * GROUPS + GROUPS;  // full, empty; sfull, pfull, pfree x2; done
   static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
   static constexpr int THREADS = 32 * (4 * GROUPS + 1 + GROUPS);
+  static constexpr uint32_t TCOLS = 256 * GROUPS;
+  static constexpr int MINB = GROUPS == 2 ? 1 : 2;    // CTAs per SM
 };
 
-template <int D>
-__global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
-    cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+// MQ = false: cascade prefix.  Rows (b, g) of KV head blockIdx.y, 256 per CTA
+// (blockIdx.x), over prefix range blockIdx.z; pieces go to workspace slot
+// extra_slot + range.
+// MQ = true: multi-token queries.  Rows (i, g) of sequence blockIdx.z and KV
+// head blockIdx.y / row blocks, 128 per CTA, over split blockIdx.x of the
+// sequence's own tokens with a causal limit per row; a sequence with one split
+// writes `out`, else (acc, m, l) partials for the combine kernel.
+template <int D, int GROUPS, bool MQ>
+__global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS>::MINB)
+    paged_tc_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                              const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using L = Layout<D, false>;
-  using C = CascadeShape<D>;
-  constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS, GROUPS = C::GROUPS;
-  constexpr int kMaxPrefixBlocks = 1024;
-  constexpr uint32_t TCOLS = 512;
-  constexpr uint32_t GCOLS = TCOLS / GROUPS;          // TMEM columns of one group
+  using C = TcShape<D, GROUPS>;
+  constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS;
+  constexpr int kMaxBlocks = 1024;                    // block ids of one range, in shared memory
+  constexpr uint32_t TCOLS = C::TCOLS;
+  constexpr uint32_t GCOLS = 256;                     // TMEM columns of one group
   constexpr uint32_t COL_O = 0, COL_S = D;            // within a group's columns
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
   constexpr int PRODUCER = 4 * GROUPS;                // warp index
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(COL_S + 2 * NKEY <= GCOLS, "TMEM columns");
+  static_assert(!MQ || GROUPS == 1, "one group per multi-token CTA");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, ps = blockIdx.z;
   const int G = p.group;
-  const int rows = p.batch * G;
+  const int H_q = p.num_q_heads;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -145,11 +160,39 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
   }
   wait_prior_grid();
 
-  const int t0 = ps * p.prefix_split_tokens;
-  const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
+  // ---- the CTA's rows, token range [t0, t1) and block list
+  int h, rows, row0, t0, t1, ctx = 0, nsplit = 0, QL = 1;
+  int64_t b_rows = 0;
+  const int32_t* blocks;
+  if constexpr (MQ) {
+    QL = p.q_len;
+    rows = QL * G;
+    const int nrb = (rows + M - 1) / M;
+    h = blockIdx.y / nrb;
+    row0 = (blockIdx.y - h * nrb) * M;
+    const int b = blockIdx.z;
+    b_rows = static_cast<int64_t>(b) * QL;
+    const int ctx_raw = p.context_lens[b];
+    ctx = clamp_ctx(p, ctx_raw);
+    if (ctx != ctx_raw && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) record_error(p.err, kDevErrContextLen);
+    nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
+    t0 = blockIdx.x * p.split_tokens;
+    const int row_last = min(rows, row0 + M) - 1;
+    const int lim_last = min(ctx, ctx - QL + row_last / G + 1);   // rows attend monotonically more
+    t1 = t0 < ctx ? min(min(ctx, t0 + p.split_tokens), lim_last) : t0;
+    if (t1 < t0) t1 = t0;
+    blocks = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+  } else {
+    h = blockIdx.y;
+    rows = p.batch * G;
+    row0 = blockIdx.x * (GROUPS * M);
+    t0 = blockIdx.z * p.prefix_split_tokens;
+    t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
+    blocks = p.prefix_blocks;
+  }
   const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
-  for (int i = tid; i < nblk && i < kMaxPrefixBlocks; i += blockDim.x) {
-    int phys = p.prefix_blocks[t0 / p.block_size + i];
+  for (int i = tid; i < nblk && i < kMaxBlocks; i += blockDim.x) {
+    int phys = blocks[t0 / p.block_size + i];
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.err, kDevErrBlockId);
       phys = -1;
@@ -157,19 +200,23 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     s_blk[i] = phys;
   }
   const int ntile = (t1 - t0 + NKEY - 1) / NKEY;
-  // k-th tile processed = tile (k + first) % ntile of the range
-  const int first = ntile > 0 ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * ntile) / gridDim.x) : 0;
+  // k-th tile processed = tile (k + first) % ntile of the range; cascade CTAs
+  // of one head start at different tiles (they all read the same prefix)
+  const int first =
+      (!MQ && ntile > 0) ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * ntile) / gridDim.x) : 0;
 
   // ---- Q rows into shared memory: group g, row r, 16-byte chunk c of d-half
   // hf at g * HALVES * QHALF + hf * QHALF + r * 128 + ((c ^ (r % 8)) * 16)
   // (the 128-byte swizzle)
   const int grp = warp / 4;                            // softmax warps only
   const int r_in = (warp % 4) * 32 + lane;             // row within the group
-  const int row = blockIdx.x * (GROUPS * M) + grp * M + r_in;
+  const int row = row0 + grp * M + r_in;
+  const bool row_ok = warp < PRODUCER && row < rows;
+  // output row of this query row: (b, hq) for the cascade, (b, i, hq) flattened
+  const int64_t orow = MQ ? (b_rows + row / G) * H_q + h * G + row % G
+                          : static_cast<int64_t>(row / G) * H_q + h * G + row % G;
   if (warp < PRODUCER) {
-    const uint16_t* q = static_cast<const uint16_t*>(p.q);
-    const uint16_t* qr = row < rows ? q + (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) * D
-                                    : nullptr;
+    const uint16_t* qr = row_ok ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
     uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
     uint4 w[D / 8];  // every load issued before the first store
 #pragma unroll
@@ -214,7 +261,7 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
         const int bx = (lane / per_half) % C::HALVES;          // d-half
         const int i = lane % per_half;                         // box within the tile
         const int t = t0 + ((k + first) % ntile) * NKEY + i * box;
-        const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;  // past the end: zeros
+        const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;  // past the range: zeros
         const uint32_t off = v * C::KREG + bx * C::HALF_BYTES + i * box * 128;
         tma_load_4d(dst + off, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, h, phys);
       }
@@ -227,19 +274,41 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
   } else if (warp > PRODUCER) {
     // ------------------------------------------------------------ MMA issuers
     const int g = warp - PRODUCER - 1;
-    if (lane == 0) {
-      const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
-      const uint32_t tg = tbase + g * GCOLS;
-      for (int k = 0; k <= ntile; ++k) {
-        if (k < ntile) {
-          const int s = k % NS, b = k & 1;
-          if (!wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort)) break;
+    const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
+    const uint32_t tg = tbase + g * GCOLS;
+    for (int k = 0; k <= ntile; ++k) {
+      if (k < ntile) {
+        const int s = k % NS, b = k & 1;
+        bool ok = true;
+        if (lane == 0) {
+          ok = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
           // buffer b still holds P(k-2) until P(k-2).V has completed
-          if (k >= 2 && !wait_or_abort(smem_u32(pfree + 2 * g + b), static_cast<uint32_t>(((k - 2) >> 1) & 1),
-                                       p.err, s_abort))
-            break;
+          if (ok && k >= 2)
+            ok = wait_or_abort(smem_u32(pfree + 2 * g + b), static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err,
+                               s_abort);
+        }
+        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
+        const uint32_t kst = stage0 + s * C::STAGE;
+        if constexpr (MQ) {
+          // rows of the last block past the sequence end may hold anything
+          // (NaN included): zero them in the V tile, P is 0 there
+          const int tstart = t0 + ((k + first) % ntile) * NKEY;
+          const int vr0 = ctx - tstart;
+          if (vr0 < NKEY) {
+            uint8_t* vt = smem + (kst - smem_u32(smem)) + C::KREG;
+            const int first_row = vr0 > 0 ? vr0 : 0;
+            const int chunks = (NKEY - first_row) * 8;   // 16-byte chunks per d-half
+            for (int c = lane; c < C::HALVES * chunks; c += 32) {
+              const int hf = c / chunks, cc = c - hf * chunks;
+              *reinterpret_cast<uint4*>(vt + hf * C::HALF_BYTES + first_row * 128 + cc * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
           tc_fence_after();
-          const uint32_t kst = stage0 + s * C::STAGE;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t ad = smem_desc_sw128(qa + (ks / 4) * C::QHALF + (ks % 4) * 32, 0, 1024);
@@ -248,10 +317,14 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
           }
           tc_commit(smem_u32(sfull + 2 * g + b));
         }
-        if (k >= 1) {
-          const int j = k - 1, sj = j % NS, bj = j & 1;
-          if (!wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort))
-            break;
+      }
+      if (k >= 1) {
+        const int j = k - 1, sj = j % NS, bj = j & 1;
+        bool ok = true;
+        if (lane == 0)
+          ok = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
+        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t vst = stage0 + sj * C::STAGE + C::KREG;
           const uint32_t pa = tg + COL_S + bj * NKEY;
@@ -266,7 +339,8 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
           tc_commit(smem_u32(empty + sj));
         }
       }
-      // nothing of this thread's may still be running when TMEM is freed
+    }
+    if (lane == 0) {  // nothing of this thread's may still be running when TMEM is freed
       tc_commit(smem_u32(done + g));
       mbar_wait(smem_u32(done + g), 0u, nullptr);
     }
@@ -277,6 +351,8 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     uint64_t* g_pfull = pfull + 2 * grp;
     uint64_t* g_pfree = pfree + 2 * grp;
     const float qk_mult = p.qk_log2_scale;
+    // tokens this row may attend: [0, lim); the cascade prefix has no causal limit
+    const int lim = MQ ? (row_ok ? min(t1, ctx - QL + row / G + 1) : t0) : t1;
     float m_used = -CUDART_INF_F, lsum = 0.f;
     bool ok = true;
     for (int k = 0; k < ntile && ok; ++k) {
@@ -296,8 +372,8 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]) * qk_mult;
       }
-      const int valid = t1 - (t0 + ((k + first) % ntile) * NKEY);
-      if (valid < NKEY) {
+      const int valid = lim - (t0 + ((k + first) % ntile) * NKEY);
+      if (__any_sync(kFull, valid < NKEY)) {
 #pragma unroll
         for (int i = 0; i < NKEY; ++i)
           if (i >= valid) x[i] = -CUDART_INF_F;
@@ -367,27 +443,37 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     if (ok && ntile > 0)
       ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + ((ntile - 1) & 1)),
                                            static_cast<uint32_t>(((ntile - 1) >> 1) & 1), p.err, s_abort));
-    if (ok && ntile > 0) {
-      tc_fence_after();
-      const int64_t S_row = p.slots_per_row;
-      const int64_t piece = (row < rows ? (static_cast<int64_t>(row / G) * p.num_q_heads + h * G + row % G) : 0) *
-                                S_row + p.extra_slot + ps;
+    // ---- this row's result: a workspace piece, or (one split) the output row
+    const bool writes = MQ ? (t0 < ctx || (ctx == 0 && blockIdx.x == 0)) : ntile > 0;
+    const bool direct = MQ && nsplit <= 1;
+    const int64_t piece = orow * p.slots_per_row + (MQ ? static_cast<int64_t>(blockIdx.x) : p.extra_slot + blockIdx.z);
+    if (ok && writes) {
+      if (ntile > 0) tc_fence_after();
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      float* dst_row = direct ? p.out + orow * D : p.ws_o + piece * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[2][16];
-        tmem_ld16(tl + COL_O + c0, v[0]);
-        tmem_ld16(tl + COL_O + c0 + 16, v[1]);
-        tmem_wait_ld();
-        if (row < rows) {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + piece * D + c0);
+        if (ntile > 0) {
+          tmem_ld16(tl + COL_O + c0, v[0]);
+          tmem_ld16(tl + COL_O + c0 + 16, v[1]);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
+        }
+        if (row_ok) {
+          const float sc = direct ? inv : 1.f;
+          float4* dst = reinterpret_cast<float4*>(dst_row + c0);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]), __uint_as_float(v[i / 4][4 * (i % 4) + 1]),
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 2]),
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 3]));
+            dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]) * sc,
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 1]) * sc,
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 2]) * sc,
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 3]) * sc);
         }
       }
-      if (row < rows) {
+      if (row_ok && !direct) {
         p.ws_ml[piece * 2] = m_used;
         p.ws_ml[piece * 2 + 1] = lsum;
       }
@@ -402,42 +488,43 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
   }
 }
 
-}  // namespace
-
-int cascade_smem_bytes(int head_dim) {
-  // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
-  const int need = head_dim == 128 ? CascadeShape<128>::BYTES : CascadeShape<64>::BYTES;
-  return need > 120 * 1024 ? need : 120 * 1024;
+template <int D, int GROUPS>
+int tc_smem_bytes() {
+  // at least 120 KB when the CTA holds all TMEM (one per SM), 80 KB otherwise
+  const int need = TcShape<D, GROUPS>::BYTES;
+  const int floor_bytes = TcShape<D, GROUPS>::MINB == 1 ? 120 * 1024 : 80 * 1024;
+  return need > floor_bytes ? need : floor_bytes;
 }
 
-namespace {
-template <int D>
-cudaError_t launch_cascade_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                             cudaStream_t stream) {
-  auto kern = cascade_prefix_tc_kernel<D>;
-  const int smem = cascade_smem_bytes(D);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+template <int D, int GROUPS, bool MQ>
+cudaError_t launch_tc_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
+                        cudaStream_t stream) {
+  auto kern = paged_tc_attention_kernel<D, GROUPS, MQ>;
+  const int smem = tc_smem_bytes<D, GROUPS>();
   static bool configured[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  const int rows = p.batch * p.group;
-  const int nps = (p.prefix_len + p.prefix_split_tokens - 1) / p.prefix_split_tokens;
-  const dim3 grid((rows + kCascadeRowsTc - 1) / kCascadeRowsTc, p.num_kv_heads, nps);
-  return launch_pdl(kern, grid, dim3(CascadeShape<D>::THREADS), smem, stream, tk, tv, p);
+  cudaError_t e = set_smem_once(kern, smem, configured);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, grid, dim3(TcShape<D, GROUPS>::THREADS), smem, stream, tk, tv, p);
 }
 
 }  // namespace
 
 cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
-  if (p.head_dim == 128) return launch_cascade_t<128>(p, tk, tv, stream);
-  return launch_cascade_t<64>(p, tk, tv, stream);
+  const int rows = p.batch * p.group;
+  const int nps = (p.prefix_len + p.prefix_split_tokens - 1) / p.prefix_split_tokens;
+  const dim3 grid((rows + kCascadeRowsTc - 1) / kCascadeRowsTc, p.num_kv_heads, nps);
+  if (p.head_dim == 128) return launch_tc_t<128, 2, false>(p, tk, tv, grid, stream);
+  return launch_tc_t<64, 2, false>(p, tk, tv, grid, stream);
+}
+
+cudaError_t launch_multi_query_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t stream) {
+  const int rows = p.q_len * p.group;
+  const int nrb = (rows + 127) / 128;
+  const dim3 grid(p.max_splits, p.num_kv_heads * nrb, p.batch);
+  if (p.head_dim == 128) return launch_tc_t<128, 1, true>(p, tk, tv, grid, stream);
+  return launch_tc_t<64, 1, true>(p, tk, tv, grid, stream);
 }
 
 }  // namespace pkv

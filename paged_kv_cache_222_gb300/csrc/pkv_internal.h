@@ -126,6 +126,15 @@ cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tmap
                                   const CUtensorMap& tmap_v, cudaStream_t stream);
 cudaError_t launch_multi_query(const DecodeParams& p, const CUtensorMap& tmap_k,
                                const CUtensorMap& tmap_v, cudaStream_t stream);
+// Multi-token queries of 64 or more rows per (sequence, KV head) on tcgen05
+// (the cascade kernel's pipeline, one 128-row group per CTA).
+cudaError_t launch_multi_query_tc(const DecodeParams& p, const CUtensorMap& tmap_k,
+                                  const CUtensorMap& tmap_v, cudaStream_t stream);
+// Rows (q_len * G) from which multi-token queries take the tcgen05 kernel:
+// more than the 64 rows one mma.sync CTA covers (at 64 rows the mma.sync
+// kernel measured 0.39 of HBM against 0.28; at 96 rows 0.22, where the
+// tcgen05 kernel runs at its 128-row speed).
+constexpr int kMultiQueryTcRows = 65;
 
 // Multi-token query kernel: 64-token tiles, rows of (query token, head) pairs
 // in 16-row warp groups; the block ids of one split staged in shared memory.

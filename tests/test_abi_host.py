@@ -270,8 +270,10 @@ def test_multi_query_plan_shapes(lib):
     assert p.split_tokens % 64 == 0 and p.max_splits == -(-8192 // p.split_tokens)
     n = 64 * 4 * 64 * p.max_splits
     assert p.workspace_bytes == -(-n * 128 * 4 // 256) * 256 + n * 8
-    r, p = _mqplan(lib, desc, 2, 16, 64, 100, st=128)
-    assert r == L.PKV_OK and p.workers == 1 and p.max_splits == 1 and p.workspace_bytes == 0
+    r, p = _mqplan(lib, desc, 2, 16, 64, 100, st=128)     # 128 rows: the tcgen05 kernel
+    assert r == L.PKV_OK and p.workers == 0 and p.max_splits == 1 and p.workspace_bytes == 0
+    r, p = _mqplan(lib, desc, 2, 8, 64, 100)                # 64 rows: one token lane
+    assert r == L.PKV_OK and p.workers == 1
     r, p = _mqplan(lib, desc, 2, 2, 64, 100)
     assert r == L.PKV_OK and p.workers == 4
 

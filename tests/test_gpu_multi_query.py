@@ -71,8 +71,12 @@ def _oracle(case):
     (4, 8, 1, 128, 32),     # 32 rows: two lanes
     (8, 4, 1, 64, 32),      # 32 rows
     (6, 8, 1, 128, 16),     # 48 rows: one lane, one partial row block
-    (16, 8, 2, 128, 16),    # 128 rows: two row blocks per head
-    (16, 16, 1, 64, 16),    # 256 rows
+    (16, 8, 2, 128, 16),    # 64 rows
+    (16, 8, 1, 128, 32),    # 128 rows: the tcgen05 kernel, whole 32-token blocks per TMA box
+    (12, 8, 1, 128, 16),    # 96 rows: a partly filled 128-row group
+    (12, 16, 1, 128, 16),   # 192 rows: a partly filled second 128-row group
+    (10, 32, 2, 64, 32),    # 160 rows, D = 64
+    (16, 16, 1, 64, 16),    # 256 rows: two row blocks per head
 ])
 @pytest.mark.parametrize("split_tokens", [0, 64, 192])
 def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, bs, split_tokens):
@@ -151,3 +155,21 @@ def test_full_size_gqa_workload_sampled(q_len):
         want = PA.multi_query_attention(qq, kc, vc, PA.BF16, table, np.array([c0 + q_len]), case["scale"])
         got = out[b, :, h * G:(h + 1) * G]
         assert np.abs(got - want[0]).max() <= 2e-3, (b, h)
+
+
+@pytest.mark.parametrize("q_len,H_q,H_kv", [(8, 16, 1), (16, 8, 1)])
+def test_tcgen05_path_short_and_empty_contexts(q_len, H_q, H_kv):
+    case = _small_case([0, 3, q_len, q_len + 1, 70, 1100], q_len, H_q, H_kv, 128, 16, seed=20260304 + q_len)
+    for st in (0, 64, 320):
+        out = _run(case, st)
+        want = _oracle(case)
+        assert np.isfinite(out).all()
+        assert np.all(out[0] == 0.0) and np.all(out[1, :q_len - 3] == 0.0)
+        assert np.abs(out - want).max() <= 2e-3
+
+
+def test_tcgen05_split_count_does_not_change_the_result():
+    case = _small_case([5000, 333, 4096], 16, 64, 8, 128, 16, seed=20260305)
+    outs = [_run(case, st) for st in (64, 256, 1024, 4096, 16384)]
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 1e-5
