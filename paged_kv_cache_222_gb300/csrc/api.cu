@@ -860,8 +860,9 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
   int32_t st = split_tokens;
   if (st == 0) {
     // largest power of two (256..4096) that still gives about four waves of
-    // two CTAs per SM when every sequence is as long as the bound
-    const int64_t want = static_cast<int64_t>(sms) * 2 * 4;
+    // CTAs (two per SM on the mma.sync kernel, one on the tcgen05 kernel) when
+    // every sequence is as long as the bound
+    const int64_t want = static_cast<int64_t>(sms) * (tc ? 1 : 2) * 4;
     st = 4096;
     while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
   }

@@ -72,8 +72,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 // rows all read the same prefix; 1 for multi-token queries, whose rows of one
 // (sequence, KV head) are at most 128 per row block), the ring of K/V stages
 // and the threads (4 softmax warps per group, a producer warp, one MMA-issuer
-// warp per group).  Two groups take all 512 TMEM columns (one CTA per SM);
-// one group takes 256, and two such CTAs share an SM.
+// warp per group).  One CTA per SM with all 512 TMEM columns.  Two groups
+// split them (O and a double buffer of S that P overwrites in place); one
+// group keeps P in buffers of its own (SEP), so that S(k+2) never waits for
+// P(k).V, and uses the shared memory for a deeper ring of stages (its tiles
+// come from HBM, not from L2).
 template <int D, int GROUPS_>
 struct TcShape {
   static constexpr int GROUPS = GROUPS_;
@@ -85,12 +88,13 @@ struct TcShape {
   static constexpr int KREG = HALVES * HALF_BYTES;    // K (or V) tile
   static constexpr int STAGE = 2 * KREG;
   static constexpr int QBYTES = GROUPS * HALVES * QHALF;
-  static constexpr int NS = GROUPS == 2 ? 4 : 2;
-  static constexpr int NBARS = 2 * NS + 6 * GROUPS + GROUPS;  // full, empty; sfull, pfull, pfree x2; done
+  static constexpr bool SEP = GROUPS == 1;            // P in TMEM columns of its own
+  static constexpr int NS = GROUPS == 2 ? 4 : 5;
+  static constexpr int NBARS = 2 * NS + 8 * GROUPS + GROUPS;  // full, empty; sfull, sfree, pfull, pfree x2; done
   static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
   static constexpr int THREADS = 32 * (4 * GROUPS + 1 + GROUPS);
-  static constexpr uint32_t TCOLS = 256 * GROUPS;
-  static constexpr int MINB = GROUPS == 2 ? 1 : 2;    // CTAs per SM
+  static constexpr uint32_t TCOLS = 512;
+  static constexpr int MINB = 1;                      // CTAs per SM
 };
 
 // MQ = false: cascade prefix.  Rows (b, g) of KV head blockIdx.y, 256 per CTA
@@ -109,13 +113,16 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS;
   constexpr int kMaxBlocks = 1024;                    // block ids of one range, in shared memory
   constexpr uint32_t TCOLS = C::TCOLS;
-  constexpr uint32_t GCOLS = 256;                     // TMEM columns of one group
-  constexpr uint32_t COL_O = 0, COL_S = D;            // within a group's columns
+  constexpr uint32_t GCOLS = TCOLS / GROUPS;          // TMEM columns of one group
+  constexpr bool SEP = C::SEP;
+  // within a group's columns: O, the S double buffer, the P double buffer
+  // (P over S unless SEP)
+  constexpr uint32_t COL_O = 0, COL_S = D, COL_P = SEP ? D + 2 * NKEY : D;
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
   constexpr int PRODUCER = 4 * GROUPS;                // warp index
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(COL_S + 2 * NKEY <= GCOLS, "TMEM columns");
+  static_assert(COL_P + 2 * NKEY <= GCOLS, "TMEM columns");
   static_assert(!MQ || GROUPS == 1, "one group per multi-token CTA");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -131,7 +138,8 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   uint64_t* full = bars;
   uint64_t* empty = full + NS;
   uint64_t* sfull = empty + NS;       // [GROUPS][2]
-  uint64_t* pfull = sfull + 2 * GROUPS;
+  uint64_t* sfree = sfull + 2 * GROUPS;  // used when SEP
+  uint64_t* pfull = sfree + 2 * GROUPS;
   uint64_t* pfree = pfull + 2 * GROUPS;
   uint64_t* done = pfree + 2 * GROUPS;  // [GROUPS]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + GROUPS);
@@ -145,6 +153,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     }
     for (int i = 0; i < 2 * GROUPS; ++i) {
       mbar_init(smem_u32(sfull + i), 1);
+      mbar_init(smem_u32(sfree + i), 4);
       mbar_init(smem_u32(pfull + i), 4);
       mbar_init(smem_u32(pfree + i), 1);
     }
@@ -282,10 +291,11 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         bool ok = true;
         if (lane == 0) {
           ok = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
-          // buffer b still holds P(k-2) until P(k-2).V has completed
+          // buffer b: the softmax has read S(k-2) (SEP), or P(k-2).V has
+          // completed (P over S)
           if (ok && k >= 2)
-            ok = wait_or_abort(smem_u32(pfree + 2 * g + b), static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err,
-                               s_abort);
+            ok = wait_or_abort(smem_u32((SEP ? sfree : pfree) + 2 * g + b),
+                               static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err, s_abort);
         }
         if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
         const uint32_t kst = stage0 + s * C::STAGE;
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         if (lane == 0) {
           tc_fence_after();
           const uint32_t vst = stage0 + sj * C::STAGE + C::KREG;
-          const uint32_t pa = tg + COL_S + bj * NKEY;
+          const uint32_t pa = tg + COL_P + bj * NKEY;
 #pragma unroll
           for (int kk = 0; kk < NKEY / 16; ++kk) {
             // MN-major V: 8-key groups 1024 B apart, d-halves HALF_BYTES apart
@@ -348,6 +358,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     // ------------------------------------------------------------ softmax
     const uint32_t tl = tbase + grp * GCOLS + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     uint64_t* g_sfull = sfull + 2 * grp;
+    uint64_t* g_sfree = sfree + 2 * grp;
     uint64_t* g_pfull = pfull + 2 * grp;
     uint64_t* g_pfree = pfree + 2 * grp;
     const float qk_mult = p.qk_log2_scale;
@@ -371,6 +382,11 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         for (int c = 0; c < NKEY / 16; ++c)
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]) * qk_mult;
+      }
+      if constexpr (SEP) {  // S[b] may be overwritten
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(g_sfree + b));
       }
       const int valid = lim - (t0 + ((k + first) % ntile) * NKEY);
       if (__any_sync(kFull, valid < NKEY)) {
@@ -418,6 +434,12 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         tmem_wait_st();
       }
       lsum *= alpha;
+      if (SEP && k >= 2) {  // P(k-2).V has read P[b]
+        ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + b), static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err,
+                                             s_abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -431,8 +453,8 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
           hi[i] = pack_bf16x2(p0, p1);
           lo[i] = pack_bf16x2(p0 - bf16lo_to_f32(hi[i]), p1 - bf16hi_to_f32(hi[i]));
         }
-        tmem_st16(tl + COL_S + b * NKEY + c0, hi);          // P(k) over S(k)
-        tmem_st16(tl + COL_S + b * NKEY + NKEY / 2 + c0, lo);
+        tmem_st16(tl + COL_P + b * NKEY + c0, hi);
+        tmem_st16(tl + COL_P + b * NKEY + NKEY / 2 + c0, lo);
       }
       lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_wait_st();
@@ -490,10 +512,9 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
 
 template <int D, int GROUPS>
 int tc_smem_bytes() {
-  // at least 120 KB when the CTA holds all TMEM (one per SM), 80 KB otherwise
+  // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
   const int need = TcShape<D, GROUPS>::BYTES;
-  const int floor_bytes = TcShape<D, GROUPS>::MINB == 1 ? 120 * 1024 : 80 * 1024;
-  return need > floor_bytes ? need : floor_bytes;
+  return need > 120 * 1024 ? need : 120 * 1024;
 }
 
 template <int D, int GROUPS, bool MQ>
