@@ -16,35 +16,31 @@ namespace pkv {
 namespace {
 
 // ----------------------------------------------------------------------------
-// Cascade prefix kernel on the 5th-generation tensor cores (tcgen05 + TMEM),
-// pipelined.  One CTA per SM owns 256 query rows of one KV head — two groups
-// of 128 rows that share every K/V tile — over one range of prefix tokens.
-// Its eleven warps have fixed roles:
-//   warps 0-7  softmax: group g = warp / 4; thread t of the group is its
-//              query row t (= TMEM lane t, in the group's half of the columns)
-//   warp 8     TMA producer: 64-token K and V tiles into a ring of four
-//              128B-swizzled stages, one box per lane
-//   warps 9-10 MMA issuers, one per group (one lane each):
+// Paged attention of many query rows on the 5th-generation tensor cores
+// (tcgen05 + TMEM), pipelined: the cascade prefix (all B * G query rows of a
+// KV head against the shared prefix) and multi-token queries with more than
+// 64 rows per (sequence, KV head).  One CTA per SM; its warps have fixed roles:
+//   softmax warps (4 per 128-row group): thread t of a group is its query row
+//              t (= TMEM lane t, in the group's columns)
+//   one TMA producer warp: 64-token K and V tiles into a ring of stages of
+//              128B-swizzled shared memory, one whole-block box per lane
+//   one MMA-issuer warp per group (one lane issues):
 //              S_g(k) = Q_g K(k)^T, then O_g += P_g(k-1) V(k-1)
-// TMEM (512 columns): group g owns [256 g, 256 g + 256): O [0, D) fp32 and a
-// double buffer of S [D, D + 128) fp32, each buffer overwritten in place by
-// its P = 2^(s - m) as bf16 hi | lo pairs.  Q sits in shared memory in the
-// K-major 128B-swizzled layout (A operand of S through a matrix descriptor);
-// K is a K-major and V an MN-major B operand.  While one group's softmax
-// turns S(k) into P(k), the tensor core works on the other group and on
-// S(k+1) and O += P(k-1) V.  S_g(k) goes into the buffer that P_g(k-2)
-// occupied only after P_g(k-2).V has completed (tcgen05 orders MMAs only on
-// one accumulator).  Hand-offs are mbarriers: full / empty per stage (TMA
-// bytes; one commit per group after the stage's P.V), and per group and
-// buffer sfull / pfree (MMA commits) and pfull (one arrive per softmax warp).
+// Q sits in shared memory in the K-major 128B-swizzled layout (A operand of S
+// through a matrix descriptor); K is a K-major and V an MN-major B operand; P
+// (as bf16 hi | lo pairs) comes from TMEM.  While a group's softmax turns
+// S(k) into P(k), the tensor core works on the other group and on S(k+1) and
+// O += P(k-1) V.  Hand-offs are mbarriers: full / empty per stage (TMA bytes;
+// one commit per group after the stage's P.V), and per group and buffer
+// sfull / pfree (MMA commits) and sfree / pfull (one arrive per softmax warp).
 // The softmax keeps a lazy running max: O in TMEM is rescaled only when the
 // max grows by more than 2^8 (then after the previous P.V has completed), so
-// P stays <= 256.  The CTAs of one KV head read the same prefix tiles; each
-// starts at a different tile of its range (the online softmax takes tiles in
-// any order) so that they do not all ask L2 for the same lines at once.
-// Every wait is bounded; a time-out records the error, raises a shared abort
-// flag that ends every role's loop, and the CTA drains its copies and MMAs
-// before it frees TMEM.
+// P stays <= 256.  The cascade CTAs of one KV head read the same prefix
+// tiles; each starts at a different tile of its range (the online softmax
+// takes tiles in any order) so that they do not all ask L2 for the same
+// lines at once.  Every wait is bounded; a time-out records the error, raises
+// a shared abort flag that ends every role's loop, and the CTA drains its
+// copies and MMAs before it frees TMEM.
 // ----------------------------------------------------------------------------
 
 // Wait for a barrier phase; false once the CTA aborts (or on time-out, which
