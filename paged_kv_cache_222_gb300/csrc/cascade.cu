@@ -1,13 +1,21 @@
-// Cascade (shared-prefix) decode: the prefix kernel.  When every sequence of
-// the batch starts with the same `prefix_len` tokens held in the same physical
+// Tensor-core (tcgen05) paged attention for many query rows per KV head.
+//
+// Cascade (shared-prefix) decode, the prefix part: when every sequence of the
+// batch starts with the same `prefix_len` tokens held in the same physical
 // blocks (shared by reference: [FN] "Sub-Millisecond Token Scheduling...",
 // "Paged KV-Cache with Radix Tree Prefix Cache", copy-on-write prefix blocks),
 // the prefix part of decode attention is one dense product per KV head,
 //   S = Q_h K_prefix^T,  Q_h = the B*G query rows (b, g) of KV head h,
-// followed by the online softmax and P V_prefix.  Each CTA takes 128 query
+// followed by the online softmax and P V_prefix.  Each CTA takes 256 query
 // rows of one KV head over one range of prefix tokens and writes (acc, m, l)
 // per row into the workspace slot reserved for its range; the combine kernel
 // of decode.cu merges those with the private-suffix splits.
+//
+// Multi-token queries ([SC] "LLM inference: prefill, decode, KV cache", "7.
+// Practical applications", item 3, and "9. Failure modes and limitations",
+// item 3) with more than 64 rows (q_len * G) per (sequence, KV head): each CTA
+// takes 128 rows of one (sequence, KV head) over one split of the sequence's
+// own tokens, with a causal limit per row.
 
 #include "decode_common.cuh"
 #include "pkv_tc.cuh"
