@@ -74,33 +74,44 @@ def parse_args():
 # ---------------------------------------------------------------- oracle leg
 
 def _oracle_unit_worker(args):
-    """Oracle decode of one (sequence, KV head) unit on its own blocks."""
+    """Oracle decode of one (sequence, KV head) unit on its own blocks;
+    returns (seconds, (b, h), output [G, D])."""
     import numpy as np
     from oracle import paged_attention as PA
-    q_bits, k_blocks, v_blocks, ctx, bs, scale = args
+    key, q_bits, k_blocks, v_blocks, kind, ks, vs, ctx, bs, scale = args
     n = k_blocks.shape[0]
     table = np.arange(n, dtype=np.int32)[None, :]
     t0 = time.perf_counter()
-    out = PA.decode_attention(q_bits[None], k_blocks, v_blocks, PA.BF16, table, np.array([ctx]), scale)
-    return time.perf_counter() - t0, out.shape
+    if kind == "e4m3":
+        out = PA.decode_attention(q_bits[None], k_blocks, v_blocks, PA.E4M3, table, np.array([ctx]), scale,
+                                  np.array([[ks]], dtype=np.float32), np.array([[vs]], dtype=np.float32))
+    else:
+        out = PA.decode_attention(q_bits[None], k_blocks, v_blocks, PA.BF16, table, np.array([ctx]), scale)
+    return time.perf_counter() - t0, key, out[0]
 
 
 def _unit_payload(case, b, h, ctx_attended):
     import torch
-    from tests.gpu_support import bits16
+    from tests.gpu_support import bits16, bytes8
     G = case["H_q"] // case["H_kv"]
     n = -(-ctx_attended // case["bs"])
     ids = case["block_tables"][b, :n].to(torch.int64).to(case["k_cache"].device)
-    kb = bits16(case["k_cache"][ids][:, h:h + 1])
-    vb = bits16(case["v_cache"][ids][:, h:h + 1])
+    raw = bytes8 if case["kv"] == "e4m3" else bits16
+    kb = raw(case["k_cache"][ids][:, h:h + 1])
+    vb = raw(case["v_cache"][ids][:, h:h + 1])
     q = bits16(case["q"][0, b, h * G:(h + 1) * G])
-    return (q, kb, vb, ctx_attended, case["bs"], case["scale"])
+    ks = vs = None
+    if case["kv"] == "e4m3":
+        ks = float(case["k_scale"][b, h])
+        vs = float(case["v_scale"][b, h])
+    return ((b, h), q, kb, vb, case["kv"], ks, vs, ctx_attended, case["bs"], case["scale"])
 
 
-def oracle_throughput(case, seconds, order_seed=0):
+def oracle_throughput(case, seconds, order_seed=0, return_outputs=False):
     """Run the oracle over (sequence, KV head) units in a spawn process pool,
     one single-threaded process per host core, until `seconds` of wall time
-    are used.  Returns (GB/s of KV attended, units done, processes)."""
+    are used.  Returns (GB/s of KV attended, units done, processes, wall
+    seconds[, {(b, h): oracle output [G, D]}])."""
     import multiprocessing as mp
     import numpy as np
     cores = len(os.sched_getaffinity(0))
@@ -115,6 +126,7 @@ def oracle_throughput(case, seconds, order_seed=0):
     ctxm = mp.get_context("spawn")
     done_bytes = 0
     done = 0
+    outputs = {}
     with ctxm.Pool(procs) as pool:
         # warm the workers (imports) before timing
         pool.map(_noop, range(procs))
@@ -123,12 +135,16 @@ def oracle_throughput(case, seconds, order_seed=0):
         while i < len(units) and time.perf_counter() - t0 < seconds:
             batch = units[i:i + procs]
             payloads = [_unit_payload(case, b, h, ctx[b]) for b, h in batch]
-            pool.map(_oracle_unit_worker, payloads)
+            for _, key, out in pool.map(_oracle_unit_worker, payloads):
+                outputs[key] = out
             done_bytes += sum(per_unit_bytes(b) for b, _ in batch)
             done += len(batch)
             i += procs
         wall = time.perf_counter() - t0
-    return done_bytes / wall / 1e9, done, procs, wall
+    throughput_gbs = done_bytes / wall / 1e9
+    if return_outputs:
+        return throughput_gbs, done, procs, wall, outputs
+    return throughput_gbs, done, procs, wall
 
 
 def _noop(_):
@@ -474,11 +490,16 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
     }
     if not args.no_cpu_baseline and world == 1:
-        gbs, n, procs, wall = oracle_throughput(case, args.cpu_seconds)
+        gbs, n, procs, wall, ref = oracle_throughput(case, args.cpu_seconds, return_outputs=True)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle",
                                 "sample": f"{n} of {B * case['H_kv']} (sequence, KV head) units of the "
                                           f"{args.workload} step, {wall:.1f} s wall, float64 numpy, "
                                           f"one process per core"}
+        # the timed steps' output against the oracle on the same units
+        got = out.cpu().numpy()
+        G = case["H_q"] // case["H_kv"]
+        err = max((float(abs(got[b, h * G:(h + 1) * G] - o).max()) for (b, h), o in ref.items()), default=None)
+        line["parity"] = {"max_abs_err": err, "units": len(ref), "tolerance": 5e-3 if fp8 else 2e-3}
     print(json.dumps(line), flush=True)
 
 
