@@ -328,6 +328,19 @@ enum {
  */
 int32_t pkv_get_device_error(pkv_stream_t stream);
 
+/*
+ * Self-test of the device-side failure detection: launches one CTA that
+ * waits on a barrier nothing ever arrives on, with a limit of `limit_us`
+ * microseconds (1..1000000) instead of the kernels' one second.
+ *   which 0: a plain bounded mbarrier wait;
+ *   which 1: the abort path of the tensor-core attention kernels (tensor
+ *            memory held, one wait times out and raises the CTA's abort flag,
+ *            the other waits leave on it, tensor memory is freed).
+ * The kernel returns normally; afterwards pkv_get_device_error reads
+ * PKV_DEVERR_WAIT_TIMEOUT and the context stays usable.
+ */
+pkv_status pkv_selftest_wait_timeout(int32_t which, int32_t limit_us, pkv_stream_t stream);
+
 /* Human-readable name of a status. */
 const char* pkv_status_string(int32_t status);
 

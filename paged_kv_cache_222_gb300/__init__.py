@@ -303,6 +303,16 @@ def device_error(device=None):
         return library().pkv_get_device_error(_stream(dev))
 
 
+def selftest_wait_timeout(which, limit_us=20000, device=None):
+    """Run the device-side bounded-wait self-test (include/pkv.h); returns the
+    device error word read afterwards (1 = PKV_DEVERR_WAIT_TIMEOUT)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _lib.check(library().pkv_selftest_wait_timeout(int(which), int(limit_us), _stream(dev)),
+                   "pkv_selftest_wait_timeout")
+    return device_error(dev)
+
+
 def trace_enable(on=True):
     _lib.check(library().pkv_trace_enable(1 if on else 0), "pkv_trace_enable")
 

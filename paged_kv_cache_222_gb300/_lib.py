@@ -89,6 +89,7 @@ SIGNATURES = {
                                        _P]),
     "pkv_host_alloc": (_I32, [ctypes.c_size_t, ctypes.POINTER(_P)]),
     "pkv_host_free": (_I32, [_P]),
+    "pkv_selftest_wait_timeout": (_I32, [_I32, _I32, _P]),
     "pkv_get_device_error": (_I32, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_last_error": (ctypes.c_char_p, []),

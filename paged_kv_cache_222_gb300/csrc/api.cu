@@ -543,6 +543,19 @@ pkv_status pkv_copy_blocks_between(const void* src_k, const void* src_v, int64_t
   return PKV_OK;
 }
 
+pkv_status pkv_selftest_wait_timeout(int32_t which, int32_t limit_us, pkv_stream_t stream) {
+  if (which != 0 && which != 1) return fail(PKV_ERR_INVALID_ARG, "which %d (0 or 1)", which);
+  if (limit_us < 1 || limit_us > 1000000) return fail(PKV_ERR_INVALID_ARG, "limit_us %d (1..1000000)", limit_us);
+  int dev;
+  DeviceState* st;
+  pkv_status s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  cudaError_t e = pkv::launch_wait_selftest(which, static_cast<uint64_t>(limit_us) * 1000ull, st->err,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_host_alloc(size_t bytes, void** ptr) {
   if (ptr == nullptr) return fail(PKV_ERR_INVALID_ARG, "ptr is NULL");
   *ptr = nullptr;

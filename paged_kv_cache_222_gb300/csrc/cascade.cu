@@ -53,7 +53,8 @@ namespace {
 
 // Wait for a barrier phase; false once the CTA aborts (or on time-out, which
 // records the error and raises the abort flag).
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err, volatile int* abort) {
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err, volatile int* abort,
+                                              uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t n = 1;; ++n) {
@@ -63,7 +64,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
       const uint64_t t = global_timer_ns();
       if (t0 == 0) {
         t0 = t;
-      } else if (t - t0 > kWaitLimitNs) {
+      } else if (t - t0 > limit_ns) {
         record_error(err, kDevErrWaitTimeout);
         *abort = 1;
         return false;
@@ -514,6 +515,52 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   }
 }
 
+// Self-test of the bounded waits and of the abort path of the tensor-core
+// kernels: barriers that nothing ever arrives on.
+//   which 0: one thread waits with mbar_wait until the limit, records the
+//            time-out, returns.
+//   which 1: as a tensor-core CTA: warp 0 holds all TMEM; thread 32 waits
+//            with wait_or_abort until the limit (recording the time-out and
+//            raising the abort flag); the threads of warps 2-3 wait on another
+//            such barrier and leave when they see the flag; then the CTA
+//            frees TMEM as the attention kernels do.
+__global__ void __launch_bounds__(128) wait_selftest_kernel(int which, uint64_t limit_ns, int* err) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (which == 1 && warp == 0) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (which == 0) {
+    if (threadIdx.x == 0) mbar_wait(smem_u32(&bars[0]), 0u, err, limit_ns);
+    return;
+  }
+  volatile int* abort = &s_abort;
+  if (threadIdx.x == 32) {
+    wait_or_abort(smem_u32(&bars[0]), 0u, err, abort, limit_ns);
+  } else if (warp >= 2) {
+    // leaves when the abort flag rises, or after four limits of its own
+    wait_or_abort(smem_u32(&bars[1]), 0u, err, abort, 4 * limit_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(s_tmem, 512);
+  }
+}
+
 template <int D, int GROUPS>
 int tc_smem_bytes() {
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
@@ -541,6 +588,11 @@ cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tk, 
   const dim3 grid((rows + kCascadeRowsTc - 1) / kCascadeRowsTc, p.num_kv_heads, nps);
   if (p.head_dim == 128) return launch_tc_t<128, 2, false>(p, tk, tv, grid, stream);
   return launch_tc_t<64, 2, false>(p, tk, tv, grid, stream);
+}
+
+cudaError_t launch_wait_selftest(int which, uint64_t limit_ns, int* err, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 128, 0, stream>>>(which, limit_ns, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_multi_query_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -69,9 +69,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // and a phase that completes while the thread reads it would be noticed late.
 constexpr uint32_t kWaitTriesPerClockRead = 256;
 
-// Wait for phase `parity` of the barrier, at most about kWaitLimitNs.  On
-// time-out the error word gets PKV_DEVERR_WAIT_TIMEOUT and false is returned.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+// Wait for phase `parity` of the barrier, at most about `limit_ns` (one
+// second unless a self-test asks for less).  On time-out the error word gets
+// PKV_DEVERR_WAIT_TIMEOUT and false is returned.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t n = 1;; ++n) {
@@ -80,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
       const uint64_t t = global_timer_ns();
       if (t0 == 0) {
         t0 = t;
-      } else if (t - t0 > kWaitLimitNs) {
+      } else if (t - t0 > limit_ns) {
         record_error(err, kDevErrWaitTimeout);
         return false;
       }

@@ -130,6 +130,9 @@ cudaError_t launch_multi_query(const DecodeParams& p, const CUtensorMap& tmap_k,
 // (the cascade kernel's pipeline, one 128-row group per CTA).
 cudaError_t launch_multi_query_tc(const DecodeParams& p, const CUtensorMap& tmap_k,
                                   const CUtensorMap& tmap_v, cudaStream_t stream);
+// Self-test of the bounded waits (0: mbarrier wait; 1: tensor-core CTA abort
+// path); records PKV_DEVERR_WAIT_TIMEOUT after about limit_ns.
+cudaError_t launch_wait_selftest(int which, uint64_t limit_ns, int* err, cudaStream_t stream);
 // Rows (q_len * G) from which multi-token queries take the tcgen05 kernel:
 // more than the 64 rows one mma.sync CTA covers (at 64 rows the mma.sync
 // kernel measured 0.39 of HBM against 0.28; at 96 rows 0.22, where the

@@ -309,3 +309,9 @@ def test_copy_between_pools_rejects_bad_arguments_on_host(lib, kw, code):
                                      ctypes.c_void_p(1024), ctypes.c_void_p(2048), kw.get("n_pairs", 2),
                                      kw.get("max_ctas", 0), None)
     assert st == code
+
+
+def test_wait_selftest_rejects_bad_arguments_before_any_launch(lib):
+    assert lib.pkv_selftest_wait_timeout(2, 1000, None) == L.PKV_ERR_INVALID_ARG
+    assert lib.pkv_selftest_wait_timeout(0, 0, None) == L.PKV_ERR_INVALID_ARG
+    assert lib.pkv_selftest_wait_timeout(1, 1000001, None) == L.PKV_ERR_INVALID_ARG
