@@ -35,8 +35,9 @@ namespace {
 //   one MMA-issuer warp per group (one lane issues):
 //              S_g(k) = Q_g K(k)^T, then O_g += P_g(k-1) V(k-1)
 // Q sits in shared memory in the K-major 128B-swizzled layout (A operand of S
-// through a matrix descriptor); K is a K-major and V an MN-major B operand; P
-// (as bf16 hi | lo pairs) comes from TMEM.  While a group's softmax turns
+// through a matrix descriptor) when the CTA has two groups, and in TMEM when
+// it has one; K is a K-major and V an MN-major B operand; P (as bf16 hi | lo
+// pairs) comes from TMEM.  While a group's softmax turns
 // S(k) into P(k), the tensor core works on the other group and on S(k+1) and
 // O += P(k-1) V.  Hand-offs are mbarriers: full / empty per stage (TMA bytes;
 // one commit per group after the stage's P.V), and per group and buffer
@@ -80,8 +81,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 // warp per group).  One CTA per SM with all 512 TMEM columns.  Two groups
 // split them (O and a double buffer of S that P overwrites in place); one
 // group keeps P in buffers of its own (SEP), so that S(k+2) never waits for
-// P(k).V, and uses the shared memory for a deeper ring of stages (its tiles
-// come from HBM, not from L2).
+// P(k).V, and Q in TMEM as well (S = Q K^T with A from TMEM), which leaves
+// the shared memory to a deeper ring of six stages (its tiles come from HBM,
+// not from L2, and the bytes in flight set its speed).
 template <int D, int GROUPS_>
 struct TcShape {
   static constexpr int GROUPS = GROUPS_;
@@ -92,10 +94,12 @@ struct TcShape {
   static constexpr int HALF_BYTES = NKEY * 128;       // one d-half of a K (or V) tile
   static constexpr int KREG = HALVES * HALF_BYTES;    // K (or V) tile
   static constexpr int STAGE = 2 * KREG;
-  static constexpr int QBYTES = GROUPS * HALVES * QHALF;
   static constexpr bool SEP = GROUPS == 1;            // P in TMEM columns of its own
-  static constexpr int NS = GROUPS == 2 ? 4 : 5;
-  static constexpr int NBARS = 2 * NS + 8 * GROUPS + GROUPS;  // full, empty; sfull, sfree, pfull, pfree x2; done
+  static constexpr bool QT = GROUPS == 1;             // Q in TMEM too (A operand of S from TMEM)
+  static constexpr int QBYTES = QT ? 0 : GROUPS * HALVES * QHALF;
+  static constexpr int NS = GROUPS == 2 ? 4 : 6;
+  // full, empty; sfull, sfree, pfull, pfree x2; done; Q in TMEM
+  static constexpr int NBARS = 2 * NS + 8 * GROUPS + GROUPS + 1;
   static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
   static constexpr int THREADS = 32 * (4 * GROUPS + 1 + GROUPS);
   static constexpr uint32_t TCOLS = 512;
@@ -123,11 +127,13 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   // within a group's columns: O, the S double buffer, the P double buffer
   // (P over S unless SEP)
   constexpr uint32_t COL_O = 0, COL_S = D, COL_P = SEP ? D + 2 * NKEY : D;
+  constexpr uint32_t COL_Q = COL_P + 2 * NKEY;        // Q as bf16 pairs when QT
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
   constexpr int PRODUCER = 4 * GROUPS;                // warp index
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(COL_P + 2 * NKEY <= GCOLS, "TMEM columns");
+  static_assert(!C::QT || (SEP && COL_Q + D / 2 <= GCOLS), "TMEM columns for Q");
   static_assert(!MQ || GROUPS == 1, "one group per multi-token CTA");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -147,7 +153,8 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   uint64_t* pfull = sfree + 2 * GROUPS;
   uint64_t* pfree = pfull + 2 * GROUPS;
   uint64_t* done = pfree + 2 * GROUPS;  // [GROUPS]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + GROUPS);
+  uint64_t* qready = done + GROUPS;     // Q is in TMEM (one arrive per softmax warp)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(qready + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_blk = reinterpret_cast<int*>(s_tmem + 4);
 
@@ -163,6 +170,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
       mbar_init(smem_u32(pfree + i), 1);
     }
     for (int g = 0; g < GROUPS; ++g) mbar_init(smem_u32(done + g), 1);
+    mbar_init(smem_u32(qready), 4);
     *s_abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
@@ -229,24 +237,49 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   // output row of this query row: (b, hq) for the cascade, (b, i, hq) flattened
   const int64_t orow = MQ ? (b_rows + row / G) * H_q + h * G + row % G
                           : static_cast<int64_t>(row / G) * H_q + h * G + row % G;
+  uint4 w[D / 8];  // the row of Q: every load issued before the first store
   if (warp < PRODUCER) {
     const uint16_t* qr = row_ok ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
-    uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
-    uint4 w[D / 8];  // every load issued before the first store
 #pragma unroll
     for (int c = 0; c < D / 8; ++c)
       w[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (!C::QT) {
+      uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const int hf = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
+      for (int c = 0; c < D / 8; ++c) {
+        const int hf = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
+      }
+      fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
     }
-    fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *s_tmem;
+  if constexpr (C::QT) {
+    // row r of Q into TMEM lane r as bf16 pairs (element 2j in the low half
+    // of column j, the memory order of the loaded words)
+    if (warp < PRODUCER) {
+      const uint32_t tq = tbase + COL_Q + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[4 * j] = w[4 * c + j].x;
+          v[4 * j + 1] = w[4 * c + j].y;
+          v[4 * j + 2] = w[4 * c + j].z;
+          v[4 * j + 3] = w[4 * c + j].w;
+        }
+        tmem_st16(tq + 16 * c, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(qready));
+    }
+  }
 
   if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
@@ -290,19 +323,24 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     const int g = warp - PRODUCER - 1;
     const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
     const uint32_t tg = tbase + g * GCOLS;
-    for (int k = 0; k <= ntile; ++k) {
+    bool ok = true;
+    if constexpr (C::QT) {
+      if (lane == 0) ok = wait_or_abort(smem_u32(qready), 0u, p.err, s_abort);
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+    }
+    for (int k = 0; k <= ntile && ok; ++k) {
       if (k < ntile) {
         const int s = k % NS, b = k & 1;
-        bool ok = true;
+        bool ok2 = true;
         if (lane == 0) {
-          ok = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
+          ok2 = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
           // buffer b: the softmax has read S(k-2) (SEP), or P(k-2).V has
           // completed (P over S)
-          if (ok && k >= 2)
-            ok = wait_or_abort(smem_u32((SEP ? sfree : pfree) + 2 * g + b),
+          if (ok2 && k >= 2)
+            ok2 = wait_or_abort(smem_u32((SEP ? sfree : pfree) + 2 * g + b),
                                static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err, s_abort);
         }
-        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
+        if (!__shfl_sync(kFull, ok2 ? 1 : 0, 0)) break;
         const uint32_t kst = stage0 + s * C::STAGE;
         if constexpr (MQ) {
           // rows of the last block past the sequence end may hold anything
@@ -325,20 +363,24 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         if (lane == 0) {
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t ad = smem_desc_sw128(qa + (ks / 4) * C::QHALF + (ks % 4) * 32, 0, 1024);
-            const uint64_t bd = smem_desc_sw128(kst + (ks / 4) * C::HALF_BYTES + (ks % 4) * 32, 0, 1024);
-            tc_mma_ss(tg + COL_S + b * NKEY, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(kst + (kk / 4) * C::HALF_BYTES + (kk % 4) * 32, 0, 1024);
+            if constexpr (C::QT) {
+              tc_mma_ts(tg + COL_S + b * NKEY, tg + COL_Q + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
+            } else {
+              const uint64_t ad = smem_desc_sw128(qa + (kk / 4) * C::QHALF + (kk % 4) * 32, 0, 1024);
+              tc_mma_ss(tg + COL_S + b * NKEY, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+            }
           }
           tc_commit(smem_u32(sfull + 2 * g + b));
         }
       }
       if (k >= 1) {
         const int j = k - 1, sj = j % NS, bj = j & 1;
-        bool ok = true;
+        bool ok2 = true;
         if (lane == 0)
-          ok = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
-        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
+          ok2 = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
+        if (!__shfl_sync(kFull, ok2 ? 1 : 0, 0)) break;
         if (lane == 0) {
           tc_fence_after();
           const uint32_t vst = stage0 + sj * C::STAGE + C::KREG;
@@ -386,7 +428,12 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
 #pragma unroll
         for (int c = 0; c < NKEY / 16; ++c)
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]) * qk_mult;
+          for (int i = 0; i < 16; i += 2) {  // packed f32x2 multiplies
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])),
+                                        make_float2(qk_mult, qk_mult));
+            x[16 * c + i] = y.x;
+            x[16 * c + i + 1] = y.y;
+          }
       }
       if constexpr (SEP) {  // S[b] may be overwritten
         tc_fence_before();
@@ -446,22 +493,24 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         tc_fence_after();
       }
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 neg_mu = make_float2(-mu, -mu);
+      float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(x[2 * (c0 + i)] - mu);
-          const float p1 = fast_exp2(x[2 * (c0 + i) + 1] - mu);
-          ls[i & 3] += p0 + p1;
-          hi[i] = pack_bf16x2(p0, p1);
-          lo[i] = pack_bf16x2(p0 - bf16lo_to_f32(hi[i]), p1 - bf16hi_to_f32(hi[i]));
+          const float2 e = __fadd2_rn(make_float2(x[2 * (c0 + i)], x[2 * (c0 + i) + 1]), neg_mu);
+          const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+          ls[i & 1] = __fadd2_rn(ls[i & 1], pp);
+          hi[i] = pack_bf16x2(pp.x, pp.y);
+          const float2 r = __fadd2_rn(pp, make_float2(-bf16lo_to_f32(hi[i]), -bf16hi_to_f32(hi[i])));
+          lo[i] = pack_bf16x2(r.x, r.y);
         }
         tmem_st16(tl + COL_P + b * NKEY + c0, hi);
         tmem_st16(tl + COL_P + b * NKEY + NKEY / 2 + c0, lo);
       }
-      lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      lsum += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
