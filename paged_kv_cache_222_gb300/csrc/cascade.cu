@@ -34,6 +34,7 @@ namespace {
 //              128B-swizzled shared memory, one whole-block box per lane
 //   one MMA-issuer warp per group (one lane issues):
 //              S_g(k) = Q_g K(k)^T, then O_g += P_g(k-1) V(k-1)
+//              (a one-group CTA has two: one for S, one for P.V)
 // Q sits in shared memory in the K-major 128B-swizzled layout (A operand of S
 // through a matrix descriptor) when the CTA has two groups, and in TMEM when
 // it has one; K is a K-major and V an MN-major B operand; P (as bf16 hi | lo
@@ -98,10 +99,15 @@ struct TcShape {
   static constexpr bool QT = GROUPS == 1;             // Q in TMEM too (A operand of S from TMEM)
   static constexpr int QBYTES = QT ? 0 : GROUPS * HALVES * QHALF;
   static constexpr int NS = GROUPS == 2 ? 4 : 6;
-  // full, empty; sfull, sfree, pfull, pfree x2; done; Q in TMEM
-  static constexpr int NBARS = 2 * NS + 8 * GROUPS + GROUPS + 1;
+  // One group: S and P.V are issued by two warps of their own, so that a
+  // P.V whose P is ready never waits behind the next tile's arrival (its
+  // stage is released as early as possible).
+  static constexpr bool SPLIT = GROUPS == 1;
+  static constexpr int ISSUERS = GROUPS * (SPLIT ? 2 : 1);  // MMA-issuing warps
+  // full, empty; sfull, sfree, pfull, pfree x2; done per issuer; Q in TMEM
+  static constexpr int NBARS = 2 * NS + 8 * GROUPS + ISSUERS + 1;
   static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
-  static constexpr int THREADS = 32 * (4 * GROUPS + 1 + GROUPS);
+  static constexpr int THREADS = 32 * (4 * GROUPS + 1 + ISSUERS);
   static constexpr uint32_t TCOLS = 512;
   static constexpr int MINB = 1;                      // CTAs per SM
 };
@@ -152,8 +158,8 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   uint64_t* sfree = sfull + 2 * GROUPS;  // used when SEP
   uint64_t* pfull = sfree + 2 * GROUPS;
   uint64_t* pfree = pfull + 2 * GROUPS;
-  uint64_t* done = pfree + 2 * GROUPS;  // [GROUPS]
-  uint64_t* qready = done + GROUPS;     // Q is in TMEM (one arrive per softmax warp)
+  uint64_t* done = pfree + 2 * GROUPS;  // [ISSUERS]
+  uint64_t* qready = done + C::ISSUERS;  // Q is in TMEM (one arrive per softmax warp)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(qready + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_blk = reinterpret_cast<int*>(s_tmem + 4);
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
       mbar_init(smem_u32(pfull + i), 4);
       mbar_init(smem_u32(pfree + i), 1);
     }
-    for (int g = 0; g < GROUPS; ++g) mbar_init(smem_u32(done + g), 1);
+    for (int i = 0; i < C::ISSUERS; ++i) mbar_init(smem_u32(done + i), 1);
     mbar_init(smem_u32(qready), 4);
     *s_abort = 0;
     fence_mbar_init();
@@ -320,16 +326,18 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     }
   } else if (warp > PRODUCER) {
     // ------------------------------------------------------------ MMA issuers
-    const int g = warp - PRODUCER - 1;
+    const int mw = warp - PRODUCER - 1;                // issuer index
+    const int g = C::SPLIT ? mw / 2 : mw;
+    const int role = C::SPLIT ? mw % 2 : 2;            // 0: S, 1: P.V, 2: both, interleaved
     const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
     const uint32_t tg = tbase + g * GCOLS;
     bool ok = true;
-    if constexpr (C::QT) {
+    if (C::QT && role != 1) {
       if (lane == 0) ok = wait_or_abort(smem_u32(qready), 0u, p.err, s_abort);
       ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
     }
     for (int k = 0; k <= ntile && ok; ++k) {
-      if (k < ntile) {
+      if (role != 1 && k < ntile) {
         const int s = k % NS, b = k & 1;
         bool ok2 = true;
         if (lane == 0) {
@@ -375,8 +383,8 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
           tc_commit(smem_u32(sfull + 2 * g + b));
         }
       }
-      if (k >= 1) {
-        const int j = k - 1, sj = j % NS, bj = j & 1;
+      if (role != 0 && (C::SPLIT ? k < ntile : k >= 1)) {
+        const int j = C::SPLIT ? k : k - 1, sj = j % NS, bj = j & 1;
         bool ok2 = true;
         if (lane == 0)
           ok2 = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
@@ -398,8 +406,8 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
       }
     }
     if (lane == 0) {  // nothing of this thread's may still be running when TMEM is freed
-      tc_commit(smem_u32(done + g));
-      mbar_wait(smem_u32(done + g), 0u, nullptr);
+      tc_commit(smem_u32(done + mw));
+      mbar_wait(smem_u32(done + mw), 0u, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
