@@ -107,7 +107,11 @@ struct TcShape {
   // full, empty; sfull, sfree, pfull, pfree x2; done per issuer; Q in TMEM
   static constexpr int NBARS = 2 * NS + 8 * GROUPS + ISSUERS + 1;
   static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
-  static constexpr int THREADS = 32 * (4 * GROUPS + 1 + ISSUERS);
+  // Two TMA producer warps, which issue a tile's boxes in parallel (one warp
+  // issuing a tile's 16 boxes was measured to hold an SM to about 12-19 bytes
+  // per cycle; four warps measured no faster than two)
+  static constexpr int NPROD = 2;
+  static constexpr int THREADS = 32 * (4 * GROUPS + NPROD + ISSUERS);
   static constexpr uint32_t TCOLS = 512;
   static constexpr int MINB = 1;                      // CTAs per SM
 };
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   constexpr uint32_t COL_Q = COL_P + 2 * NKEY;        // Q as bf16 pairs when QT
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
-  constexpr int PRODUCER = 4 * GROUPS;                // warp index
+  constexpr int PRODUCER = 4 * GROUPS;                // first producer warp
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(COL_P + 2 * NKEY <= GCOLS, "TMEM columns");
   static_assert(!C::QT || (SEP && COL_Q + D / 2 <= GCOLS), "TMEM columns for Q");
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(full + s), C::NPROD);
       mbar_init(smem_u32(empty + s), GROUPS);
     }
     for (int i = 0; i < 2 * GROUPS; ++i) {
@@ -287,14 +291,16 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     }
   }
 
-  if (warp == PRODUCER) {
+  if (warp >= PRODUCER && warp < PRODUCER + C::NPROD) {
     // ------------------------------------------------------------ producer
-    // Every lane of the warp issues one TMA box of each tile: one thread
-    // issuing all of a tile's boxes back to back was measured to hold a tile
-    // to about 16 bytes per cycle.
+    // A tile's TMA boxes (K then V; d-half; block) are split evenly over the
+    // producer warps, one box per lane: one thread issuing all of a tile's
+    // boxes back to back was measured to hold a tile to about 16 bytes per
+    // cycle.
+    const int pw = warp - PRODUCER;
     const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
     const int per_half = NKEY / box;
-    const int nbox = 2 * C::HALVES * per_half;                   // K and V boxes of a tile (<= 32)
+    const int nbox = 2 * C::HALVES * per_half / C::NPROD;        // boxes of a tile per warp (<= 32)
     int issued = 0;
     for (int k = 0; k < ntile; ++k) {
       const int s = k % NS;
@@ -306,13 +312,14 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
       const uint32_t bar = smem_u32(full + s);
       if (lane == 0) {
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, C::STAGE);
+        mbar_arrive_expect_tx(bar, C::STAGE / C::NPROD);
       }
       __syncwarp();
       if (lane < nbox) {
-        const int v = lane / (C::HALVES * per_half);          // 0: K, 1: V
-        const int bx = (lane / per_half) % C::HALVES;          // d-half
-        const int i = lane % per_half;                         // box within the tile
+        const int gi = pw * nbox + lane;                       // box of the tile
+        const int v = gi / (C::HALVES * per_half);             // 0: K, 1: V
+        const int bx = (gi / per_half) % C::HALVES;            // d-half
+        const int i = gi % per_half;                           // box within the half
         const int t = t0 + ((k + first) % ntile) * NKEY + i * box;
         const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;  // past the range: zeros
         const uint32_t off = v * C::KREG + bx * C::HALF_BYTES + i * box * 128;
@@ -324,9 +331,9 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
       for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
         mbar_wait(smem_u32(full + k % NS), static_cast<uint32_t>((k / NS) & 1), nullptr);
     }
-  } else if (warp > PRODUCER) {
+  } else if (warp >= PRODUCER + C::NPROD) {
     // ------------------------------------------------------------ MMA issuers
-    const int mw = warp - PRODUCER - 1;                // issuer index
+    const int mw = warp - PRODUCER - C::NPROD;         // issuer index
     const int g = C::SPLIT ? mw / 2 : mw;
     const int role = C::SPLIT ? mw % 2 : 2;            // 0: S, 1: P.V, 2: both, interleaved
     const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
