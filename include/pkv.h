@@ -291,7 +291,7 @@ pkv_status pkv_cascade_decode_attention(const void* q, int32_t batch, int32_t nu
  *   Other arguments as pkv_decode_attention; bf16 caches only (E4M3:
  *   PKV_ERR_UNSUPPORTED).  q_len = 1 computes decode attention.
  *
- * Up to 64 query rows (q_len * G) per (sequence, KV head) run on an mma.sync
+ * Up to 32 query rows (q_len * G) per (sequence, KV head) run on an mma.sync
  * kernel whose warps split rows and tokens; more run on a tcgen05 kernel (128
  * rows per CTA, operands staged by TMA, accumulators in tensor memory).
  *

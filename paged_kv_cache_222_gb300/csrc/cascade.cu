@@ -13,7 +13,7 @@
 //
 // Multi-token queries ([SC] "LLM inference: prefill, decode, KV cache", "7.
 // Practical applications", item 3, and "9. Failure modes and limitations",
-// item 3) with more than 64 rows (q_len * G) per (sequence, KV head): each CTA
+// item 3) with more than 32 rows (q_len * G) per (sequence, KV head): each CTA
 // takes 128 rows of one (sequence, KV head) over one split of the sequence's
 // own tokens, with a causal limit per row.
 
@@ -27,7 +27,7 @@ namespace {
 // Paged attention of many query rows on the 5th-generation tensor cores
 // (tcgen05 + TMEM), pipelined: the cascade prefix (all B * G query rows of a
 // KV head against the shared prefix) and multi-token queries with more than
-// 64 rows per (sequence, KV head).  One CTA per SM; its warps have fixed roles:
+// 32 rows per (sequence, KV head).  One CTA per SM; its warps have fixed roles:
 //   softmax warps (4 per 128-row group): thread t of a group is its query row
 //              t (= TMEM lane t, in the group's columns)
 //   one TMA producer warp: 64-token K and V tiles into a ring of stages of

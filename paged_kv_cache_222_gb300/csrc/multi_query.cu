@@ -10,7 +10,8 @@
 // Design (GB300):
 //  * Rows are (query token i, head g) pairs of one KV head: R = q_len * G of
 //    them share every K/V byte.  A CTA takes up to 64 rows of one (sequence,
-//    KV head) over one split of `split_tokens` tokens, streamed in 64-token
+//    KV head) (the library sends it up to 32: more go to the tcgen05 kernel
+//    of cascade.cu, which is faster there) over one split of `split_tokens` tokens, streamed in 64-token
 //    tiles (four 16-token TMA sub-tiles of K and V, 128B-swizzled, two or
 //    three stages, full / empty mbarriers, block ids of the split staged in
 //    shared memory).

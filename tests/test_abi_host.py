@@ -272,8 +272,12 @@ def test_multi_query_plan_shapes(lib):
     assert p.workspace_bytes == -(-n * 128 * 4 // 256) * 256 + n * 8
     r, p = _mqplan(lib, desc, 2, 16, 64, 100, st=128)     # 128 rows: the tcgen05 kernel
     assert r == L.PKV_OK and p.workers == 0 and p.max_splits == 1 and p.workspace_bytes == 0
-    r, p = _mqplan(lib, desc, 2, 8, 64, 100)                # 64 rows: one token lane
-    assert r == L.PKV_OK and p.workers == 1
+    r, p = _mqplan(lib, desc, 2, 8, 64, 100)                # 64 rows: the tcgen05 kernel
+    assert r == L.PKV_OK and p.workers == 0
+    r, p = _mqplan(lib, desc, 2, 5, 48, 100)                # 30 rows: two token lanes
+    assert r == L.PKV_OK and p.workers == 2
+    r, p = _mqplan(lib, desc, 2, 11, 24, 100)               # 33 rows: the tcgen05 kernel
+    assert r == L.PKV_OK and p.workers == 0
     r, p = _mqplan(lib, desc, 2, 2, 64, 100)
     assert r == L.PKV_OK and p.workers == 4
 
