@@ -847,6 +847,14 @@ extern "C" pkv_status pkv_cascade_decode_attention(
 
 namespace {
 
+// Work units of the tcgen05 multi-token kernel: (split, sequence, KV head,
+// 128-row block).
+int64_t tc_units(const pkv_decode_plan_t& pl, int32_t batch, int32_t q_len, int32_t num_q_heads,
+                 const pkv_cache_desc& c) {
+  const int64_t rows = static_cast<int64_t>(q_len) * (num_q_heads / c.num_kv_heads);
+  return static_cast<int64_t>(pl.max_splits) * batch * c.num_kv_heads * ((rows + 127) / 128);
+}
+
 pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_cache_desc* c,
                    int32_t max_ctx, int32_t split_tokens, int32_t sms, pkv_decode_plan_t* out) {
   pkv_status s = check_cache(c);
@@ -891,6 +899,12 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
   if (splits > 1) {
     const int64_t n = static_cast<int64_t>(batch) * q_len * num_q_heads * splits;
     out->workspace_bytes = align256(n * c->head_dim * 4) + n * 2 * 4;
+  }
+  // the tcgen05 kernel's work-unit counter and unit order, after the partials
+  if (tc) {
+    const int64_t units = tc_units(*out, batch, q_len, num_q_heads, *c);
+    if (units > (1ll << 28)) return fail(PKV_ERR_UNSUPPORTED, "%lld work units", static_cast<long long>(units));
+    out->workspace_bytes = align256(out->workspace_bytes) + 256 + align256(units * 4);
   }
   return PKV_OK;
 }
@@ -946,8 +960,8 @@ extern "C" pkv_status pkv_multi_query_attention(
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
-  p.ws_o = static_cast<float*>(workspace);
-  p.ws_ml = pl.workspace_bytes > 0
+  p.ws_o = pl.max_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = pl.max_splits > 1
                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(n * c.head_dim * 4))
                 : nullptr;
   p.num_blocks = c.num_blocks;
@@ -969,9 +983,20 @@ extern "C" pkv_status pkv_multi_query_attention(
   p.q_len = q_len;
   p.err = st->err;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = traced(pkv::kKindMultiQuery, cs, [&] {
-    return tc ? pkv::launch_multi_query_tc(p, tk, tv, cs) : pkv::launch_multi_query(p, tk, tv, cs);
-  });
+  cudaError_t e = cudaSuccess;
+  if (tc) {
+    // persistent grid (one CTA per SM) over work units taken, longest first,
+    // from a counter after the partials in the workspace (the unit order
+    // follows it)
+    const int64_t units = tc_units(pl, batch, q_len, num_q_heads, c);
+    p.workers = static_cast<int32_t>(units < st->sms ? (units > 0 ? units : 1) : st->sms);
+    const int64_t part = pl.max_splits > 1 ? align256(align256(n * c.head_dim * 4) + n * 2 * 4) : 0;
+    p.ws_q = reinterpret_cast<int*>(static_cast<char*>(workspace) + part);
+  }
+  if (e == cudaSuccess)
+    e = traced(pkv::kKindMultiQuery, cs, [&] {
+      return tc ? pkv::launch_multi_query_tc(p, tk, tv, cs) : pkv::launch_multi_query(p, tk, tv, cs);
+    });
   if (e == cudaSuccess && pl.max_splits > 1) {
     DecodeParams pc = p;            // rows (b, i, hq) flatten to b * (q_len * H_q) + i * H_q + hq
     pc.num_q_heads = q_len * num_q_heads;

@@ -625,6 +625,565 @@ __global__ void __launch_bounds__(128) wait_selftest_kernel(int which, uint64_t 
   }
 }
 
+// ----------------------------------------------------------------------------
+// Multi-token queries on the tensor cores, persistent.  One CTA per SM takes
+// work units (split, sequence, KV head, 128-row block) from a counter in the
+// caller's workspace, in split-major order (the first, longest splits of all
+// sequences first), until none are left; the producers run ahead into the
+// next unit while the softmax warps finish the current one, so a unit costs
+// no pipeline fill and no setup.  Warps:
+//   0-3  softmax: thread t is query row t of the unit (TMEM lane t); at the
+//        end of a unit they put the next unit's Q into TMEM (one buffer: all
+//        S of the unit have completed by then), then read O of the unit
+//        and write its output row or (acc, m, l) piece
+//   4-5  TMA producers: half of each tile's boxes each; warp 4 takes units
+//        from the counter and publishes them in a ring of shared slots
+//   6    S issuer: S(g) = Q K(g)^T (A from TMEM)
+//   7    P.V issuer: O += P(g) V(g) (P from TMEM as bf16 hi | lo pairs)
+// g counts tiles over all of the CTA's units, so ring slots and TMEM
+// buffers keep their phases across units.  Every wait is bounded; a time-out
+// records the error and raises the CTA's abort flag, which ends every loop.
+// ----------------------------------------------------------------------------
+struct MqUnit {
+  int b, h, row0, t0, t1, ctx, nsplit, split, ntile;
+};
+
+// Work unit u (split-major: split, then sequence, then KV head and row block).
+__device__ __forceinline__ MqUnit mq_unit(const DecodeParams& p, int u, int nrb, bool note) {
+  MqUnit w;
+  const int rows = p.q_len * p.group;
+  const int hn_all = p.num_kv_heads * nrb;
+  w.split = u / (p.batch * hn_all);
+  const int r = u - w.split * (p.batch * hn_all);
+  w.b = r / hn_all;
+  const int hn = r - w.b * hn_all;
+  w.h = hn / nrb;
+  w.row0 = (hn - w.h * nrb) * 128;
+  const int ctx_raw = p.context_lens[w.b];
+  w.ctx = clamp_ctx(p, ctx_raw);
+  if (note && w.ctx != ctx_raw && w.split == 0 && hn == 0) record_error(p.err, kDevErrContextLen);
+  w.nsplit = (w.ctx + p.split_tokens - 1) / p.split_tokens;
+  w.t0 = w.split * p.split_tokens;
+  const int row_last = min(rows, w.row0 + 128) - 1;
+  const int lim_last = min(w.ctx, w.ctx - p.q_len + row_last / p.group + 1);  // rows attend monotonically more
+  w.t1 = w.t0 < w.ctx ? min(min(w.ctx, w.t0 + p.split_tokens), lim_last) : w.t0;
+  if (w.t1 < w.t0) w.t1 = w.t0;
+  w.ntile = (w.t1 - w.t0 + 63) / 64;
+  return w;
+}
+
+// Work units in order of decreasing tile count (longest first, so that the
+// last units any CTA takes are short): a counting sort over the tile counts
+// into `perm`, by one CTA.  Also zeroes the unit counter.
+__global__ void __launch_bounds__(1024) mq_order_kernel(const DecodeParams p, int* perm) {
+  __shared__ int cnt[kMultiQueryMaxSplitBlocks + 1];
+  const int rows = p.q_len * p.group, nrb = (rows + 127) / 128;
+  const int U = p.max_splits * p.batch * p.num_kv_heads * nrb;
+  const int nb = p.split_tokens / 64 + 1;            // tile counts 0 .. split_tokens / 64
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) atomicAdd(&cnt[mq_unit(p, u, nrb, false).ntile], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {  // start of each count's run, largest count first
+    int run = 0;
+    for (int i = nb - 1; i >= 0; --i) {
+      const int c = cnt[i];
+      cnt[i] = run;
+      run += c;
+    }
+    p.ws_q[0] = 0;
+  }
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) perm[atomicAdd(&cnt[mq_unit(p, u, nrb, false).ntile], 1)] = u;
+}
+
+// Unit number n of this CTA from the ring (readers: one call per warp, lane
+// 0 waits); -1 when none is left or the CTA aborts.
+__device__ __forceinline__ int mq_read_unit(uint64_t* ufull, uint64_t* uempty, const int* s_unit, int n,
+                                            int* err, volatile int* abort) {
+  constexpr int R = 8;
+  int u = -1;
+  if ((threadIdx.x & 31) == 0) {
+    const int slot = n % R;
+    if (wait_or_abort(smem_u32(ufull + slot), static_cast<uint32_t>((n / R) & 1), err, abort)) {
+      u = *reinterpret_cast<const volatile int*>(s_unit + slot);
+      mbar_arrive(smem_u32(uempty + slot));
+    }
+  }
+  return __shfl_sync(kFull, u, 0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    mq_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                 const DecodeParams p) {
+  using L = Layout<D, false>;
+  using C = TcShape<D, 1>;
+  constexpr int M = 128, NKEY = C::NKEY, NS = C::NS;
+  constexpr int R = 8;                                // unit ring slots
+  constexpr int READERS = 7;                          // warps 0-3, 5, 6, 7
+  constexpr uint32_t COL_O = 0, COL_S = D, COL_P = D + 2 * NKEY, COL_Q = COL_P + 2 * NKEY;
+  constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
+  constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
+  static_assert(COL_Q + D / 2 <= 512, "TMEM columns");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.group, QL = p.q_len, H_q = p.num_q_heads;
+  const int rows = QL * G, nrb = (rows + M - 1) / M;
+  const int U = p.max_splits * p.batch * p.num_kv_heads * nrb;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t stage0 = smem_u32(smem);
+  int* s_ids = reinterpret_cast<int*>(smem + NS * C::STAGE);  // [2][1024] each producer's block ids
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_ids + 2 * kMultiQueryMaxSplitBlocks);  // [NS]
+  uint64_t* empty = full + NS;                        // [NS]
+  uint64_t* sfull = empty + NS;                       // [2]
+  uint64_t* sfree = sfull + 2;                        // [2]
+  uint64_t* pfull = sfree + 2;                        // [2]
+  uint64_t* pfree = pfull + 2;                        // [2]
+  uint64_t* qready = pfree + 2;                       // [1]
+  uint64_t* ufull = qready + 1;                       // [R]
+  uint64_t* uempty = ufull + R;                       // [R]
+  uint64_t* done = uempty + R;                        // [2]
+  int* s_unit = reinterpret_cast<int*>(done + 2);     // [R]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_unit + R);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(full + s), 2);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(sfull + i), 1);
+      mbar_init(smem_u32(sfree + i), 4);
+      mbar_init(smem_u32(pfull + i), 4);
+      mbar_init(smem_u32(pfree + i), 1);
+      mbar_init(smem_u32(done + i), 1);
+    }
+    mbar_init(smem_u32(qready), 4);
+    for (int i = 0; i < R; ++i) {
+      mbar_init(smem_u32(ufull + i), 1);
+      mbar_init(smem_u32(uempty + i), READERS);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(s_tmem), 512);
+    tmem_relinquish();
+  }
+  wait_prior_grid();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_tmem;
+
+  if (warp == 4 || warp == 5) {
+    // ------------------------------------------------------------ producers
+    const int pw = warp - 4;
+    const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
+    const int per_half = NKEY / box;
+    const int nbox = C::HALVES * per_half;                       // boxes of a tile per warp
+    int g = 0;
+    for (int n = 0;; ++n) {
+      int u;
+      if (pw == 0) {
+        u = -1;
+        if (lane == 0) {
+          const int slot = n % R;
+          if (n < R || wait_or_abort(smem_u32(uempty + slot), static_cast<uint32_t>((n / R - 1) & 1), p.err,
+                                     s_abort)) {
+            u = *s_abort ? -1 : atomicAdd(p.ws_q, 1);
+            u = u < U ? p.ws_q[64 + u] : -1;  // the order of mq_order_kernel
+          }
+          s_unit[slot] = u;
+          mbar_arrive(smem_u32(ufull + slot));  // releases the slot's value to the readers
+        }
+        u = __shfl_sync(kFull, u, 0);
+      } else {
+        u = mq_read_unit(ufull, uempty, s_unit, n, p.err, s_abort);
+      }
+      if (u < 0) break;
+      const MqUnit w = mq_unit(p, u, nrb, pw == 0 && lane == 0);
+      // the unit's block ids into this warp's shared array (it has issued
+      // every box of the previous unit)
+      const int32_t* blocks = p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks + w.t0 / p.block_size;
+      int* ids = s_ids + pw * kMultiQueryMaxSplitBlocks;
+      const int nblk = (w.t1 - w.t0 + p.block_size - 1) / p.block_size;
+      for (int j = lane; j < nblk; j += 32) {
+        int phys = blocks[j];
+        if (phys < 0 || phys >= p.num_blocks) {
+          if (pw == 0) record_error(p.err, kDevErrBlockId);
+          phys = -1;  // fully outside the tensor: the TMA unit fills zeros
+        }
+        ids[j] = phys;
+      }
+      __syncwarp();
+      // this lane's box of each tile: K or V, d-half, block within the tile
+      const int gi = pw * nbox + lane;
+      const int v = gi / (C::HALVES * per_half);
+      const int bx = (gi / per_half) % C::HALVES;
+      const int i = gi % per_half;
+      bool ok = true;
+      for (int k = 0; k < w.ntile; ++k, ++g) {
+        const int s = g % NS;
+        bool go = true;
+        if (lane == 0 && g >= NS)
+          go = wait_or_abort(smem_u32(empty + s), static_cast<uint32_t>((g / NS - 1) & 1), p.err, s_abort);
+        if (!__shfl_sync(kFull, go ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = stage0 + s * C::STAGE;
+        const uint32_t bar = smem_u32(full + s);
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(bar, C::STAGE / 2);
+        }
+        __syncwarp();
+        if (lane < nbox) {
+          const int t = w.t0 + k * NKEY + i * box;
+          const int phys = t < w.t1 ? ids[(t - w.t0) / p.block_size] : -1;  // past the range: zeros
+          const uint32_t off = v * C::KREG + bx * C::HALF_BYTES + i * box * 128;
+          tma_load_4d(dst + off, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, w.h, phys);
+        }
+      }
+      if (!ok) break;
+    }
+    if (lane == 0 && *s_abort) {  // the copies in flight land before the stages are released
+      for (int k = g > NS ? g - NS : 0; k < g; ++k)
+        mbar_wait(smem_u32(full + k % NS), static_cast<uint32_t>((k / NS) & 1), nullptr);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ S issuer
+    int g = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int u = mq_read_unit(ufull, uempty, s_unit, n, p.err, s_abort);
+      if (u < 0) break;
+      const MqUnit w = mq_unit(p, u, nrb, false);
+      if (lane == 0) ok = wait_or_abort(smem_u32(qready), static_cast<uint32_t>(n & 1), p.err, s_abort);
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      for (int k = 0; k < w.ntile && ok; ++k, ++g) {
+        const int s = g % NS, b = g & 1;
+        bool ok2 = true;
+        if (lane == 0) {
+          ok2 = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((g / NS) & 1), p.err, s_abort);
+          if (ok2 && g >= 2)  // the softmax has read S(g-2) out of buffer b
+            ok2 = wait_or_abort(smem_u32(sfree + b), static_cast<uint32_t>(((g - 2) >> 1) & 1), p.err, s_abort);
+        }
+        ok = __shfl_sync(kFull, ok2 ? 1 : 0, 0) != 0;
+        if (ok && lane == 0) {
+          tc_fence_after();
+          const uint32_t kst = stage0 + s * C::STAGE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(kst + (kk / 4) * C::HALF_BYTES + (kk % 4) * 32, 0, 1024);
+            tc_mma_ts(tbase + COL_S + b * NKEY, tbase + COL_Q + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(sfull + b));
+        }
+      }
+    }
+    if (lane == 0) {  // nothing of this thread's may still be running when TMEM is freed
+      tc_commit(smem_u32(done));
+      mbar_wait(smem_u32(done), 0u, nullptr);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ P.V issuer
+    int g = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int u = mq_read_unit(ufull, uempty, s_unit, n, p.err, s_abort);
+      if (u < 0) break;
+      const MqUnit w = mq_unit(p, u, nrb, false);
+      for (int k = 0; k < w.ntile && ok; ++k, ++g) {
+        const int s = g % NS, b = g & 1;
+        bool ok2 = true;
+        if (lane == 0) {
+          ok2 = wait_or_abort(smem_u32(pfull + b), static_cast<uint32_t>((g >> 1) & 1), p.err, s_abort);
+          if (ok2)  // complete already (S read the stage); orders the V bytes before the zeroing below
+            ok2 = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((g / NS) & 1), p.err, s_abort);
+        }
+        ok = __shfl_sync(kFull, ok2 ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t vst = stage0 + s * C::STAGE + C::KREG;
+        // rows of the last block past the sequence end may hold anything (NaN
+        // included): zero them in the V tile, P is 0 there
+        const int vr0 = w.ctx - (w.t0 + k * NKEY);
+        if (vr0 < NKEY) {
+          uint8_t* vt = smem + (vst - stage0);
+          const int first_row = vr0 > 0 ? vr0 : 0;
+          const int chunks = (NKEY - first_row) * 8;   // 16-byte chunks per d-half
+          for (int c = lane; c < C::HALVES * chunks; c += 32) {
+            const int hf = c / chunks, cc = c - hf * chunks;
+            *reinterpret_cast<uint4*>(vt + hf * C::HALF_BYTES + first_row * 128 + cc * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t pa = tbase + COL_P + b * NKEY;
+#pragma unroll
+          for (int kk = 0; kk < NKEY / 16; ++kk) {
+            // MN-major V: 8-key groups 1024 B apart, d-halves HALF_BYTES apart
+            const uint64_t vd = smem_desc_sw128(vst + kk * 2048, C::HALVES > 1 ? C::HALF_BYTES : 0, 1024);
+            tc_mma_ts(tbase + COL_O, pa + kk * 8, vd, IDESC_PV, (k > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(tbase + COL_O, pa + NKEY / 2 + kk * 8, vd, IDESC_PV, 1u);
+          }
+          tc_commit(smem_u32(pfree + b));
+          tc_commit(smem_u32(empty + s));
+        }
+      }
+    }
+    if (lane == 0) {
+      tc_commit(smem_u32(done + 1));
+      mbar_wait(smem_u32(done + 1), 0u, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r_in = warp * 32 + lane;                 // row within the unit's row block
+    const uint32_t tl = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    const float qk_mult = p.qk_log2_scale;
+    uint4 qw[D / 8];                                   // the next unit's Q row
+    // load this thread's Q row of unit w (zeros past the rows)
+    auto load_q = [&](const MqUnit& w) {
+      const int row = w.row0 + r_in;
+      const int64_t orow = (static_cast<int64_t>(w.b) * QL + row / G) * H_q + w.h * G + row % G;
+      const uint16_t* qr = row < rows ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        qw[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    // row r of Q into TMEM lane r as bf16 pairs (element 2j in the low half
+    // of column j, the memory order of the loaded words), then tell the S issuer
+    auto store_q = [&]() {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[4 * j] = qw[4 * c + j].x;
+          v[4 * j + 1] = qw[4 * c + j].y;
+          v[4 * j + 2] = qw[4 * c + j].z;
+          v[4 * j + 3] = qw[4 * c + j].w;
+        }
+        tmem_st16(tl + COL_Q + 16 * c, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(qready));
+    };
+    int g = 0;
+    bool ok = true;
+    int u = mq_read_unit(ufull, uempty, s_unit, 0, p.err, s_abort);
+    MqUnit w;
+    if (u >= 0) {
+      w = mq_unit(p, u, nrb, false);
+      load_q(w);
+      store_q();
+    }
+    for (int n = 0; u >= 0 && ok; ++n) {
+      const int row = w.row0 + r_in;
+      const bool row_ok = row < rows;
+      const int64_t orow = (static_cast<int64_t>(w.b) * QL + row / G) * H_q + w.h * G + row % G;
+      // tokens this row may attend: [0, lim)
+      const int lim = row_ok ? min(w.t1, w.ctx - QL + row / G + 1) : w.t0;
+      float m_used = -CUDART_INF_F, lsum = 0.f;
+      for (int k = 0; k < w.ntile; ++k, ++g) {
+        const int b = g & 1;
+        ok = __all_sync(kFull, wait_or_abort(smem_u32(sfull + b), static_cast<uint32_t>((g >> 1) & 1), p.err,
+                                             s_abort));
+        if (!ok) break;
+        tc_fence_after();
+        float x[NKEY];
+        {
+          uint32_t v[NKEY / 16][16];
+#pragma unroll
+          for (int c = 0; c < NKEY / 16; ++c) tmem_ld16(tl + COL_S + b * NKEY + 16 * c, v[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < NKEY / 16; ++c)
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {  // packed f32x2 multiplies
+              const float2 y = __fmul2_rn(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])),
+                                          make_float2(qk_mult, qk_mult));
+              x[16 * c + i] = y.x;
+              x[16 * c + i + 1] = y.y;
+            }
+        }
+        tc_fence_before();  // S[b] may be overwritten
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sfree + b));
+        const int valid = lim - (w.t0 + k * NKEY);
+        if (__any_sync(kFull, valid < NKEY)) {
+#pragma unroll
+          for (int i = 0; i < NKEY; ++i)
+            if (i >= valid) x[i] = -CUDART_INF_F;
+        }
+        float mt;
+        {  // tree of partial maxima: a short dependency chain
+          float mp[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mp[i] = x[i];
+#pragma unroll
+          for (int i = 8; i < NKEY; ++i) mp[i & 7] = fmaxf(mp[i & 7], x[i]);
+          mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        }
+        float alpha = 1.f;
+        bool resc = false;
+        if (m_used == -CUDART_INF_F) {
+          m_used = mt;  // nothing accumulated yet for this row
+        } else if (mt > m_used + 8.f) {
+          alpha = fast_exp2(m_used - mt);
+          m_used = mt;
+          resc = true;
+        }
+        if (__any_sync(kFull, resc)) {
+          // O holds tiles 0..k-1 of the unit once P(g-1).V has completed
+          ok = __all_sync(kFull, wait_or_abort(smem_u32(pfree + ((g - 1) & 1)),
+                                               static_cast<uint32_t>(((g - 1) >> 1) & 1), p.err, s_abort));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[2][16];
+            tmem_ld16(tl + COL_O + c0, v[0]);
+            tmem_ld16(tl + COL_O + c0 + 16, v[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[hh][i] = __float_as_uint(__uint_as_float(v[hh][i]) * alpha);
+            tmem_st16(tl + COL_O + c0, v[0]);
+            tmem_st16(tl + COL_O + c0 + 16, v[1]);
+          }
+          tmem_wait_st();
+        }
+        lsum *= alpha;
+        if (g >= 2) {  // P(g-2).V has read P[b]
+          ok = __all_sync(kFull, wait_or_abort(smem_u32(pfree + b), static_cast<uint32_t>(((g - 2) >> 1) & 1),
+                                               p.err, s_abort));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
+        const float2 neg_mu = make_float2(-mu, -mu);
+        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 e = __fadd2_rn(make_float2(x[2 * (c0 + i)], x[2 * (c0 + i) + 1]), neg_mu);
+            const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+            ls[i & 1] = __fadd2_rn(ls[i & 1], pp);
+            hi[i] = pack_bf16x2(pp.x, pp.y);
+            const float2 rr = __fadd2_rn(pp, make_float2(-bf16lo_to_f32(hi[i]), -bf16hi_to_f32(hi[i])));
+            lo[i] = pack_bf16x2(rr.x, rr.y);
+          }
+          tmem_st16(tl + COL_P + b * NKEY + c0, hi);
+          tmem_st16(tl + COL_P + b * NKEY + NKEY / 2 + c0, lo);
+        }
+        lsum += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(pfull + b));   // P(g) is in TMEM
+      }
+      if (!ok) break;
+      // the next unit: its Q rows are loaded now, stored into TMEM after this
+      // unit's output (every S of this unit has completed: the loop above saw
+      // each one's sfull)
+      const int u_next = mq_read_unit(ufull, uempty, s_unit, n + 1, p.err, s_abort);
+      MqUnit w_next;
+      if (u_next >= 0) {
+        w_next = mq_unit(p, u_next, nrb, false);
+        load_q(w_next);
+      }
+      // ---- this unit's result: a workspace piece, or (one split) the output row
+      if (w.ntile > 0)
+        ok = __all_sync(kFull, wait_or_abort(smem_u32(pfree + ((g - 1) & 1)),
+                                             static_cast<uint32_t>(((g - 1) >> 1) & 1), p.err, s_abort));
+      const bool writes = w.t0 < w.ctx || (w.ctx == 0 && w.split == 0);
+      const bool direct = w.nsplit <= 1;
+      const int64_t piece = orow * p.slots_per_row + w.split;
+      if (ok && writes) {
+        if (w.ntile > 0) tc_fence_after();
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        float* dst_row = direct ? p.out + orow * D : p.ws_o + piece * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[2][16];
+          if (w.ntile > 0) {
+            tmem_ld16(tl + COL_O + c0, v[0]);
+            tmem_ld16(tl + COL_O + c0 + 16, v[1]);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
+          }
+          if (row_ok) {
+            const float sc = direct ? inv : 1.f;
+            float4* dst = reinterpret_cast<float4*>(dst_row + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]) * sc,
+                                   __uint_as_float(v[i / 4][4 * (i % 4) + 1]) * sc,
+                                   __uint_as_float(v[i / 4][4 * (i % 4) + 2]) * sc,
+                                   __uint_as_float(v[i / 4][4 * (i % 4) + 3]) * sc);
+          }
+        }
+        if (row_ok && !direct) {
+          p.ws_ml[piece * 2] = m_used;
+          p.ws_ml[piece * 2 + 1] = lsum;
+        }
+      }
+      if (!ok) break;
+      if (u_next >= 0) store_q();  // after O was read: P.V of the next unit overwrites O
+      u = u_next;
+      w = w_next;
+    }
+  }
+  allow_next_grid();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+int mq_tc_smem_bytes() {
+  // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
+  const int need = TcShape<D, 1>::NS * TcShape<D, 1>::STAGE + 2 * kMultiQueryMaxSplitBlocks * 4 + 64 * 8 + 1024 + 1024;
+  return need > 120 * 1024 ? need : 120 * 1024;
+}
+
+template <int D>
+cudaError_t launch_mq_tc_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           cudaStream_t stream) {
+  auto kern = mq_tc_kernel<D>;
+  const int smem = mq_tc_smem_bytes<D>();
+  static bool configured[64] = {};
+  cudaError_t e = set_smem_once(kern, smem, configured);
+  if (e != cudaSuccess) return e;
+  // plain launches: the order kernel writes the unit order and zeroes the
+  // counter just before the persistent grid starts
+  mq_order_kernel<<<1, 1024, 0, stream>>>(p, p.ws_q + 64);
+  kern<<<dim3(p.workers), dim3(256), smem, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
 template <int D, int GROUPS>
 int tc_smem_bytes() {
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
@@ -661,11 +1220,8 @@ cudaError_t launch_wait_selftest(int which, uint64_t limit_ns, int* err, cudaStr
 
 cudaError_t launch_multi_query_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
-  const int rows = p.q_len * p.group;
-  const int nrb = (rows + 127) / 128;
-  const dim3 grid(p.max_splits, p.num_kv_heads * nrb, p.batch);
-  if (p.head_dim == 128) return launch_tc_t<128, 1, true>(p, tk, tv, grid, stream);
-  return launch_tc_t<64, 1, true>(p, tk, tv, grid, stream);
+  if (p.head_dim == 128) return launch_mq_tc_t<128>(p, tk, tv, stream);
+  return launch_mq_tc_t<64>(p, tk, tv, stream);
 }
 
 }  // namespace pkv

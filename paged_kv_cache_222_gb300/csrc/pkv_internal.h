@@ -63,7 +63,8 @@ struct DecodeParams {
   float* out;                 // [B, H_q, D]
   float* ws_o;                // fixed split: [B, H_q, S, D]; stream-K: [2W, GP, D]
   float* ws_ml;               // fixed split: [B, H_q, S, 2]; stream-K: [2W, GP, 2]
-  int* ws_q;                  // stream-K: tile prefix over sequences [B + 1]
+  int* ws_q;                  // stream-K: tile prefix over sequences [B + 1];
+                              // tcgen05 multi-token: the work-unit counter
   const float* k_scale;
   const float* v_scale;
   int64_t scale_stride;
@@ -81,7 +82,8 @@ struct DecodeParams {
   float qk_log2_scale;        // softmax scale * log2(e)
   int32_t cache_dtype;
   int32_t mode;               // kModeStreamK / kModeFixedSplit
-  int32_t workers;            // stream-K: warps of the persistent grid (W)
+  int32_t workers;            // stream-K: warps of the persistent grid (W);
+                              // tcgen05 multi-token: CTAs of the persistent grid
   // cascade (shared-prefix) decode; zero / -1 / NULL otherwise
   int32_t token_offset;       // fixed split: attend tokens [token_offset, ctx)
   int32_t force_partial;      // fixed split: always write partials, never `out`

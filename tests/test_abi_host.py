@@ -271,7 +271,13 @@ def test_multi_query_plan_shapes(lib):
     n = 64 * 4 * 64 * p.max_splits
     assert p.workspace_bytes == -(-n * 128 * 4 // 256) * 256 + n * 8
     r, p = _mqplan(lib, desc, 2, 16, 64, 100, st=128)     # 128 rows: the tcgen05 kernel
-    assert r == L.PKV_OK and p.workers == 0 and p.max_splits == 1 and p.workspace_bytes == 0
+    assert r == L.PKV_OK and p.workers == 0 and p.max_splits == 1
+    assert p.workspace_bytes == 256 + 256                   # work-unit counter, unit order (16 units)
+    r, p = _mqplan(lib, desc, 3, 16, 64, 1000, st=128)    # with partials: counter and order after them
+    n = 3 * 16 * 64 * p.max_splits
+    units = p.max_splits * 3 * 8
+    part = -(-(-(-n * 128 * 4 // 256) * 256 + n * 8) // 256) * 256
+    assert p.max_splits == 8 and p.workspace_bytes == part + 256 + -(-units * 4 // 256) * 256
     r, p = _mqplan(lib, desc, 2, 8, 64, 100)                # 64 rows: the tcgen05 kernel
     assert r == L.PKV_OK and p.workers == 0
     r, p = _mqplan(lib, desc, 2, 5, 48, 100)                # 30 rows: two token lanes
