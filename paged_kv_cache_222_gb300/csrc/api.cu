@@ -880,11 +880,13 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
   const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * nrb;
   int32_t st = split_tokens;
   if (st == 0) {
-    // largest power of two (256..4096) that still gives about four waves of
-    // CTAs (two per SM on the mma.sync kernel, one on the tcgen05 kernel) when
-    // every sequence is as long as the bound
-    const int64_t want = static_cast<int64_t>(sms) * (tc ? 1 : 2) * 4;
-    st = 4096;
+    // mma.sync: the largest power of two (256..4096) that still gives about
+    // four waves of CTAs (two per SM) when every sequence is as long as the
+    // bound.  tcgen05 (persistent, longest units first): the largest power of
+    // two up to the longest split (1024 blocks) that still gives three units
+    // per SM (larger units cost less per token: one setup, fewer partials)
+    const int64_t want = static_cast<int64_t>(sms) * (tc ? 3 : 8);
+    st = tc ? static_cast<int32_t>(max_st) : 4096;
     while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
   }
   const int64_t splits = max_ctx > 0 ? ceil_div(max_ctx, st) : 1;

@@ -136,10 +136,10 @@ cudaError_t launch_multi_query_tc(const DecodeParams& p, const CUtensorMap& tmap
 // path); records PKV_DEVERR_WAIT_TIMEOUT after about limit_ns.
 cudaError_t launch_wait_selftest(int which, uint64_t limit_ns, int* err, cudaStream_t stream);
 // Rows (q_len * G) from which multi-token queries take the tcgen05 kernel.
-// Its speed does not depend on the rows (0.60-0.61 of HBM from 16 to 128
-// rows on the 70B-class GQA batch); the mma.sync kernel measured 0.82 at 16
-// rows, 0.65 at 24, 0.63 at 32 and 0.41 at 40.
-constexpr int kMultiQueryTcRows = 33;
+// Its speed hardly depends on the rows (0.68-0.70 of HBM from 8 to 128 rows
+// on the 70B-class GQA batch); the mma.sync kernel measured 0.82 at 16 rows,
+// 0.65 at 24, 0.63 at 32 and 0.41 at 40.
+constexpr int kMultiQueryTcRows = 17;
 
 // Multi-token query kernel: 64-token tiles, rows of (query token, head) pairs
 // in 16-row warp groups; the block ids of one split staged in shared memory.

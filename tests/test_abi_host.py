@@ -265,11 +265,16 @@ def _mqplan(lib, desc, batch, q_len, hq, max_ctx, st=0, sms=152):
 
 def test_multi_query_plan_shapes(lib):
     desc = _desc()
-    r, p = _mqplan(lib, desc, 64, 4, 64, 8192)
-    assert r == L.PKV_OK and p.mode == 3 and p.workers == 2          # 32 rows: two lanes
+    r, p = _mqplan(lib, desc, 64, 2, 64, 8192)
+    assert r == L.PKV_OK and p.mode == 3 and p.workers == 4          # 16 rows: four token lanes
     assert p.split_tokens % 64 == 0 and p.max_splits == -(-8192 // p.split_tokens)
-    n = 64 * 4 * 64 * p.max_splits
+    n = 64 * 2 * 64 * p.max_splits
     assert p.workspace_bytes == -(-n * 128 * 4 // 256) * 256 + n * 8
+    r, p = _mqplan(lib, desc, 64, 4, 64, 8192)               # 32 rows: the tcgen05 kernel, whose
+    assert r == L.PKV_OK and p.workers == 0                  # splits are the longest (1024 blocks)
+    assert p.split_tokens == 16 * 1024 and p.max_splits == 1  # that leave 3 units per SM
+    r, p = _mqplan(lib, desc, 1, 16, 64, 131072)
+    assert r == L.PKV_OK and p.workers == 0 and 8 * p.max_splits >= 3 * 152 > 8 * (-(-131072 // (2 * p.split_tokens)))
     r, p = _mqplan(lib, desc, 2, 16, 64, 100, st=128)     # 128 rows: the tcgen05 kernel
     assert r == L.PKV_OK and p.workers == 0 and p.max_splits == 1
     assert p.workspace_bytes == 256 + 256                   # work-unit counter, unit order (16 units)
@@ -280,9 +285,9 @@ def test_multi_query_plan_shapes(lib):
     assert p.max_splits == 8 and p.workspace_bytes == part + 256 + -(-units * 4 // 256) * 256
     r, p = _mqplan(lib, desc, 2, 8, 64, 100)                # 64 rows: the tcgen05 kernel
     assert r == L.PKV_OK and p.workers == 0
-    r, p = _mqplan(lib, desc, 2, 5, 48, 100)                # 30 rows: two token lanes
-    assert r == L.PKV_OK and p.workers == 2
-    r, p = _mqplan(lib, desc, 2, 11, 24, 100)               # 33 rows: the tcgen05 kernel
+    r, p = _mqplan(lib, desc, 2, 1, 128, 100)               # 16 rows: mma.sync
+    assert r == L.PKV_OK and p.workers == 4
+    r, p = _mqplan(lib, desc, 2, 2, 72, 100)                # 18 rows: the tcgen05 kernel
     assert r == L.PKV_OK and p.workers == 0
     r, p = _mqplan(lib, desc, 2, 2, 64, 100)
     assert r == L.PKV_OK and p.workers == 4

@@ -68,11 +68,11 @@ def _oracle(case):
     (1, 8, 1, 128, 16),     # 8 rows: four token lanes
     (2, 8, 1, 128, 16),     # 16 rows
     (3, 10, 2, 64, 16),     # 15 rows, G = 5
-    (4, 8, 1, 128, 32),     # 32 rows: two lanes
-    (8, 4, 1, 64, 32),      # 32 rows
-    (6, 8, 1, 128, 16),     # 48 rows: the tcgen05 kernel, a partly filled group
+    (4, 8, 1, 128, 32),     # 32 rows: the tcgen05 kernel
+    (8, 4, 1, 64, 32),      # 32 rows, D = 64
+    (6, 8, 1, 128, 16),     # 48 rows: a partly filled group
     (16, 8, 2, 128, 16),    # 64 rows
-    (11, 3, 1, 128, 16),    # 33 rows, G = 3
+    (6, 3, 1, 128, 16),     # 18 rows, G = 3: the smallest tcgen05 case
     (16, 8, 1, 128, 32),    # 128 rows: the tcgen05 kernel, whole 32-token blocks per TMA box
     (12, 8, 1, 128, 16),    # 96 rows: a partly filled 128-row group
     (12, 16, 1, 128, 16),   # 192 rows: a partly filled second 128-row group
