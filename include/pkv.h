@@ -291,12 +291,15 @@ pkv_status pkv_cascade_decode_attention(const void* q, int32_t batch, int32_t nu
  *   Other arguments as pkv_decode_attention; bf16 caches only (E4M3:
  *   PKV_ERR_UNSUPPORTED).  q_len = 1 computes decode attention.
  *
- * Up to 32 query rows (q_len * G) per (sequence, KV head) run on an mma.sync
- * kernel whose warps split rows and tokens; more run on a tcgen05 kernel (128
- * rows per CTA, operands staged by TMA, accumulators in tensor memory).
+ * Up to 16 query rows (q_len * G) per (sequence, KV head) run on an mma.sync
+ * kernel whose warps split the tokens; more run on a persistent tcgen05
+ * kernel (one CTA per SM taking (split, sequence, KV head, 128-row block)
+ * units longest first; operands staged by TMA, accumulators in tensor
+ * memory), which keeps a work-unit counter and the unit order in the last
+ * part of the workspace (so a workspace is always needed there).
  *
  * pkv_multi_query_plan (host only): mode 3; split_tokens / max_splits as for
- * decode; workers = warps per CTA that share each 16 query rows (4, 2 or 1)
+ * decode; workers = warps per CTA that share each 16 query rows (4)
  * on the mma.sync kernel, 0 when the tcgen05 kernel runs.
  */
 pkv_status pkv_multi_query_plan(int32_t batch, int32_t q_len, int32_t num_q_heads,

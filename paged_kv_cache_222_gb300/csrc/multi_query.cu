@@ -10,8 +10,8 @@
 // Design (GB300):
 //  * Rows are (query token i, head g) pairs of one KV head: R = q_len * G of
 //    them share every K/V byte.  A CTA takes up to 64 rows of one (sequence,
-//    KV head) (the library sends it up to 32: more go to the tcgen05 kernel
-//    of cascade.cu, which is faster there) over one split of `split_tokens` tokens, streamed in 64-token
+//    KV head) (the library sends it up to 16: more go to the persistent
+//    tcgen05 kernel of cascade.cu, which is faster there) over one split of `split_tokens` tokens, streamed in 64-token
 //    tiles (four 16-token TMA sub-tiles of K and V, 128B-swizzled, two or
 //    three stages, full / empty mbarriers, block ids of the split staged in
 //    shared memory).
@@ -377,15 +377,11 @@ cudaError_t launch_mq_t(const DecodeParams& p, const CUtensorMap& tk, const CUte
 
 cudaError_t launch_multi_query(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
-  const int tl = multi_query_lanes(p.q_len * p.group);
-  if (p.head_dim == 128) {
-    if (tl == 4) return launch_mq_t<128, 4>(p, tk, tv, stream);
-    if (tl == 2) return launch_mq_t<128, 2>(p, tk, tv, stream);
-    return launch_mq_t<128, 1>(p, tk, tv, stream);
-  }
-  if (tl == 4) return launch_mq_t<64, 4>(p, tk, tv, stream);
-  if (tl == 2) return launch_mq_t<64, 2>(p, tk, tv, stream);
-  return launch_mq_t<64, 1>(p, tk, tv, stream);
+  // the library sends this kernel up to 16 rows (kMultiQueryTcRows): four
+  // token lanes; the two- and one-lane shapes are not instantiated
+  if (multi_query_lanes(p.q_len * p.group) != 4) return cudaErrorInvalidValue;
+  if (p.head_dim == 128) return launch_mq_t<128, 4>(p, tk, tv, stream);
+  return launch_mq_t<64, 4>(p, tk, tv, stream);
 }
 
 }  // namespace pkv
