@@ -13,9 +13,9 @@
 //
 // Multi-token queries ([SC] "LLM inference: prefill, decode, KV cache", "7.
 // Practical applications", item 3, and "9. Failure modes and limitations",
-// item 3) with more than 32 rows (q_len * G) per (sequence, KV head): each CTA
-// takes 128 rows of one (sequence, KV head) over one split of the sequence's
-// own tokens, with a causal limit per row.
+// item 3) with more than 16 rows (q_len * G) per (sequence, KV head): a
+// persistent kernel whose CTAs take (split, sequence, KV head, 128-row block)
+// units, longest first, with a causal limit per row.
 
 #include "decode_common.cuh"
 #include "pkv_tc.cuh"
@@ -25,32 +25,32 @@ namespace {
 
 // ----------------------------------------------------------------------------
 // Paged attention of many query rows on the 5th-generation tensor cores
-// (tcgen05 + TMEM), pipelined: the cascade prefix (all B * G query rows of a
-// KV head against the shared prefix) and multi-token queries with more than
-// 32 rows per (sequence, KV head).  One CTA per SM; its warps have fixed roles:
+// (tcgen05 + TMEM), pipelined, one CTA per SM with all 512 TMEM columns.  Its
+// warps have fixed roles:
 //   softmax warps (4 per 128-row group): thread t of a group is its query row
 //              t (= TMEM lane t, in the group's columns)
-//   one TMA producer warp: 64-token K and V tiles into a ring of stages of
-//              128B-swizzled shared memory, one whole-block box per lane
-//   one MMA-issuer warp per group (one lane issues):
-//              S_g(k) = Q_g K(k)^T, then O_g += P_g(k-1) V(k-1)
-//              (a one-group CTA has two: one for S, one for P.V)
-// Q sits in shared memory in the K-major 128B-swizzled layout (A operand of S
-// through a matrix descriptor) when the CTA has two groups, and in TMEM when
-// it has one; K is a K-major and V an MN-major B operand; P (as bf16 hi | lo
-// pairs) comes from TMEM.  While a group's softmax turns
-// S(k) into P(k), the tensor core works on the other group and on S(k+1) and
-// O += P(k-1) V.  Hand-offs are mbarriers: full / empty per stage (TMA bytes;
-// one commit per group after the stage's P.V), and per group and buffer
-// sfull / pfree (MMA commits) and sfree / pfull (one arrive per softmax warp).
-// The softmax keeps a lazy running max: O in TMEM is rescaled only when the
-// max grows by more than 2^8 (then after the previous P.V has completed), so
-// P stays <= 256.  The cascade CTAs of one KV head read the same prefix
-// tiles; each starts at a different tile of its range (the online softmax
-// takes tiles in any order) so that they do not all ask L2 for the same
-// lines at once.  Every wait is bounded; a time-out records the error, raises
-// a shared abort flag that ends every role's loop, and the CTA drains its
-// copies and MMAs before it frees TMEM.
+//   two TMA producer warps: 64-token K and V tiles into a ring of stages of
+//              128B-swizzled shared memory, one box (a block's rows of one
+//              128-byte d-half) per lane
+//   MMA issuers (one lane issues): S(k) = Q K(k)^T and O += P(k) V(k)
+// K is a K-major and V an MN-major B operand; P (as bf16 hi | lo pairs, so
+// that P.V keeps fp32-like accuracy) comes from TMEM.  While a group's
+// softmax turns S(k) into P(k), the tensor core works on S(k+1) and O +=
+// P(k-1) V.  Hand-offs are mbarriers: full / empty per stage (TMA bytes; an
+// MMA commit after the stage's P.V), and per buffer sfull / pfree (MMA
+// commits) and pfull (one arrive per softmax warp).  The softmax keeps a lazy
+// running max: O in TMEM is rescaled only when the max grows by more than
+// 2^8 (then after the previous P.V has completed), so P stays <= 256.  Every
+// wait is bounded; a time-out records the error, raises a shared abort flag
+// that ends every role's loop, and the CTA drains its copies and MMAs before
+// it frees TMEM.
+//
+// The cascade prefix kernel has two groups sharing each tile, Q in shared
+// memory and P over S; its CTAs of one KV head each start at a different
+// tile of their range (the online softmax takes tiles in any order) so that
+// they do not all ask L2 for the same lines at once.  The multi-token kernel
+// has one group, Q in TMEM (A operand of S), P in buffers of its own (so S
+// never waits for a P.V), S and P.V issued by two warps, and six stages.
 // ----------------------------------------------------------------------------
 
 // Wait for a barrier phase; false once the CTA aborts (or on time-out, which
@@ -75,19 +75,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
   }
 }
 
-// Shape of a CTA: GROUPS 128-row groups (2 for the cascade prefix, whose
-// rows all read the same prefix; 1 for multi-token queries, whose rows of one
-// (sequence, KV head) are at most 128 per row block), the ring of K/V stages
-// and the threads (4 softmax warps per group, a producer warp, one MMA-issuer
-// warp per group).  One CTA per SM with all 512 TMEM columns.  Two groups
-// split them (O and a double buffer of S that P overwrites in place); one
-// group keeps P in buffers of its own (SEP), so that S(k+2) never waits for
-// P(k).V, and Q in TMEM as well (S = Q K^T with A from TMEM), which leaves
-// the shared memory to a deeper ring of six stages (its tiles come from HBM,
-// not from L2, and the bytes in flight set its speed).
-template <int D, int GROUPS_>
-struct TcShape {
-  static constexpr int GROUPS = GROUPS_;
+// Tile geometry of the tensor-core kernels: 128 query rows per group, 64-key
+// K and V tiles stored as 128-byte rows (one d-half after the other),
+// 128B-swizzled.
+template <int D>
+struct TcTile {
   static constexpr int M = 128;                       // query rows per group
   static constexpr int NKEY = kCascadeTile;           // keys per tile
   static constexpr int HALVES = D / 64;               // 128-byte d-halves of a row
@@ -95,56 +87,47 @@ struct TcShape {
   static constexpr int HALF_BYTES = NKEY * 128;       // one d-half of a K (or V) tile
   static constexpr int KREG = HALVES * HALF_BYTES;    // K (or V) tile
   static constexpr int STAGE = 2 * KREG;
-  static constexpr bool SEP = GROUPS == 1;            // P in TMEM columns of its own
-  static constexpr bool QT = GROUPS == 1;             // Q in TMEM too (A operand of S from TMEM)
-  static constexpr int QBYTES = QT ? 0 : GROUPS * HALVES * QHALF;
-  static constexpr int NS = GROUPS == 2 ? 4 : 6;
-  // One group: S and P.V are issued by two warps of their own, so that a
-  // P.V whose P is ready never waits behind the next tile's arrival (its
-  // stage is released as early as possible).
-  static constexpr bool SPLIT = GROUPS == 1;
-  static constexpr int ISSUERS = GROUPS * (SPLIT ? 2 : 1);  // MMA-issuing warps
-  // full, empty; sfull, sfree, pfull, pfree x2; done per issuer; Q in TMEM
-  static constexpr int NBARS = 2 * NS + 8 * GROUPS + ISSUERS + 1;
-  static constexpr int BYTES = QBYTES + NS * STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
-  // Two TMA producer warps, which issue a tile's boxes in parallel (one warp
-  // issuing a tile's 16 boxes was measured to hold an SM to about 12-19 bytes
-  // per cycle; four warps measured no faster than two)
-  static constexpr int NPROD = 2;
-  static constexpr int THREADS = 32 * (4 * GROUPS + NPROD + ISSUERS);
-  static constexpr uint32_t TCOLS = 512;
-  static constexpr int MINB = 1;                      // CTAs per SM
 };
 
-// MQ = false: cascade prefix.  Rows (b, g) of KV head blockIdx.y, 256 per CTA
-// (blockIdx.x), over prefix range blockIdx.z; pieces go to workspace slot
-// extra_slot + range.
-// MQ = true: multi-token queries.  Rows (i, g) of sequence blockIdx.z and KV
-// head blockIdx.y / row blocks, 128 per CTA, over split blockIdx.x of the
-// sequence's own tokens with a causal limit per row; a sequence with one split
-// writes `out`, else (acc, m, l) partials for the combine kernel.
-template <int D, int GROUPS, bool MQ>
-__global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS>::MINB)
-    paged_tc_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                              const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+// Cascade prefix CTA: two 128-row groups (their rows all read the same
+// prefix tiles), Q of both in shared memory, four K/V stages, and threads:
+// 4 softmax warps per group, two TMA producer warps, one MMA issuer per
+// group.  One CTA per SM with all 512 TMEM columns, 256 per group: O and a
+// double buffer of S that P overwrites in place.
+template <int D>
+struct CascadeShape : TcTile<D> {
+  using T = TcTile<D>;
+  static constexpr int GROUPS = 2;
+  static constexpr int QBYTES = GROUPS * T::HALVES * T::QHALF;
+  static constexpr int NS = 4;
+  // full, empty; sfull, pfull, pfree x2 per group; done per group
+  static constexpr int NBARS = 2 * NS + 6 * GROUPS + GROUPS;
+  static constexpr int BYTES = QBYTES + NS * T::STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
+  // two producer warps issue a tile's boxes in parallel (one warp issuing a
+  // tile's boxes was measured to hold an SM to about 12-19 bytes per cycle)
+  static constexpr int NPROD = 2;
+  static constexpr int THREADS = 32 * (4 * GROUPS + NPROD + GROUPS);
+};
+
+// Rows (b, g) of KV head blockIdx.y, 256 per CTA (blockIdx.x), over prefix
+// range blockIdx.z; (acc, m, l) pieces go to workspace slot extra_slot +
+// range.
+template <int D>
+__global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
+    cascade_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                          const DecodeParams p) {
   using L = Layout<D, false>;
-  using C = TcShape<D, GROUPS>;
-  constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS;
+  using C = CascadeShape<D>;
+  constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS, GROUPS = C::GROUPS;
   constexpr int kMaxBlocks = 1024;                    // block ids of one range, in shared memory
-  constexpr uint32_t TCOLS = C::TCOLS;
-  constexpr uint32_t GCOLS = TCOLS / GROUPS;          // TMEM columns of one group
-  constexpr bool SEP = C::SEP;
-  // within a group's columns: O, the S double buffer, the P double buffer
-  // (P over S unless SEP)
-  constexpr uint32_t COL_O = 0, COL_S = D, COL_P = SEP ? D + 2 * NKEY : D;
-  constexpr uint32_t COL_Q = COL_P + 2 * NKEY;        // Q as bf16 pairs when QT
+  constexpr uint32_t GCOLS = 512 / GROUPS;            // TMEM columns of one group
+  // within a group's columns: O, then the S double buffer (P over S)
+  constexpr uint32_t COL_O = 0, COL_S = D, COL_P = D;
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
   constexpr int PRODUCER = 4 * GROUPS;                // first producer warp
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(COL_P + 2 * NKEY <= GCOLS, "TMEM columns");
-  static_assert(!C::QT || (SEP && COL_Q + D / 2 <= GCOLS), "TMEM columns for Q");
-  static_assert(!MQ || GROUPS == 1, "one group per multi-token CTA");
+  static_assert(COL_S + 2 * NKEY <= GCOLS, "TMEM columns");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group;
@@ -159,12 +142,10 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   uint64_t* full = bars;
   uint64_t* empty = full + NS;
   uint64_t* sfull = empty + NS;       // [GROUPS][2]
-  uint64_t* sfree = sfull + 2 * GROUPS;  // used when SEP
-  uint64_t* pfull = sfree + 2 * GROUPS;
+  uint64_t* pfull = sfull + 2 * GROUPS;
   uint64_t* pfree = pfull + 2 * GROUPS;
-  uint64_t* done = pfree + 2 * GROUPS;  // [ISSUERS]
-  uint64_t* qready = done + C::ISSUERS;  // Q is in TMEM (one arrive per softmax warp)
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(qready + 1);
+  uint64_t* done = pfree + 2 * GROUPS;  // [GROUPS]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + GROUPS);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_blk = reinterpret_cast<int*>(s_tmem + 4);
 
@@ -175,53 +156,28 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     }
     for (int i = 0; i < 2 * GROUPS; ++i) {
       mbar_init(smem_u32(sfull + i), 1);
-      mbar_init(smem_u32(sfree + i), 4);
       mbar_init(smem_u32(pfull + i), 4);
       mbar_init(smem_u32(pfree + i), 1);
     }
-    for (int i = 0; i < C::ISSUERS; ++i) mbar_init(smem_u32(done + i), 1);
-    mbar_init(smem_u32(qready), 4);
+    for (int i = 0; i < GROUPS; ++i) mbar_init(smem_u32(done + i), 1);
     *s_abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(s_tmem), TCOLS);
+    tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
   wait_prior_grid();
 
   // ---- the CTA's rows, token range [t0, t1) and block list
-  int h, rows, row0, t0, t1, ctx = 0, nsplit = 0, QL = 1;
-  int64_t b_rows = 0;
-  const int32_t* blocks;
-  if constexpr (MQ) {
-    QL = p.q_len;
-    rows = QL * G;
-    const int nrb = (rows + M - 1) / M;
-    h = blockIdx.y / nrb;
-    row0 = (blockIdx.y - h * nrb) * M;
-    const int b = blockIdx.z;
-    b_rows = static_cast<int64_t>(b) * QL;
-    const int ctx_raw = p.context_lens[b];
-    ctx = clamp_ctx(p, ctx_raw);
-    if (ctx != ctx_raw && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) record_error(p.err, kDevErrContextLen);
-    nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-    t0 = blockIdx.x * p.split_tokens;
-    const int row_last = min(rows, row0 + M) - 1;
-    const int lim_last = min(ctx, ctx - QL + row_last / G + 1);   // rows attend monotonically more
-    t1 = t0 < ctx ? min(min(ctx, t0 + p.split_tokens), lim_last) : t0;
-    if (t1 < t0) t1 = t0;
-    blocks = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
-  } else {
-    h = blockIdx.y;
-    rows = p.batch * G;
-    row0 = blockIdx.x * (GROUPS * M);
-    t0 = blockIdx.z * p.prefix_split_tokens;
-    t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
-    blocks = p.prefix_blocks;
-  }
+  const int h = blockIdx.y;
+  const int rows = p.batch * G;
+  const int row0 = blockIdx.x * (GROUPS * M);
+  const int t0 = blockIdx.z * p.prefix_split_tokens;
+  const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
+  const int32_t* blocks = p.prefix_blocks;
   const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
   for (int i = tid; i < nblk && i < kMaxBlocks; i += blockDim.x) {
     int phys = blocks[t0 / p.block_size + i];
@@ -232,10 +188,9 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     s_blk[i] = phys;
   }
   const int ntile = (t1 - t0 + NKEY - 1) / NKEY;
-  // k-th tile processed = tile (k + first) % ntile of the range; cascade CTAs
-  // of one head start at different tiles (they all read the same prefix)
-  const int first =
-      (!MQ && ntile > 0) ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * ntile) / gridDim.x) : 0;
+  // k-th tile processed = tile (k + first) % ntile of the range: the CTAs of
+  // one head start at different tiles (they all read the same prefix)
+  const int first = ntile > 0 ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * ntile) / gridDim.x) : 0;
 
   // ---- Q rows into shared memory: group g, row r, 16-byte chunk c of d-half
   // hf at g * HALVES * QHALF + hf * QHALF + r * 128 + ((c ^ (r % 8)) * 16)
@@ -244,59 +199,30 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   const int r_in = (warp % 4) * 32 + lane;             // row within the group
   const int row = row0 + grp * M + r_in;
   const bool row_ok = warp < PRODUCER && row < rows;
-  // output row of this query row: (b, hq) for the cascade, (b, i, hq) flattened
-  const int64_t orow = MQ ? (b_rows + row / G) * H_q + h * G + row % G
-                          : static_cast<int64_t>(row / G) * H_q + h * G + row % G;
-  uint4 w[D / 8];  // the row of Q: every load issued before the first store
+  const int64_t orow = static_cast<int64_t>(row / G) * H_q + h * G + row % G;  // output row (b, hq)
   if (warp < PRODUCER) {
     const uint16_t* qr = row_ok ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
+    uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
+    uint4 w[D / 8];  // every load issued before the first store
 #pragma unroll
     for (int c = 0; c < D / 8; ++c)
       w[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (!C::QT) {
-      uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const int hf = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
-      }
-      fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
+    for (int c = 0; c < D / 8; ++c) {
+      const int hf = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
     }
+    fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *s_tmem;
-  if constexpr (C::QT) {
-    // row r of Q into TMEM lane r as bf16 pairs (element 2j in the low half
-    // of column j, the memory order of the loaded words)
-    if (warp < PRODUCER) {
-      const uint32_t tq = tbase + COL_Q + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[4 * j] = w[4 * c + j].x;
-          v[4 * j + 1] = w[4 * c + j].y;
-          v[4 * j + 2] = w[4 * c + j].z;
-          v[4 * j + 3] = w[4 * c + j].w;
-        }
-        tmem_st16(tq + 16 * c, v);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(qready));
-    }
-  }
 
   if (warp >= PRODUCER && warp < PRODUCER + C::NPROD) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producers
     // A tile's TMA boxes (K then V; d-half; block) are split evenly over the
-    // producer warps, one box per lane: one thread issuing all of a tile's
-    // boxes back to back was measured to hold a tile to about 16 bytes per
-    // cycle.
+    // producer warps, one box per lane.
     const int pw = warp - PRODUCER;
     const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
     const int per_half = NKEY / box;
@@ -333,69 +259,40 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     }
   } else if (warp >= PRODUCER + C::NPROD) {
     // ------------------------------------------------------------ MMA issuers
-    const int mw = warp - PRODUCER - C::NPROD;         // issuer index
-    const int g = C::SPLIT ? mw / 2 : mw;
-    const int role = C::SPLIT ? mw % 2 : 2;            // 0: S, 1: P.V, 2: both, interleaved
+    // one per group: S(k) = Q K(k)^T, then O += P(k-1) V(k-1)
+    const int g = warp - PRODUCER - C::NPROD;
     const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
     const uint32_t tg = tbase + g * GCOLS;
-    bool ok = true;
-    if (C::QT && role != 1) {
-      if (lane == 0) ok = wait_or_abort(smem_u32(qready), 0u, p.err, s_abort);
-      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-    }
-    for (int k = 0; k <= ntile && ok; ++k) {
-      if (role != 1 && k < ntile) {
+    for (int k = 0; k <= ntile; ++k) {
+      if (k < ntile) {
         const int s = k % NS, b = k & 1;
-        bool ok2 = true;
+        bool ok = true;
         if (lane == 0) {
-          ok2 = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
-          // buffer b: the softmax has read S(k-2) (SEP), or P(k-2).V has
-          // completed (P over S)
-          if (ok2 && k >= 2)
-            ok2 = wait_or_abort(smem_u32((SEP ? sfree : pfree) + 2 * g + b),
-                               static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err, s_abort);
+          ok = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
+          // buffer b: P(k-2).V has completed (P lives over S)
+          if (ok && k >= 2)
+            ok = wait_or_abort(smem_u32(pfree + 2 * g + b), static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err,
+                               s_abort);
         }
-        if (!__shfl_sync(kFull, ok2 ? 1 : 0, 0)) break;
-        const uint32_t kst = stage0 + s * C::STAGE;
-        if constexpr (MQ) {
-          // rows of the last block past the sequence end may hold anything
-          // (NaN included): zero them in the V tile, P is 0 there
-          const int tstart = t0 + ((k + first) % ntile) * NKEY;
-          const int vr0 = ctx - tstart;
-          if (vr0 < NKEY) {
-            uint8_t* vt = smem + (kst - smem_u32(smem)) + C::KREG;
-            const int first_row = vr0 > 0 ? vr0 : 0;
-            const int chunks = (NKEY - first_row) * 8;   // 16-byte chunks per d-half
-            for (int c = lane; c < C::HALVES * chunks; c += 32) {
-              const int hf = c / chunks, cc = c - hf * chunks;
-              *reinterpret_cast<uint4*>(vt + hf * C::HALF_BYTES + first_row * 128 + cc * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-        }
+        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
         if (lane == 0) {
           tc_fence_after();
+          const uint32_t kst = stage0 + s * C::STAGE;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(qa + (kk / 4) * C::QHALF + (kk % 4) * 32, 0, 1024);
             const uint64_t bd = smem_desc_sw128(kst + (kk / 4) * C::HALF_BYTES + (kk % 4) * 32, 0, 1024);
-            if constexpr (C::QT) {
-              tc_mma_ts(tg + COL_S + b * NKEY, tg + COL_Q + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
-            } else {
-              const uint64_t ad = smem_desc_sw128(qa + (kk / 4) * C::QHALF + (kk % 4) * 32, 0, 1024);
-              tc_mma_ss(tg + COL_S + b * NKEY, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-            }
+            tc_mma_ss(tg + COL_S + b * NKEY, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(sfull + 2 * g + b));
         }
       }
-      if (role != 0 && (C::SPLIT ? k < ntile : k >= 1)) {
-        const int j = C::SPLIT ? k : k - 1, sj = j % NS, bj = j & 1;
-        bool ok2 = true;
+      if (k >= 1) {
+        const int j = k - 1, sj = j % NS, bj = j & 1;
+        bool ok = true;
         if (lane == 0)
-          ok2 = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
-        if (!__shfl_sync(kFull, ok2 ? 1 : 0, 0)) break;
+          ok = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
+        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
         if (lane == 0) {
           tc_fence_after();
           const uint32_t vst = stage0 + sj * C::STAGE + C::KREG;
@@ -413,19 +310,16 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
       }
     }
     if (lane == 0) {  // nothing of this thread's may still be running when TMEM is freed
-      tc_commit(smem_u32(done + mw));
-      mbar_wait(smem_u32(done + mw), 0u, nullptr);
+      tc_commit(smem_u32(done + g));
+      mbar_wait(smem_u32(done + g), 0u, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
     const uint32_t tl = tbase + grp * GCOLS + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     uint64_t* g_sfull = sfull + 2 * grp;
-    uint64_t* g_sfree = sfree + 2 * grp;
     uint64_t* g_pfull = pfull + 2 * grp;
     uint64_t* g_pfree = pfree + 2 * grp;
     const float qk_mult = p.qk_log2_scale;
-    // tokens this row may attend: [0, lim); the cascade prefix has no causal limit
-    const int lim = MQ ? (row_ok ? min(t1, ctx - QL + row / G + 1) : t0) : t1;
     float m_used = -CUDART_INF_F, lsum = 0.f;
     bool ok = true;
     for (int k = 0; k < ntile && ok; ++k) {
@@ -450,12 +344,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
             x[16 * c + i + 1] = y.y;
           }
       }
-      if constexpr (SEP) {  // S[b] may be overwritten
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(g_sfree + b));
-      }
-      const int valid = lim - (t0 + ((k + first) % ntile) * NKEY);
+      const int valid = t1 - (t0 + ((k + first) % ntile) * NKEY);  // the prefix has no causal limit
       if (__any_sync(kFull, valid < NKEY)) {
 #pragma unroll
         for (int i = 0; i < NKEY; ++i)
@@ -501,12 +390,6 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
         tmem_wait_st();
       }
       lsum *= alpha;
-      if (SEP && k >= 2) {  // P(k-2).V has read P[b]
-        ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + b), static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err,
-                                             s_abort));
-        if (!ok) break;
-        tc_fence_after();
-      }
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
       const float2 neg_mu = make_float2(-mu, -mu);
       float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -534,37 +417,27 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
     if (ok && ntile > 0)
       ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + ((ntile - 1) & 1)),
                                            static_cast<uint32_t>(((ntile - 1) >> 1) & 1), p.err, s_abort));
-    // ---- this row's result: a workspace piece, or (one split) the output row
-    const bool writes = MQ ? (t0 < ctx || (ctx == 0 && blockIdx.x == 0)) : ntile > 0;
-    const bool direct = MQ && nsplit <= 1;
-    const int64_t piece = orow * p.slots_per_row + (MQ ? static_cast<int64_t>(blockIdx.x) : p.extra_slot + blockIdx.z);
-    if (ok && writes) {
-      if (ntile > 0) tc_fence_after();
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      float* dst_row = direct ? p.out + orow * D : p.ws_o + piece * D;
+    // ---- this row's (acc, m, l) piece of the prefix range
+    const int64_t piece = orow * p.slots_per_row + p.extra_slot + blockIdx.z;
+    if (ok && ntile > 0) {
+      tc_fence_after();
+      float* dst_row = p.ws_o + piece * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[2][16];
-        if (ntile > 0) {
-          tmem_ld16(tl + COL_O + c0, v[0]);
-          tmem_ld16(tl + COL_O + c0 + 16, v[1]);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
-        }
+        tmem_ld16(tl + COL_O + c0, v[0]);
+        tmem_ld16(tl + COL_O + c0 + 16, v[1]);
+        tmem_wait_ld();
         if (row_ok) {
-          const float sc = direct ? inv : 1.f;
           float4* dst = reinterpret_cast<float4*>(dst_row + c0);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]) * sc,
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 1]) * sc,
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 2]) * sc,
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 3]) * sc);
+            dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]), __uint_as_float(v[i / 4][4 * (i % 4) + 1]),
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 2]),
+                                 __uint_as_float(v[i / 4][4 * (i % 4) + 3]));
         }
       }
-      if (row_ok && !direct) {
+      if (row_ok) {
         p.ws_ml[piece * 2] = m_used;
         p.ws_ml[piece * 2 + 1] = lsum;
       }
@@ -575,7 +448,7 @@ __global__ void __launch_bounds__(TcShape<D, GROUPS>::THREADS, TcShape<D, GROUPS
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tbase, TCOLS);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -644,6 +517,10 @@ __global__ void __launch_bounds__(128) wait_selftest_kernel(int which, uint64_t 
 // buffers keep their phases across units.  Every wait is bounded; a time-out
 // records the error and raises the CTA's abort flag, which ends every loop.
 // ----------------------------------------------------------------------------
+// K/V stages of the persistent kernel: its tiles come from HBM, where the
+// bytes in flight set the speed, and Q in TMEM leaves it the shared memory.
+constexpr int kMqStages = 6;
+
 struct MqUnit {
   int b, h, row0, t0, t1, ctx, nsplit, split, ntile;
 };
@@ -718,8 +595,8 @@ __global__ void __launch_bounds__(256, 1)
     mq_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const DecodeParams p) {
   using L = Layout<D, false>;
-  using C = TcShape<D, 1>;
-  constexpr int M = 128, NKEY = C::NKEY, NS = C::NS;
+  using C = TcTile<D>;
+  constexpr int M = 128, NKEY = C::NKEY, NS = kMqStages;
   constexpr int R = 8;                                // unit ring slots
   constexpr int READERS = 7;                          // warps 0-3, 5, 6, 7
   constexpr uint32_t COL_O = 0, COL_S = D, COL_P = D + 2 * NKEY, COL_Q = COL_P + 2 * NKEY;
@@ -1165,7 +1042,7 @@ __global__ void __launch_bounds__(256, 1)
 template <int D>
 int mq_tc_smem_bytes() {
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
-  const int need = TcShape<D, 1>::NS * TcShape<D, 1>::STAGE + 2 * kMultiQueryMaxSplitBlocks * 4 + 64 * 8 + 1024 + 1024;
+  const int need = kMqStages * TcTile<D>::STAGE + 2 * kMultiQueryMaxSplitBlocks * 4 + 64 * 8 + 1024 + 1024;
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 
@@ -1184,22 +1061,16 @@ cudaError_t launch_mq_tc_t(const DecodeParams& p, const CUtensorMap& tk, const C
   return cudaGetLastError();
 }
 
-template <int D, int GROUPS>
-int tc_smem_bytes() {
+template <int D>
+cudaError_t launch_cascade_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
+                             cudaStream_t stream) {
+  auto kern = cascade_prefix_kernel<D>;
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
-  const int need = TcShape<D, GROUPS>::BYTES;
-  return need > 120 * 1024 ? need : 120 * 1024;
-}
-
-template <int D, int GROUPS, bool MQ>
-cudaError_t launch_tc_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
-                        cudaStream_t stream) {
-  auto kern = paged_tc_attention_kernel<D, GROUPS, MQ>;
-  const int smem = tc_smem_bytes<D, GROUPS>();
+  const int smem = CascadeShape<D>::BYTES > 120 * 1024 ? CascadeShape<D>::BYTES : 120 * 1024;
   static bool configured[64] = {};
   cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, grid, dim3(TcShape<D, GROUPS>::THREADS), smem, stream, tk, tv, p);
+  return launch_pdl(kern, grid, dim3(CascadeShape<D>::THREADS), smem, stream, tk, tv, p);
 }
 
 }  // namespace
@@ -1209,8 +1080,8 @@ cudaError_t launch_cascade_prefix(const DecodeParams& p, const CUtensorMap& tk, 
   const int rows = p.batch * p.group;
   const int nps = (p.prefix_len + p.prefix_split_tokens - 1) / p.prefix_split_tokens;
   const dim3 grid((rows + kCascadeRowsTc - 1) / kCascadeRowsTc, p.num_kv_heads, nps);
-  if (p.head_dim == 128) return launch_tc_t<128, 2, false>(p, tk, tv, grid, stream);
-  return launch_tc_t<64, 2, false>(p, tk, tv, grid, stream);
+  if (p.head_dim == 128) return launch_cascade_t<128>(p, tk, tv, grid, stream);
+  return launch_cascade_t<64>(p, tk, tv, grid, stream);
 }
 
 cudaError_t launch_wait_selftest(int which, uint64_t limit_ns, int* err, cudaStream_t stream) {
