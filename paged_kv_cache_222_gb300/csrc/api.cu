@@ -61,10 +61,28 @@ struct DeviceState {
   int sms = 0;
   int* err = nullptr;
   cudaMemPool_t pool = nullptr;
+  // a high-priority stream of the library's own with a fork and a join
+  // event: the cascade prefix runs there beside the suffix decode
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+std::mutex g_fork_mu;  // one fork / join on the side streams at a time
+
+// The device's side stream and events, made on first use.
+pkv_status side_stream(DeviceState* st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->side != nullptr) return PKV_OK;
+  int lo = 0, hi = 0;
+  cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&st->side, cudaStreamNonBlocking, hi);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->join, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(e, "side stream");
+  return PKV_OK;
+}
 
 pkv_status current_device(int* dev, DeviceState** st) {
   cudaError_t e = cudaGetDevice(dev);
@@ -695,6 +713,13 @@ pkv_status pkv_shutdown(void) {
       cudaMemPoolDestroy(s.pool);
       s.pool = nullptr;
     }
+    if (s.side != nullptr) {
+      cudaStreamDestroy(s.side);
+      cudaEventDestroy(s.fork);
+      cudaEventDestroy(s.join);
+      s.side = nullptr;
+      s.fork = s.join = nullptr;
+    }
   }
   return PKV_OK;
 }
@@ -832,9 +857,22 @@ extern "C" pkv_status pkv_cascade_decode_attention(
   p.prefix_split_tokens = pl.prefix_split_tokens;
   p.err = st->err;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = traced(pkv::kKindCascadePrefix, cs, [&] { return pkv::launch_cascade_prefix(p, tkb, tvb, cs); });
+  // The prefix (tensor-core bound, from L2) and the suffix (HBM bound) do not
+  // depend on each other: the prefix runs on the high-priority side stream,
+  // taking its SMs first, while the suffix decode fills the rest; the
+  // combine waits for both.
+  s = side_stream(st);
+  if (s != PKV_OK) return s;
+  std::lock_guard<std::mutex> fj(g_fork_mu);
+  cudaError_t e = cudaEventRecord(st->fork, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st->side, st->fork, 0);
+  if (e == cudaSuccess)
+    e = traced(pkv::kKindCascadePrefix, st->side,
+               [&] { return pkv::launch_cascade_prefix(p, tkb, tvb, st->side); });
+  if (e == cudaSuccess) e = cudaEventRecord(st->join, st->side);
   if (e == cudaSuccess)
     e = traced(pkv::kKindDecodeSplit, cs, [&] { return pkv::launch_decode_split(p, tk, tv, cs); });
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, st->join, 0);
   if (e == cudaSuccess)
     e = traced(pkv::kKindCombine, cs, [&] { return pkv::launch_decode_combine(p, cs); });
   if (e != cudaSuccess) return cuda_fail(e, "cascade decode launch");
