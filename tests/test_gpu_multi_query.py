@@ -174,3 +174,23 @@ def test_tcgen05_split_count_does_not_change_the_result():
     outs = [_run(case, st) for st in (64, 256, 1024, 4096, 16384)]
     for o in outs[1:]:
         assert np.abs(o - outs[0]).max() <= 1e-5
+
+
+def test_tcgen05_many_units_per_cta_full_size():
+    """The GQA workload (B=64, H_kv=8, contexts up to 8208) with 256-token
+    splits: about 16,900 work units, some 110 per persistent CTA, so the ring
+    of published units wraps many times and partials of 33 splits are
+    combined.  Same result as the default plan (one split per sequence)."""
+    q_len = 16
+    case = W.make_case("gqa_bf16", device=DEV, steps=q_len)
+    bt = case["block_tables"].to(DEV)
+    lens = (case["ctx"] + q_len).to(DEV).to(torch.int32)
+    q = case["q"].permute(1, 0, 2, 3).contiguous()
+    mx = int(lens.max())
+    plan = pkv.multi_query_plan(case["B"], q_len, case["H_q"], case["k_cache"], mx, 256, 152)
+    assert plan.workers == 0 and plan.max_splits == -(-mx // 256)
+    a = pkv.multi_query_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"], mx)
+    b = pkv.multi_query_attention(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"], mx,
+                                  split_tokens=256)
+    assert pkv.device_error(DEV) == 0
+    assert np.abs(a.cpu().numpy() - b.cpu().numpy()).max() <= 1e-5
