@@ -249,11 +249,11 @@ pkv_status pkv_decode_attention_noalloc(const void* q, int32_t batch, int32_t nu
  *   PKV_ERR_UNSUPPORTED).  Scratch: at least plan.workspace_bytes from
  *   pkv_cascade_plan, 256-byte aligned.
  *
- * The prefix product runs on a high-priority stream the library owns (one per
- * device, made on first use, destroyed by pkv_shutdown), forked from `stream`
- * and joined back to it by events before the combine, so that it shares the
- * GPU with the suffix decode; the call stays asynchronous and ordered on
- * `stream` (also under stream capture).
+ * The prefix product runs on `stream`; the suffix decode runs beside it on a
+ * stream the library owns (one per device, made on first use, destroyed by
+ * pkv_shutdown), forked from `stream` and joined back to it by events before
+ * the combine; the call stays asynchronous and ordered on `stream` (also
+ * under stream capture).
  *
  * pkv_cascade_plan (host only): mode 2; split_tokens / max_splits describe the
  * suffix splits, workers the number of prefix ranges and prefix_split_tokens

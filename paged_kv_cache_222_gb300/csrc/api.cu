@@ -61,8 +61,8 @@ struct DeviceState {
   int sms = 0;
   int* err = nullptr;
   cudaMemPool_t pool = nullptr;
-  // a high-priority stream of the library's own with a fork and a join
-  // event: the cascade prefix runs there beside the suffix decode
+  // a stream of the library's own with a fork and a join event: the
+  // cascade's suffix decode runs there beside the prefix
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
@@ -75,9 +75,7 @@ std::mutex g_fork_mu;  // one fork / join on the side streams at a time
 pkv_status side_stream(DeviceState* st) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->side != nullptr) return PKV_OK;
-  int lo = 0, hi = 0;
-  cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
-  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&st->side, cudaStreamNonBlocking, hi);
+  cudaError_t e = cudaStreamCreateWithFlags(&st->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->join, cudaEventDisableTiming);
   if (e != cudaSuccess) return cuda_fail(e, "side stream");
@@ -858,20 +856,20 @@ extern "C" pkv_status pkv_cascade_decode_attention(
   p.err = st->err;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The prefix (tensor-core bound, from L2) and the suffix (HBM bound) do not
-  // depend on each other: the prefix runs on the high-priority side stream,
-  // taking its SMs first, while the suffix decode fills the rest; the
+  // depend on each other.  The prefix is launched first, on the caller's
+  // stream, so that its CTAs (one per SM) take their SMs before the suffix
+  // decode, forked onto the library's side stream, fills the rest; the
   // combine waits for both.
   s = side_stream(st);
   if (s != PKV_OK) return s;
   std::lock_guard<std::mutex> fj(g_fork_mu);
   cudaError_t e = cudaEventRecord(st->fork, cs);
+  if (e == cudaSuccess)
+    e = traced(pkv::kKindCascadePrefix, cs, [&] { return pkv::launch_cascade_prefix(p, tkb, tvb, cs); });
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st->side, st->fork, 0);
   if (e == cudaSuccess)
-    e = traced(pkv::kKindCascadePrefix, st->side,
-               [&] { return pkv::launch_cascade_prefix(p, tkb, tvb, st->side); });
+    e = traced(pkv::kKindDecodeSplit, st->side, [&] { return pkv::launch_decode_split(p, tk, tv, st->side); });
   if (e == cudaSuccess) e = cudaEventRecord(st->join, st->side);
-  if (e == cudaSuccess)
-    e = traced(pkv::kKindDecodeSplit, cs, [&] { return pkv::launch_decode_split(p, tk, tv, cs); });
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, st->join, 0);
   if (e == cudaSuccess)
     e = traced(pkv::kKindCombine, cs, [&] { return pkv::launch_decode_combine(p, cs); });
