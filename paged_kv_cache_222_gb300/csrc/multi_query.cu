@@ -9,17 +9,17 @@
 //
 // Design (GB300):
 //  * Rows are (query token i, head g) pairs of one KV head: R = q_len * G of
-//    them share every K/V byte.  A CTA takes up to 64 rows of one (sequence,
-//    KV head) (the library sends it up to 16: more go to the persistent
-//    tcgen05 kernel of cascade.cu, which is faster there) over one split of `split_tokens` tokens, streamed in 64-token
-//    tiles (four 16-token TMA sub-tiles of K and V, 128B-swizzled, two or
-//    three stages, full / empty mbarriers, block ids of the split staged in
-//    shared memory).
-//  * Warps are arranged as row groups x token lanes: with R <= 16 all four
-//    warps hold the same 16 rows and each takes one sub-tile of every tile;
-//    R <= 32 gives two groups of two lanes; larger R one 16-row group per
-//    warp.  Lanes of a group merge (m, l, acc) through shared memory at the
-//    end, so no warp idles when q_len * G is small.
+//    them share every K/V byte.  A CTA takes up to 16 rows of one (sequence,
+//    KV head) (more go to the persistent tcgen05 kernel of cascade.cu) over
+//    one split of `split_tokens` tokens, streamed in 64-token tiles, block
+//    ids of the split staged in shared memory.
+//  * All four warps hold the same 16 rows; warp w takes tokens 16w..16w+15
+//    of every tile, loading them itself (one 16-token TMA box per lane, K
+//    and V, 128B-swizzled, into its part of a two-stage ring, on barriers of
+//    its own) and refilling its slot as soon as it has read it, so no warp
+//    waits for another.  The warps merge (m, l, acc) through shared memory
+//    at the end.  (The row-group x token-lane shapes for 17-64 rows are in
+//    the template but not instantiated.)
 //  * S = Q K^T and O += P V are mma.sync m16n8k16 tiles (bf16, fp32
 //    accumulate); P is fed as a bf16 hi + lo pair.  The causal limit is per
 //    row; V rows past the end of the sequence are zeroed in registers.
@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
   constexpr int NS = MqShape<TL>::NS;
   constexpr int DP = D + 4;
   static_assert(4 * 16 * DP * 4 + 4 * 16 * 2 * 4 <= NS * STAGE, "merge buffer fits the stages");
+  static_assert(TL == 4, "each warp loads and reads its own 16-token sub-tile of every tile");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, j = lane & 3;
@@ -69,16 +70,12 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
-  uint64_t* empty = full + NS;
-  int* s_blk = reinterpret_cast<int*>(empty + NS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);  // [NS][4]: per stage and warp
+  int* s_blk = reinterpret_cast<int*>(full + 4 * NS);
   const uint32_t stage0 = smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 4);
-    }
+    for (int s = 0; s < 4 * NS; ++s) mbar_init(smem_u32(full + s), 1);
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
@@ -120,32 +117,33 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
   }
   __syncthreads();
 
-  // Warp 0 loads tile k: lane 0 arms the stage's barrier, then every lane
-  // issues one 16-token TMA box (one thread issuing all of a tile's boxes was
-  // measured to hold a stage to about 16 bytes per cycle).
-  constexpr int NBOXES = 2 * NSUB * L::NBOX;  // K and V boxes of a tile (<= 32)
+  // Each warp loads its own 16-token sub-tile (warp w: tokens 16w..16w+15
+  // of every 64-token tile) into its part of the stage, on a barrier of its
+  // own, one TMA box per lane (K and V, per 128-byte column band), and
+  // refills the slot as soon as it has read it: no warp waits for another,
+  // and a tile's boxes are issued by four warps at once (one warp issuing
+  // all of a tile's boxes held an SM to about 12-19 bytes per cycle).
   auto issue = [&](int k) {
     const int s = k % NS;
-    const uint32_t dst = stage0 + s * STAGE;
-    const uint32_t bar = smem_u32(full + s);
+    const uint32_t dst = stage0 + s * STAGE + warp * L::STAGEB;
+    const uint32_t bar = smem_u32(full + 4 * s + warp);
     if (lane == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, STAGE);
+      fence_proxy_async_smem();  // this warp's reads of the slot come before the copy
+      mbar_arrive_expect_tx(bar, L::STAGEB);
     }
     __syncwarp();
-    if (lane < NBOXES) {
-      const int v = lane / (NSUB * L::NBOX);
-      const int i = (lane / L::NBOX) % NSUB;
+    if (lane < 2 * L::NBOX) {
+      const int v = lane / L::NBOX;
       const int bx = lane % L::NBOX;
-      const int t = t_begin + k * kMultiQueryTile + i * kTileTokens;
+      const int t = t_begin + k * kMultiQueryTile + warp * kTileTokens;
       const int bi = (t - t_begin) / p.block_size;
       const int phys = (t < t_stop && bi < kMultiQueryMaxSplitBlocks) ? s_blk[bi] : -1;
-      tma_load_4d(dst + i * L::STAGEB + v * L::TILEB + bx * L::BOX_BYTES, v ? &tmap_v : &tmap_k, bar,
-                  bx * L::BOX_ELEMS, t % p.block_size, h, phys);
+      tma_load_4d(dst + v * L::TILEB + bx * L::BOX_BYTES, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS,
+                  t % p.block_size, h, phys);
     }
   };
-  if (warp == 0)
-    for (int k = 0; k < ntile && k < NS; ++k) issue(k);
+  int issued = 0;
+  for (; issued < ntile && issued < NS; ++issued) issue(issued);
 
   // query fragments (A operand of S = Q K^T): rows ra and rb = ra + 8
   const int ra = row0 + rg * 16 + r, rb = ra + 8;
@@ -181,7 +179,7 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
   for (int k = 0; k < ntile; ++k) {
     const int s = k % NS;
     const uint32_t par = static_cast<uint32_t>((k / NS) & 1);
-    const bool arrived = mbar_wait(smem_u32(full + s), par, p.err);
+    const bool arrived = mbar_wait(smem_u32(full + 4 * s + warp), par, p.err);
     if (!__all_sync(kFull, arrived)) healthy = false;
     const uint32_t base = stage0 + s * STAGE;
     const int tile_t0 = t_begin + k * kMultiQueryTile;
@@ -282,21 +280,14 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
         }
       }
     }
-    // ---- release the stage; warp 0 refills it once all four warps are done
+    // ---- this warp has read its part of the slot: refill it
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(empty + s));
-    if (warp == 0 && healthy && k + NS < ntile) {
-      const bool freed = lane == 0 ? mbar_wait(smem_u32(empty + s), par, p.err) : true;
-      if (__shfl_sync(kFull, freed ? 1 : 0, 0)) issue(k + NS);
-    }
-    __syncwarp();
+    if (healthy && k + NS < ntile) issue(issued++);
   }
-  if (!healthy && threadIdx.x == 0) {
-    // a copy may still be landing: one more bounded wait per stage
-    for (int s = 0; s < NS && s < ntile; ++s) {
-      const int klast = s + ((ntile - 1 - s) / NS) * NS;
-      mbar_wait(smem_u32(full + s), static_cast<uint32_t>((klast / NS) & 1), nullptr);
-    }
+  if (!healthy && lane == 0) {
+    // a copy of this warp's may still be landing: one more bounded wait each
+    for (int kk = issued > NS ? issued - NS : 0; kk < issued; ++kk)
+      mbar_wait(smem_u32(full + 4 * (kk % NS) + warp), static_cast<uint32_t>((kk / NS) & 1), nullptr);
   }
   allow_next_grid();
 
@@ -363,7 +354,7 @@ cudaError_t launch_mq_t(const DecodeParams& p, const CUtensorMap& tk, const CUte
                         cudaStream_t stream) {
   auto kern = multi_query_kernel<D, TL>;
   const int stage = (kMultiQueryTile / kTileTokens) * 2 * kTileTokens * D * 2;
-  const int smem = MqShape<TL>::NS * stage + 6 * 8 + kMultiQueryMaxSplitBlocks * 4 + 1024;
+  const int smem = MqShape<TL>::NS * stage + 4 * MqShape<TL>::NS * 8 + kMultiQueryMaxSplitBlocks * 4 + 1024;
   static bool configured[64] = {};
   cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
