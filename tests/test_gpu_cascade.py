@@ -88,3 +88,47 @@ def test_cascade_sharp_softmax():
     for (b, h), snap in snaps.items():
         ref = S.oracle_unit(case, b, h, 0, snap)
         assert np.max(np.abs(got[b, h * 8:(h + 1) * 8] - ref)) <= 2e-3
+
+
+def test_cascade_under_graph_capture_and_on_two_streams():
+    """The call forks its suffix decode onto the library's side stream and
+    joins it back: captured into a CUDA graph and replayed, and issued on two
+    streams at once, it gives the eager result bit for bit."""
+    case = shared_case(9, 256, (1, 200), 8, 2, 128, 16, seed=20260711)
+    out_c, _ = run_cascade(case)                      # appends the new token, eager result
+    bs = case["bs"]
+    bt = case["block_tables"].to(DEV)
+    lens = (case["ctx"].to(DEV) + 1).to(torch.int32)
+    mx = int(case["ctx"].max()) + 1
+    prefix = case["prefix"]
+    pblocks = bt[0, : prefix // bs].contiguous()
+    q = case["q"][0].contiguous()
+    plan = pkv.cascade_plan(q.shape[0], q.shape[1], pkv.cache_desc(case["k_cache"]), prefix, mx)
+
+    def call(out, ws):
+        return pkv.cascade_decode_attention(q, case["k_cache"], case["v_cache"], pblocks, prefix, bt, lens,
+                                            case["scale"], mx, out=out, workspace=ws)
+
+    want = out_c.cpu()
+    outs = [torch.empty_like(out_c) for _ in range(3)]
+    wss = [torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=DEV) for _ in range(3)]
+    s1, s2 = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        call(outs[0], wss[0])
+    with torch.cuda.stream(s2):
+        call(outs[1], wss[1])
+    torch.cuda.current_stream().wait_stream(s1)
+    torch.cuda.current_stream().wait_stream(s2)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].cpu(), want) and torch.equal(outs[1].cpu(), want)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(outs[2], wss[2])
+    outs[2].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[2].cpu(), want)
+    assert pkv.device_error(DEV) == 0

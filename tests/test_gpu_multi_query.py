@@ -194,3 +194,45 @@ def test_tcgen05_many_units_per_cta_full_size():
                                   split_tokens=256)
     assert pkv.device_error(DEV) == 0
     assert np.abs(a.cpu().numpy() - b.cpu().numpy()).max() <= 1e-5
+
+
+def test_tcgen05_under_graph_capture_and_on_two_streams():
+    """The persistent kernel's unit counter and order live in each call's
+    workspace: two calls at once on two streams, and a captured call
+    replayed from a CUDA graph, give the eager result bit for bit."""
+    case = _small_case([700, 33, 4100, 1, 1500], 16, 16, 2, 128, 16, seed=20260712)
+    dev = torch.device(DEV)
+    q, kc, vc = case["q"].to(dev), case["kc"].to(dev), case["vc"].to(dev)
+    tbl = torch.from_numpy(case["table"]).to(dev)
+    lens = torch.from_numpy(case["ctx"]).to(dev)
+    mx = int(case["ctx"].max())
+    plan = pkv.multi_query_plan(q.shape[0], q.shape[1], q.shape[2], kc, mx, 256, 152)
+    assert plan.workers == 0
+
+    def call(out, ws):
+        return pkv.multi_query_attention(q, kc, vc, tbl, lens, case["scale"], mx, split_tokens=256, out=out,
+                                         workspace=ws)
+
+    want = call(None, None).cpu()
+    outs = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3)]
+    wss = [torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dev) for _ in range(3)]
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        call(outs[0], wss[0])
+    with torch.cuda.stream(s2):
+        call(outs[1], wss[1])
+    torch.cuda.current_stream().wait_stream(s1)
+    torch.cuda.current_stream().wait_stream(s2)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].cpu(), want) and torch.equal(outs[1].cpu(), want)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(outs[2], wss[2])
+    outs[2].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[2].cpu(), want)
+    assert pkv.device_error(DEV) == 0
+    assert np.abs(want.numpy() - _oracle(case)).max() <= 2e-3
