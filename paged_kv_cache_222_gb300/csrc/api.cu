@@ -746,15 +746,27 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
   const int32_t suffix = max_ctx - prefix_len;
   const int32_t st = auto_split_tokens(batch, c->num_kv_heads, suffix > 0 ? suffix : 1, sms);
   const int64_t splits = suffix > 0 ? ceil_div(suffix, st) : 1;
-  // prefix ranges: the prefix kernel runs one CTA per SM; pick the number of
-  // ranges that minimises (waves of CTAs) x (tiles per range + two tiles of
-  // per-CTA overhead); fewer ranges on ties (fewer pieces to combine)
+  // Prefix ranges.  The prefix kernel runs one CTA (256 rows x one range)
+  // per SM and the suffix decode runs beside it on the other SMs, so the
+  // number of ranges n is the one that minimises the longer of (a) the
+  // prefix CTAs' own time, waves x (tiles per range + two tiles of per-CTA
+  // cost), and (b) prefix and suffix work spread over every SM.  Work is in
+  // prefix-tile units: on GB300 a 64-key tile of a 256-row CTA took about as
+  // long as one SM streams 92 KB of suffix K/V (2.2 us at 42 KB/us).  Fewer
+  // ranges on ties (fewer pieces to combine).  On the 128-sequence workload
+  // this picks 2 ranges (call 83.6 us; 4 ranges 93.1 us).
   const int64_t rows = static_cast<int64_t>(batch) * (num_q_heads / c->num_kv_heads);
   const int64_t row_blocks = ceil_div(rows, pkv::kCascadeRowsTc) * c->num_kv_heads;
   const int64_t tiles = ceil_div(prefix_len, pkv::kCascadeTile);
-  int64_t nps = 1, best = -1;
+  const double suffix_work = static_cast<double>(batch) * c->num_kv_heads * (suffix > 0 ? suffix : 0) * 2.0 *
+                             c->head_dim * 2.0 / (92.0 * 1024.0);
+  int64_t nps = 1;
+  double best = -1.0;
   for (int64_t n = 1; n <= tiles && n <= 64; ++n) {
-    const int64_t est = ceil_div(row_blocks * n, sms) * (ceil_div(tiles, n) + 2);
+    const int64_t per_cta = ceil_div(tiles, n) + 2;
+    const double own = static_cast<double>(ceil_div(row_blocks * n, sms) * per_cta);
+    const double spread = (static_cast<double>(row_blocks * n * per_cta) + suffix_work) / sms;
+    const double est = own > spread ? own : spread;
     if (best < 0 || est < best) {
       best = est;
       nps = n;
