@@ -174,6 +174,19 @@ pkv_status pkv_bm_eviction_candidates(pkv_block_manager* bm, int64_t seq_id, con
                                       int32_t* logical, int32_t* n_out);
 
 /*
+ * Prefetch candidates, the other half of the same policy ([UI] "Predictive
+ * Prefetching and Attention-Salience Eviction Policy": an evicted block whose
+ * predicted activation exceeds the prefetch threshold is staged some steps
+ * ahead of the decode step that needs it): the host entries j of a sequence
+ * with activation[j] > threshold, most probable first (ties by index), at
+ * most `capacity` and at most the free device blocks, so that staging all of
+ * them succeeds.  *n_out is how many were written.
+ *   activation  float [entries of the sequence], host memory.
+ */
+pkv_status pkv_bm_prefetch_candidates(pkv_block_manager* bm, int64_t seq_id, const float* activation,
+                                      float threshold, int32_t capacity, int32_t* logical, int32_t* n_out);
+
+/*
  * pkv_copy_blocks_between — pair i copies block src_blocks[i] of the source
  * pool (src_k, src_v; src_num_blocks blocks) to block dst_blocks[i] of the
  * destination pool; both pools have the block geometry and dtype of `cache`

@@ -204,6 +204,16 @@ class BlockManagerModel:
              if j not in pin and j not in host and salience[j] < threshold]
         return sorted(c, key=lambda j: (salience[j], j))
 
+    def prefetch_candidates(self, seq_id, activation, threshold, capacity=None):
+        """Host entries with activation above the threshold, most probable
+        first (ties by index), no more than `capacity` nor the free device
+        blocks ([UI] "Predictive Prefetching and Attention-Salience Eviction
+        Policy": evicted blocks predicted to be needed are staged ahead)."""
+        host = self.on_host[seq_id]
+        c = sorted((j for j in host if activation[j] > threshold), key=lambda j: (-activation[j], j))
+        cap = len(c) if capacity is None else capacity
+        return c[:min(cap, len(self.free))]
+
     def _append_one(self, seq_id, n_new, slots, cows):
         bs = self.block_size
         tbl = self.tables[seq_id]

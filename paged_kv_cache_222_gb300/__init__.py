@@ -462,6 +462,17 @@ class BlockManager:
                                                        ctypes.byref(n)), "pkv_bm_eviction_candidates")
         return out[:n.value].copy()
 
+    def prefetch_candidates(self, seq_id, activation, threshold, capacity=None):
+        """Host entries to stage ahead: activation > threshold, most probable
+        first, at most `capacity` and the free device blocks."""
+        act = np.ascontiguousarray(activation, dtype=np.float32)
+        cap = len(act) if capacity is None else int(capacity)
+        out = np.empty(max(cap, 1), dtype=np.int32)
+        n = ctypes.c_int32()
+        _bm_check(library().pkv_bm_prefetch_candidates(self._h, int(seq_id), _np_ptr(act), float(threshold), cap,
+                                                       _np_ptr(out), ctypes.byref(n)), "pkv_bm_prefetch_candidates")
+        return out[:n.value].copy()
+
     def block_tables(self, seq_ids, max_blocks_per_seq):
         """(block_tables int32 [n, max_blocks_per_seq] with -1 past each table, lens int32 [n])."""
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)

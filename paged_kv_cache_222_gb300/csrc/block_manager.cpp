@@ -470,4 +470,27 @@ pkv_status pkv_bm_eviction_candidates(pkv_block_manager* bm, int64_t seq_id, con
   return PKV_OK;
 }
 
+pkv_status pkv_bm_prefetch_candidates(pkv_block_manager* bm, int64_t seq_id, const float* activation,
+                                      float threshold, int32_t capacity, int32_t* logical, int32_t* n_out) {
+  if (bm == nullptr || n_out == nullptr) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (capacity < 0) return fail(PKV_ERR_INVALID_ARG, "capacity %d", capacity);
+  std::lock_guard<std::mutex> lk(bm->mu);
+  Manager::Seq* sq;
+  pkv_status s = find_seq(bm, seq_id, &sq);
+  if (s != PKV_OK) return s;
+  const int64_t n = static_cast<int64_t>(sq->blocks.size());
+  if (n > 0 && activation == nullptr) return fail(PKV_ERR_INVALID_ARG, "activation is NULL");
+  std::vector<int32_t> c;
+  for (int64_t j = 0; j < n; ++j)
+    if (sq->on_host[static_cast<size_t>(j)] && activation[j] > threshold) c.push_back(static_cast<int32_t>(j));
+  std::stable_sort(c.begin(), c.end(), [&](int32_t a, int32_t b) { return activation[a] > activation[b]; });
+  size_t keep = c.size();
+  if (keep > static_cast<size_t>(capacity)) keep = static_cast<size_t>(capacity);
+  if (keep > bm->free_stack.size()) keep = bm->free_stack.size();
+  if (keep > 0 && logical == nullptr) return fail(PKV_ERR_INVALID_ARG, "logical is NULL");
+  for (size_t i = 0; i < keep; ++i) logical[i] = c[i];
+  *n_out = static_cast<int32_t>(keep);
+  return PKV_OK;
+}
+
 }  // extern "C"

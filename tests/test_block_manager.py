@@ -207,6 +207,10 @@ def test_native_host_tier_matches_the_model(seed):
             w = rng.choice([0, 1, bs, 3 * bs])
             assert native.eviction_candidates(s, sal, 0.1, w).tolist() == \
                 model.eviction_candidates(s, sal, 0.1, w)
+            act = [rng.choice([0.0, 0.2, 0.35, 0.6, 0.9]) for _ in range(n)]
+            cap = rng.randint(0, n + 1)
+            assert native.prefetch_candidates(s, act, 0.3, cap).tolist() == \
+                model.prefetch_candidates(s, act, 0.3, cap)
         else:
             s = rng.choice(live)
             k = rng.randint(1, 2 * bs)

@@ -247,6 +247,28 @@ def test_eviction_candidates_keep_sinks_and_the_local_window():
     assert m.eviction_candidates(0, sal, 0.1, local_window=0) == [7, 8, 9, 10, 2, 4, 5]
 
 
+def test_prefetch_candidates_most_probable_first_within_the_free_blocks():
+    # [UI] "Predictive Prefetching and Attention-Salience Eviction Policy":
+    # an evicted block whose predicted activation is above the prefetch
+    # threshold is staged ahead of need; most probable first, and no more
+    # than the device can take.
+    m = BlockManagerModel(10, 4, num_host_blocks=8)
+    m.add_sequence(0)
+    m.append([0], [8 * 4])                    # 8 device blocks, 2 free
+    m.evict(0, [1, 3, 4, 6, 7])               # 7 free
+    act = [0.9, 0.5, 0.99, 0.05, 0.5, 0.7, 0.8, 0.31]
+    # host entries 1, 3, 4, 6, 7 with activation 0.5, 0.05, 0.5, 0.8, 0.31
+    assert m.prefetch_candidates(0, act, 0.3) == [6, 1, 4, 7]
+    assert m.prefetch_candidates(0, act, 0.3, capacity=2) == [6, 1]
+    assert m.prefetch_candidates(0, act, 0.9) == []
+    m.add_sequence(1)
+    m.append([1], [6 * 4])                    # leaves one free device block
+    assert len(m.free) == 1
+    assert m.prefetch_candidates(0, act, 0.3) == [6]
+    m.stage(0, [6])
+    assert m.prefetch_candidates(0, act, 0.3) == []
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_random_tier_moves_keep_every_sequence_view(seed):
     rng = random.Random(100 + seed)
