@@ -147,6 +147,60 @@ def oracle_throughput(case, seconds, order_seed=0, return_outputs=False):
     return throughput_gbs, done, procs, wall
 
 
+def _oracle_mq_unit_worker(args):
+    """Oracle multi-token attention of one (sequence, KV head) unit; returns
+    (seconds, (b, h), output [q_len, G, D])."""
+    import numpy as np
+    from oracle import paged_attention as PA
+    key, q_bits, k_blocks, v_blocks, ctx, scale = args
+    table = np.arange(k_blocks.shape[0], dtype=np.int32)[None, :]
+    t0 = time.perf_counter()
+    out = PA.multi_query_attention(q_bits[None], k_blocks, v_blocks, PA.BF16, table, np.array([ctx]), scale)
+    return time.perf_counter() - t0, key, out[0]
+
+
+def oracle_mq_throughput(case, q, lens, seconds):
+    """The oracle's multi-token attention over (sequence, KV head) units of
+    q [B, q_len, H_q, D] against the cache as it is, lens [B] tokens each
+    (the new ones included), in a spawn pool of one process per host core,
+    until `seconds` of wall time are used.  Returns (KV GB/s, units,
+    processes, wall seconds, {(b, h): output [q_len, G, D]})."""
+    import multiprocessing as mp
+    import numpy as np
+    import torch
+    from tests.gpu_support import bits16
+    cores = len(os.sched_getaffinity(0))
+    procs = max(1, min(cores, 32))
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    G = case["H_q"] // case["H_kv"]
+    units = [(b, h) for b in range(case["B"]) for h in range(case["H_kv"])]
+    np.random.default_rng(1).shuffle(units)
+    L = lens.cpu().tolist()
+    qb = bits16(q)
+
+    def payload(b, h):
+        n = -(-L[b] // case["bs"])
+        ids = case["block_tables"][b, :n].to(torch.int64).to(case["k_cache"].device)
+        return ((b, h), qb[b, :, h * G:(h + 1) * G], bits16(case["k_cache"][ids][:, h:h + 1]),
+                bits16(case["v_cache"][ids][:, h:h + 1]), L[b], case["scale"])
+
+    done_bytes, done, outputs = 0, 0, {}
+    with mp.get_context("spawn").Pool(procs) as pool:
+        pool.map(_noop, range(procs))
+        t0 = time.perf_counter()
+        i = 0
+        while i < len(units) and time.perf_counter() - t0 < seconds:
+            batch = units[i:i + procs]
+            for _, key, out in pool.map(_oracle_mq_unit_worker, [payload(b, h) for b, h in batch]):
+                outputs[key] = out
+            done_bytes += sum(L[b] * case["D"] * 4 for b, _ in batch)
+            done += len(batch)
+            i += procs
+        wall = time.perf_counter() - t0
+    return done_bytes / wall / 1e9, done, procs, wall, outputs
+
+
 def _noop(_):
     import numpy  # noqa: F401
     from oracle import paged_attention  # noqa: F401
@@ -560,6 +614,7 @@ def run_op(args, local_rank):
     (cascade decode, multi-token query, block copy, host swap); device-timed
     with CUDA events on the launching stream, per-kernel times from the
     library's trace."""
+    import numpy as np
     import torch
     import paged_kv_cache_222_gb300 as pkv
     import workloads as W
@@ -626,6 +681,17 @@ def run_op(args, local_rank):
                                 "suffix_split_tokens": plan.split_tokens},
                      "kernel_times_ms": {k: {"launches": nn, "avg_ms": tt / nn} for k, (nn, tt) in tr.items() if nn},
                      "roofline": dominant, "roofline_other_kernel": other})
+        if not args.no_cpu_baseline:
+            # the oracle (plain decode of every sequence's whole context; the
+            # cascade reaches the same result) on (sequence, KV head) units
+            gbs, nu, procs, wall, ref = oracle_throughput(case, args.cpu_seconds, return_outputs=True)
+            got = out.cpu().numpy()
+            G = case["H_q"] // case["H_kv"]
+            err = max(float(np.abs(got[b, h * G:(h + 1) * G] - r).max()) for (b, h), r in ref.items())
+            line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle",
+                                    "sample": f"{nu} of {B * case['H_kv']} (sequence, KV head) units, "
+                                              f"{wall:.1f} s wall, float64 numpy, one process per core"}
+            line["parity"] = {"max_abs_err": err, "units": nu, "tolerance": 2e-3}
     elif args.op == "multi_query":
         ql = args.q_len
         case = W.make_case(args.workload, device=dev, steps=ql)
@@ -662,6 +728,15 @@ def run_op(args, local_rank):
                                   "peak_source": f"{hbm_kind} (hbm_gbs, copy bandwidth)",
                                   "algorithmic_bytes_per_launch": kv, "avg_launch_ms": k_ms,
                                   "tensor_TFLOPs": flops / (k_ms / 1e3) / 1e12, "traffic": None}})
+        if not args.no_cpu_baseline:
+            gbs, nu, procs, wall, ref = oracle_mq_throughput(case, q, lens, args.cpu_seconds)
+            got = out.cpu().numpy()
+            G = case["H_q"] // case["H_kv"]
+            err = max(float(np.abs(got[b, :, h * G:(h + 1) * G] - r).max()) for (b, h), r in ref.items())
+            line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle",
+                                    "sample": f"{nu} of {B * case['H_kv']} (sequence, KV head) units, "
+                                              f"{wall:.1f} s wall, float64 numpy, one process per core"}
+            line["parity"] = {"max_abs_err": err, "units": nu, "tolerance": 2e-3}
     else:
         nb, hkv, bs, d = 40000, 8, 16, 128
         kc = torch.zeros((nb, hkv, bs, d), dtype=torch.bfloat16, device=dev)
@@ -670,6 +745,8 @@ def run_op(args, local_rank):
         g = torch.Generator().manual_seed(20260500)
         if args.op == "block_copy":
             npairs = 8192
+            for c in (kc, vc):  # random bits, so that a copy shows
+                c.view(torch.int16).copy_(torch.randint(-2**15, 2**15, c.shape, dtype=torch.int16, device=dev))
             perm = torch.randperm(nb, generator=g)
             src = perm[:npairs].to(torch.int32).to(dev)
             dst = perm[npairs:2 * npairs].to(torch.int32).to(dev)
@@ -684,6 +761,24 @@ def run_op(args, local_rank):
                                       "unit": "GB/s", "frac": gbs / hbm,
                                       "peak_source": f"{hbm_kind} (hbm_gbs, copy bandwidth)",
                                       "algorithmic_bytes_per_launch": byts, "avg_launch_ms": ms, "traffic": None}})
+            if not args.no_cpu_baseline:
+                # the oracle's copy on a sample of the pairs (host copies of
+                # the blocks involved), timed, and the GPU pool checked against
+                # it bit for bit
+                from oracle.block_manager import copy_blocks as oracle_copy_blocks
+                ns = 512
+                s_ids, d_ids = src[:ns].cpu().tolist(), dst[:ns].cpu().tolist()
+                sample = torch.tensor(s_ids + d_ids, dtype=torch.int64, device=dev)
+                host = kc[sample].view(torch.int16).cpu().numpy()  # src blocks, then dst blocks
+                pairs = [(i, ns + i) for i in range(ns)]
+                t0 = time.perf_counter()
+                want = oracle_copy_blocks(host, pairs)
+                wall = time.perf_counter() - t0
+                same = bool(np.array_equal(want[ns:], host[ns:]))   # the pool was copied already
+                line["cpu_baseline"] = {"value": ns * blk * 2 / wall / 1e9, "unit": "GB/s", "cores": 1,
+                                        "kind": "oracle", "sample": f"{ns} of {npairs} pairs of the K cache "
+                                                                  f"(read + write), {wall * 1e3:.1f} ms, numpy"}
+                line["parity"] = {"bit_exact": same, "pairs": ns}
         else:
             nh = 8192
             hk, hv = pkv.host_pool_like(kc, nh)
