@@ -928,12 +928,14 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
   const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * nrb;
   int32_t st = split_tokens;
   if (st == 0) {
-    // mma.sync: the largest power of two (256..4096) that still gives about
-    // four waves of CTAs (two per SM) when every sequence is as long as the
-    // bound.  tcgen05 (persistent, longest units first): the largest power of
-    // two up to the longest split (1024 blocks) that still gives three units
-    // per SM (larger units cost less per token: one setup, fewer partials)
-    const int64_t want = static_cast<int64_t>(sms) * (tc ? 3 : 8);
+    // mma.sync: as for decode, the largest power of two (256..4096) that
+    // still gives about six waves of three CTAs per SM when every sequence is
+    // as long as the bound (q_len 1 / 2 on the GQA workload: 1024-token
+    // splits, 0.92 / 0.89 of HBM, against 0.90 / 0.87 at 2048).  tcgen05
+    // (persistent, longest units first): the largest power of two up to the
+    // longest split (1024 blocks) that still gives three units per SM (larger
+    // units cost less per token: one setup, fewer partials)
+    const int64_t want = static_cast<int64_t>(sms) * (tc ? 3 : 18);
     st = tc ? static_cast<int32_t>(max_st) : 4096;
     while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
   }
