@@ -54,6 +54,8 @@ def run_cascade(case):
     (7, 48, (1, 50), 4, 2, 64, 16),        # prefix not a multiple of the 64-token tile
     (2, 512, (1, 40), 16, 2, 128, 32),     # G = 16
     (33, 96, (1, 20), 6, 1, 64, 32),       # ragged row blocks (33 * 6 rows)
+    (64, 256, (1, 2000), 8, 2, 128, 16),   # long suffixes: the plan takes one prefix range
+    (16, 128, (1, 3000), 8, 1, 128, 16),   # two one-tile ranges beside long suffixes
 ])
 def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, bs):
     case = shared_case(B, prefix, suffix, G, H_kv, D, bs, seed=500 + B + prefix)
