@@ -151,6 +151,63 @@ def test_e4m3_quantisation_sweep(scale):
     assert np.all((got[nan] & 0x7F) == 0x7F)        # NaN stays NaN
 
 
+def _oracle_code_steps(scale):
+    """Where the oracle's quantiser (fp32 division by `scale`, then the
+    brute-force E4M3 encoder) changes code over the non-negative finite fp32
+    bit patterns 0 .. 0x7F800000 (+inf), in pattern order: (first pattern of
+    each new code, that code).  The composition is monotone in the pattern,
+    so one bisection per code finds its first pattern."""
+    enc = lambda u: F.e4m3_encode(F.f32_div(np.asarray(u, dtype=np.uint32).view(np.float32), np.float32(scale)))
+    codes = np.arange(1, 0x7F, dtype=np.int64)
+    lo = np.zeros(codes.size, dtype=np.int64)                  # enc(lo) < code
+    hi = np.full(codes.size, 0x7F800000, dtype=np.int64)       # enc(hi) >= code
+    assert np.all(enc(lo) < codes) and np.all(enc(hi) >= codes)
+    while np.any(hi - lo > 1):
+        mid = (lo + hi) // 2
+        up = enc(mid).astype(np.int64) >= codes
+        hi = np.where(up, mid, hi)
+        lo = np.where(up, lo, mid)
+    first = np.unique(hi)
+    return first, enc(first).astype(np.int64)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0123])
+def test_e4m3_quantisation_every_fp32_pattern(scale):
+    """All 2^32 fp32 bit patterns through the append kernel: the positive
+    half must step through the codes exactly where the oracle does, NaN
+    patterns stay NaN, and each negative pattern gives its magnitude's code
+    with the sign bit set."""
+    n_fin = 0x7F800001                          # +0 .. +inf
+    rows = (1 << 31) // 128
+    slots = torch.arange(rows, device=DEV, dtype=torch.int64)
+    sc = torch.full((1,), scale, dtype=torch.float32, device=DEV)
+    first, code = _oracle_code_steps(scale)
+    halves = []
+    for start in (0, -(1 << 31)):               # patterns 0x00000000.., then 0x80000000..
+        bits = torch.arange(start, start + (1 << 31), device=DEV, dtype=torch.int64).to(torch.int32)
+        x = bits.view(torch.float32).view(rows, 1, 128)
+        kc = torch.zeros((rows // 16, 1, 16, 128), dtype=torch.uint8, device=DEV)
+        vc = torch.zeros_like(kc)
+        pkv.append(x, x, slots, kc, vc, sc, sc)
+        torch.cuda.synchronize()
+        assert torch.equal(kc, vc)
+        del bits, x, vc
+        halves.append(kc.view(-1))
+    pos, neg = halves
+    # positive finite patterns: the steps of the code sequence
+    fin = pos[:n_fin]
+    assert int(fin[0]) == 0
+    at = (torch.nonzero(fin[1:] != fin[:-1]).view(-1) + 1)
+    got_first = at.cpu().numpy()
+    got_code = fin[at].cpu().numpy().astype(np.int64)
+    assert np.array_equal(got_first, first)
+    assert np.array_equal(got_code, code)
+    assert torch.all((pos[n_fin:] & 0x7F) == 0x7F)     # NaN patterns
+    # negative patterns: the magnitude's code with the sign bit
+    assert torch.equal(neg[:n_fin], fin | 0x80)
+    assert torch.all((neg[n_fin:] & 0x7F) == 0x7F)
+
+
 # ------------------------------------------------------------------ decode
 
 
