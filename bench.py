@@ -670,8 +670,11 @@ def run_op(args, local_rank):
                        "peak": hbm, "unit": "GB/s", "frac": sf_gbs / hbm,
                        "peak_source": f"{hbm_kind} (hbm_gbs, copy bandwidth)",
                        "algorithmic_bytes_per_launch": suffix_bytes, "avg_launch_ms": sf_ms, "traffic": None}
-        # the kernel that runs longest is the roofline line; the other rides along
-        dominant, other = (prefix_line, suffix_line) if pf_ms >= sf_ms else (suffix_line, prefix_line)
+        # the roofline line is the kernel that holds more SM time (its duration
+        # times the SMs it runs on: the prefix CTAs hold sm_share of them, the
+        # suffix decode the rest); the other rides along
+        pf_smt, sf_smt = pf_ms * sm_share, sf_ms * (1.0 - sm_share)
+        dominant, other = (prefix_line, suffix_line) if pf_smt > sf_smt else (suffix_line, prefix_line)
         line.update({"metric": "cascade decode KV GB/s (logical bytes: every sequence's whole context)",
                      "value": logical / ms / 1e6, "unit": "GB/s", "ms_per_step": ms, "higher_is_better": True,
                      "dtype": "bf16", "unique_GBs": unique / ms / 1e6, "plain_decode_ms": ms_plain,

@@ -212,11 +212,12 @@ pkv_status check_cache(const pkv_cache_desc* c) {
   return PKV_OK;
 }
 
-int32_t auto_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int32_t sms) {
-  // Largest power-of-two chunk (256..4096 tokens) that still gives about six
-  // waves of three CTAs per SM when every sequence is as long as the bound.
+int32_t auto_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int32_t sms, int32_t waves = 6) {
+  // Largest power-of-two chunk (256..4096 tokens) that still gives about
+  // `waves` waves of three CTAs per SM when every sequence is as long as the
+  // bound.
   const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
-  const int64_t want = static_cast<int64_t>(sms) * 3 * 6;
+  const int64_t want = static_cast<int64_t>(sms) * 3 * waves;
   int32_t st = 4096;
   while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
   return st;
@@ -744,8 +745,6 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
   if (max_ctx < prefix_len) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d < prefix_len %d", max_ctx, prefix_len);
   if (sms <= 0) sms = kDefaultSms;
   const int32_t suffix = max_ctx - prefix_len;
-  const int32_t st = auto_split_tokens(batch, c->num_kv_heads, suffix > 0 ? suffix : 1, sms);
-  const int64_t splits = suffix > 0 ? ceil_div(suffix, st) : 1;
   // Prefix ranges.  The prefix kernel runs one CTA (256 rows x one range)
   // per SM and the suffix decode runs beside it on the other SMs, so the
   // number of ranges n is the one that minimises the longer of (a) the
@@ -754,7 +753,8 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
   // prefix-tile units: on GB300 a 64-key tile of a 256-row CTA took about as
   // long as one SM streams 92 KB of suffix K/V (2.2 us at 42 KB/us).  Fewer
   // ranges on ties (fewer pieces to combine).  On the 128-sequence workload
-  // this picks 2 ranges (call 83.6 us; 4 ranges 93.1 us).
+  // this picks 2 ranges (with 256-token suffix splits the call took 83.6 us,
+  // against 93.1 with 4 ranges).
   const int64_t rows = static_cast<int64_t>(batch) * (num_q_heads / c->num_kv_heads);
   const int64_t row_blocks = ceil_div(rows, pkv::kCascadeRowsTc) * c->num_kv_heads;
   const int64_t tiles = ceil_div(prefix_len, pkv::kCascadeTile);
@@ -776,6 +776,18 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
   const int64_t max_pst = 1024LL * c->block_size / pkv::kCascadeTile * pkv::kCascadeTile;
   if (pst > max_pst) pst = max_pst;
   nps = ceil_div(prefix_len, pst);
+  // Suffix splits, sized for the SMs the prefix CTAs leave free and for two
+  // waves of three CTAs per SM there rather than six: the suffix decode
+  // streams beside the prefix, which covers its tail, and on short suffixes
+  // each CTA's fixed cost (setup, pipeline fill, partial write) weighs on
+  // every split.  On the 128-sequence workload (suffixes up to 1024 tokens)
+  // this leaves each suffix whole: call 73.4 us, against 76.0 with 512-token
+  // splits and 83.6 with the 256 of the six-wave rule over all SMs.
+  const int64_t prefix_ctas = row_blocks * nps;
+  const int32_t free_sms = static_cast<int32_t>(
+      prefix_ctas < sms - sms / 4 ? sms - prefix_ctas : sms / 4 > 0 ? sms / 4 : 1);
+  const int32_t st = auto_split_tokens(batch, c->num_kv_heads, suffix > 0 ? suffix : 1, free_sms, 2);
+  const int64_t splits = suffix > 0 ? ceil_div(suffix, st) : 1;
   *out = pkv_decode_plan_t{};
   out->mode = 2;
   out->split_tokens = st;
