@@ -226,6 +226,30 @@ def test_cascade_plan_shapes(lib):
     assert st2 == L.PKV_OK and p2.workers > p.workers
 
 
+def test_cascade_suffix_splits_sized_for_the_free_sms(lib):
+    """The suffix decode runs beside the prefix CTAs (one per SM): its split
+    length is the largest power of two (256..4096) that still gives two waves
+    of three CTAs per SM on the SMs the prefix leaves free, if every suffix
+    were as long as the longest."""
+    d = _desc(block_size=32)
+
+    def want(batch, max_suffix, free):
+        st = 4096
+        while st > 256 and batch * 8 * -(-max_suffix // st) < free * 3 * 2:
+            st //= 2
+        return st
+
+    for batch, max_ctx in [(128, 4096 + 1025), (32, 4096 + 1025), (8, 4096 + 131072), (256, 4096 + 64)]:
+        st, p = _cplan(lib, d, batch, 64, 4096, max_ctx)
+        assert st == L.PKV_OK, lib.pkv_last_error()
+        prefix_ctas = -(-batch * 8 // 256) * 8 * p.workers
+        free = 152 - prefix_ctas if prefix_ctas < 152 - 38 else 38
+        assert p.split_tokens == want(batch, max_ctx - 4096, free), (batch, p.split_tokens, p.workers)
+    # the shared-prefix workload: two prefix ranges, each suffix whole
+    st, p = _cplan(lib, d, 128, 64, 4096, 4096 + 1025)
+    assert p.workers == 2 and p.max_splits == 1
+
+
 @pytest.mark.parametrize("desc_kw,prefix,max_ctx,code", [
     (dict(block_size=32), 48, 100, L.PKV_ERR_INVALID_ARG),     # not whole blocks
     (dict(block_size=16), 0, 100, L.PKV_ERR_INVALID_ARG),
