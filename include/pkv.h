@@ -24,7 +24,7 @@
  *   - Work is enqueued on `stream` and the call returns without synchronising.
  *   - Arguments are checked on the host before anything is launched; a bad
  *     argument returns PKV_ERR_INVALID_ARG (or PKV_ERR_UNSUPPORTED for a
- *     shape this build has no kernel for) and enqueues nothing.  A CUDA
+ *     shape the library has no kernel for) and enqueues nothing.  A CUDA
  *     runtime failure returns PKV_ERR_CUDA.  pkv_last_error() gives a message.
  *   - Values that only the device can see (block ids, slots, lengths) are
  *     checked in the kernels: an out-of-range value is skipped (reads as zero,
