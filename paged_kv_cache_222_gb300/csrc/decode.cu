@@ -596,6 +596,77 @@ __global__ void __launch_bounds__(128) combine_rows_kernel(const DecodeParams p)
 }
 
 // ----------------------------------------------------------------------------
+// LSE combine of a cascade call (at most R = 4 or 8 slots per row: the row's
+// suffix splits, then the shared-prefix pieces).  Every slot is written but
+// suffix splits past a row's own count, so the loads go out before the
+// context length arrives and the unwritten slots (which may hold anything)
+// are dropped by selection afterwards.  One warp per (sequence, query head);
+// each lane owns D/32 consecutive dims; with 4 slots sixteen CTAs fit an SM.
+// ----------------------------------------------------------------------------
+template <int D, int R>
+__global__ void __launch_bounds__(128, R <= 4 ? 16 : 1) combine_cascade_kernel(const DecodeParams p) {
+  constexpr int V = D / 32;
+  wait_prior_grid();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= static_cast<int64_t>(p.batch) * p.num_q_heads) return;
+  const int b = static_cast<int>(row / p.num_q_heads);
+  const int S_max = p.slots_per_row;
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + row * S_max * 2);
+  const float* wo = p.ws_o + row * S_max * D + lane * V;
+  float2 mlr[R];
+  float x[R][V];
+#pragma unroll
+  for (int s = 0; s < R; ++s) {
+    mlr[s] = make_float2(-CUDART_INF_F, 0.f);
+#pragma unroll
+    for (int v = 0; v < V; ++v) x[s][v] = 0.f;
+    if (s < S_max) {
+      mlr[s] = ml[s];
+      if constexpr (V == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<int64_t>(s) * D);
+        x[s][0] = t.x; x[s][1] = t.y; x[s][2] = t.z; x[s][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<int64_t>(s) * D);
+        x[s][0] = t.x; x[s][1] = t.y;
+      }
+    }
+  }
+  const int ctx = clamp_ctx(p, p.context_lens[b]);
+  const int cs = ctx > p.token_offset ? ctx - p.token_offset : 0;
+  const int nsplit = (cs + p.split_tokens - 1) / p.split_tokens;
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int s = 0; s < R; ++s) {
+    // a split of the row, or a shared-prefix piece
+    const bool holds = s < nsplit || (s >= p.extra_slot && s < p.extra_slot + p.extra_count);
+    if (!holds) {
+      mlr[s] = make_float2(-CUDART_INF_F, 0.f);
+#pragma unroll
+      for (int v = 0; v < V; ++v) x[s][v] = 0.f;
+    }
+    M = fmaxf(M, mlr[s].x);
+  }
+  float L = 0.f, acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+#pragma unroll
+  for (int s = 0; s < R; ++s) {
+    const float w = (mlr[s].x == -CUDART_INF_F) ? 0.f : fast_exp2(mlr[s].x - M);
+    L += w * mlr[s].y;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] += w * x[s][v];
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;  // a row with nothing to attend gives zeros
+  float* dst = p.out + row * D + lane * V;
+  if constexpr (V == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+  } else {
+    *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // LSE combine of the fixed-split kernel's partials:
 //   out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
 // One CTA (4 warps) per (sequence, query head).  Warp w takes splits w, w+4,
@@ -1146,6 +1217,16 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
                : launch_pdl(streamk_fixup_kernel<64, 1>, dim3(units), dim3(128), 0, stream, p);
   }
   if (p.max_splits + p.extra_count <= 1 && !p.force_partial) return cudaSuccess;
+  if (p.force_partial && p.slots_per_row <= 8) {
+    // a cascade call: every slot written but suffix splits past a row's count
+    const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
+    const bool d128 = p.head_dim == 128;
+    if (p.slots_per_row <= 4)
+      return d128 ? launch_pdl(combine_cascade_kernel<128, 4>, dim3(blocks), dim3(128), 0, stream, p)
+                  : launch_pdl(combine_cascade_kernel<64, 4>, dim3(blocks), dim3(128), 0, stream, p);
+    return d128 ? launch_pdl(combine_cascade_kernel<128, 8>, dim3(blocks), dim3(128), 0, stream, p)
+                : launch_pdl(combine_cascade_kernel<64, 8>, dim3(blocks), dim3(128), 0, stream, p);
+  }
   if (p.max_splits + p.extra_count <= 8) {
     const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
     if (p.head_dim == 128) return launch_pdl(combine_rows_kernel<128>, dim3(blocks), dim3(128), 0, stream, p);

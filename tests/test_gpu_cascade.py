@@ -69,6 +69,39 @@ def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, 
     assert torch.max(torch.abs(out_c - out_p)) < 1e-4
 
 
+@pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs", [
+    (12, 128, (1, 200), 8, 2, 128, 16),    # one suffix split per sequence
+    (9, 64, (1, 700), 4, 2, 64, 16),       # several suffix splits
+])
+def test_cascade_sequences_that_attend_only_the_prefix(B, prefix, suffix, G, H_kv, D, bs):
+    """Every third sequence attends exactly the shared prefix (no private
+    token): its suffix slots are never written, and the workspace is filled
+    with NaN first, so a combine that read them would show it."""
+    from oracle import paged_attention as PA
+    case = shared_case(B, prefix, suffix, G, H_kv, D, bs, seed=900 + B + D)
+    S.poison_unused(case)
+    bt = case["block_tables"].to(DEV)
+    lens = case["ctx"].clone().to(torch.int32)
+    lens[::3] = prefix
+    mx = int(lens.max())
+    q = case["q"][0].contiguous()
+    pblocks = bt[0, : prefix // bs].contiguous()
+    plan = pkv.cascade_plan(B, G * H_kv, case["k_cache"], prefix, mx)
+    ws = torch.full((int(plan.workspace_bytes),), 0xFF, dtype=torch.uint8, device=DEV)
+    out_c = pkv.cascade_decode_attention(q, case["k_cache"], case["v_cache"], pblocks, prefix, bt,
+                                         lens.to(DEV), case["scale"], mx, workspace=ws)
+    got = out_c.cpu().numpy()
+    lens_h = lens.numpy()
+    for b in range(B):
+        n = case["blocks_needed"][b]
+        for h in range(H_kv):
+            k, v = S.snapshot_sequence(case, b, h)
+            want = PA.decode_attention(S.bits16(q[b, h * G:(h + 1) * G])[None], k, v, PA.BF16,
+                                       np.arange(n, dtype=np.int32)[None, :], lens_h[b:b + 1],
+                                       case["scale"])[0]
+            assert np.max(np.abs(got[b, h * G:(h + 1) * G] - want)) <= 2e-3, (b, h, int(lens_h[b]))
+
+
 def test_cascade_full_size_shared_prefix_workload():
     case = W.make_case("shared_prefix", device=DEV)
     units = [(0, 0), (77, 5), (127, 7)]
