@@ -56,6 +56,8 @@ def run_cascade(case):
     (33, 96, (1, 20), 6, 1, 64, 32),       # ragged row blocks (33 * 6 rows)
     (64, 256, (1, 2000), 8, 2, 128, 16),   # long suffixes: the plan takes one prefix range
     (16, 128, (1, 3000), 8, 1, 128, 16),   # two one-tile ranges beside long suffixes
+    (4, 256, (1, 1000), 8, 2, 128, 16),    # 8 slots per row: 4 suffix splits + 4 prefix ranges
+    (8, 192, (1, 900), 8, 2, 64, 16),      # 5-8 slots per row, D = 64
 ])
 def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, bs):
     case = shared_case(B, prefix, suffix, G, H_kv, D, bs, seed=500 + B + prefix)
@@ -72,6 +74,7 @@ def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, 
 @pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs", [
     (12, 128, (1, 200), 8, 2, 128, 16),    # one suffix split per sequence
     (9, 64, (1, 700), 4, 2, 64, 16),       # several suffix splits
+    (8, 192, (1, 900), 8, 2, 128, 16),     # 7 slots per row
 ])
 def test_cascade_sequences_that_attend_only_the_prefix(B, prefix, suffix, G, H_kv, D, bs):
     """Every third sequence attends exactly the shared prefix (no private
