@@ -71,13 +71,14 @@ def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, 
     assert torch.max(torch.abs(out_c - out_p)) < 1e-4
 
 
-@pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs", [
-    (12, 128, (1, 200), 8, 2, 128, 16),    # one suffix split per sequence
-    (9, 64, (1, 700), 4, 2, 64, 16),       # several suffix splits
-    (8, 192, (1, 900), 8, 2, 128, 16),     # 7 slots per row
+@pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs,every", [
+    (12, 128, (1, 200), 8, 2, 128, 16, 3),    # one suffix split per sequence
+    (9, 64, (1, 700), 4, 2, 64, 16, 3),       # several suffix splits
+    (8, 192, (1, 900), 8, 2, 128, 16, 3),     # 7 slots per row
+    (6, 128, (1, 200), 8, 2, 128, 16, 1),     # no sequence has a private token
 ])
-def test_cascade_sequences_that_attend_only_the_prefix(B, prefix, suffix, G, H_kv, D, bs):
-    """Every third sequence attends exactly the shared prefix (no private
+def test_cascade_sequences_that_attend_only_the_prefix(B, prefix, suffix, G, H_kv, D, bs, every):
+    """Every `every`-th sequence attends exactly the shared prefix (no private
     token): its suffix slots are never written, and the workspace is filled
     with NaN first, so a combine that read them would show it."""
     from oracle import paged_attention as PA
@@ -85,7 +86,7 @@ def test_cascade_sequences_that_attend_only_the_prefix(B, prefix, suffix, G, H_k
     S.poison_unused(case)
     bt = case["block_tables"].to(DEV)
     lens = case["ctx"].clone().to(torch.int32)
-    lens[::3] = prefix
+    lens[::every] = prefix
     mx = int(lens.max())
     q = case["q"][0].contiguous()
     pblocks = bt[0, : prefix // bs].contiguous()
