@@ -174,7 +174,9 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_s
         stride = scale_row_stride if scale_row_stride is not None else (
             desc.num_kv_heads if k_scale.dim() == 2 else 0)
     mb = block_tables.shape[1] if b > 0 else 1
-    plan = decode_plan(b, hq, desc, max_context_len, split_tokens)
+    # planned for this device's SMs, as the library plans the call itself
+    plan = decode_plan(b, hq, desc, max_context_len, split_tokens,
+                       torch.cuda.get_device_properties(dev).multi_processor_count)
     ws_bytes = int(plan.workspace_bytes)
     if ws_bytes > 0 and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -231,7 +233,9 @@ def cascade_decode_attention(q, k_cache, v_cache, prefix_blocks, prefix_len, blo
     b, hq, d = q.shape
     if out is None:
         out = torch.empty((b, hq, d), dtype=torch.float32, device=dev)
-    plan = cascade_plan(b, hq, desc, prefix_len, max_context_len)
+    # planned for this device's SMs, as the library plans the call itself
+    plan = cascade_plan(b, hq, desc, prefix_len, max_context_len,
+                        torch.cuda.get_device_properties(dev).multi_processor_count)
     if workspace is None:
         workspace = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dev)
     st = lib.pkv_cascade_decode_attention(
