@@ -257,7 +257,12 @@ pkv_status pkv_decode_attention_noalloc(const void* q, int32_t batch, int32_t nu
  *
  * pkv_cascade_plan (host only): mode 2; split_tokens / max_splits describe the
  * suffix splits, workers the number of prefix ranges and prefix_split_tokens
- * their length.
+ * their length.  The ranges are chosen to balance the prefix CTAs (one per
+ * SM) against the suffix decode beside them; the suffix splits are then sized
+ * for the SMs the prefix leaves free (about two waves of three CTAs per SM),
+ * so they are longer than a plain decode of the same batch would take.  The
+ * call plans again with the device's SM count and refuses a smaller
+ * workspace (PKV_ERR_WORKSPACE): plan with that count (num_sms), or 0 for 152.
  */
 pkv_status pkv_cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* cache,
                             int32_t prefix_len, int32_t max_context_len, int32_t num_sms,
