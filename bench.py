@@ -568,6 +568,13 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "gpu_launches": launches,
     }
+    if case.get("prefix", 0):
+        # sequences sharing their first blocks: those bytes counted once, each
+        # private suffix once (same time base as `value`)
+        esz = 1 if fp8 else 2
+        uniq = (case["prefix"] + float((case["ctx"].double() + 1 - case["prefix"]).sum())) * \
+            case["H_kv"] * case["D"] * 2 * esz
+        line["unique_GBs"] = value * uniq / kv_bytes
     if not args.no_cpu_baseline and world == 1:
         gbs, n, procs, wall, ref = oracle_throughput(case, args.cpu_seconds, return_outputs=True)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle",
