@@ -8,11 +8,13 @@
 // block between Tier-1 HBM and Tier-2 host memory).
 //
 // A block of one cache is num_kv_heads * block_size * head_dim elements,
-// contiguous.  The kernel walks the flat space of 16-byte words of all pairs
-// (K words, then V words, pair after pair) with a grid-stride loop over one
-// wave of resident CTAs; each thread issues four independent 16-byte loads
-// before its four stores, so a warp keeps 2 KB in flight.  Source and destination ids are range-checked;
-// a bad pair is skipped and recorded in the device error word.
+// contiguous.  The work is cut into chunks of 32 KB of one block (the K block
+// of a pair, then its V block, pair after pair), which one wave of resident
+// CTAs takes in a grid-stride loop: a CTA step reads the pair's ids once (the
+// next step's ids are loaded while this one copies), then each thread issues
+// eight independent 16-byte loads before its eight stores, so a warp keeps
+// 4 KB in flight.  Source and destination ids are range-checked; a bad pair
+// is skipped and recorded in the device error word.
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -21,7 +23,8 @@ namespace pkv {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kCopyUnroll = 4;
+constexpr int kCopyUnroll = 8;
+constexpr int64_t kChunkWords = kCopyThreads * kCopyUnroll;  // 16-byte words per CTA step (32 KB)
 
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyParams p) {
   // Start the next kernel's launch now (it waits for this grid before it
@@ -29,34 +32,45 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyPar
   // write a destination block.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t per_pair = 2 * p.block_vec;
-  const int64_t total = p.n_pairs * per_pair;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
-       base += kCopyUnroll * stride) {
-    uint4 v[kCopyUnroll];
-    uint4* dst[kCopyUnroll];
+  const int64_t per_block = (p.block_vec + kChunkWords - 1) / kChunkWords;  // chunks of one block
+  const int64_t total = p.n_pairs * 2 * per_block;
+  // ids of chunk c's pair
+  auto ids = [&](int64_t c, int64_t& s, int64_t& d) {
+    const int64_t pair = c / (2 * per_block);
+    s = p.src[pair];
+    d = p.dst[pair];
+  };
+  int64_t c = blockIdx.x;
+  int64_t s = 0, d = 0;
+  if (c < total) ids(c, s, d);
+  while (c < total) {
+    const int64_t c_next = c + gridDim.x;
+    int64_t s_next = 0, d_next = 0;
+    if (c_next < total) ids(c_next, s_next, d_next);  // in flight while this chunk copies
+    const int64_t pb = c / per_block;                 // (pair, cache): K of pair pb/2, or its V
+    const bool is_v = (pb & 1) != 0;
+    const int64_t w0 = (c - pb * per_block) * kChunkWords;
+    if (s < 0 || s >= p.src_blocks || d < 0 || d >= p.dst_blocks) {
+      if (w0 == 0 && !is_v && threadIdx.x == 0) record_error(p.err, kDevErrBlockId);
+    } else {
+      const uint4* src = static_cast<const uint4*>(is_v ? p.v_src : p.k_src) + s * p.block_vec + w0;
+      uint4* dst = static_cast<uint4*>(is_v ? p.v_dst : p.k_dst) + d * p.block_vec + w0;
+      const int64_t n = p.block_vec - w0 < kChunkWords ? p.block_vec - w0 : kChunkWords;
+      uint4 v[kCopyUnroll];
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u) {
-      dst[u] = nullptr;
-      const int64_t idx = base + u * stride;
-      if (idx >= total) continue;
-      const int64_t pair = idx / per_pair;
-      const int64_t r = idx - pair * per_pair;
-      const bool is_v = r >= p.block_vec;
-      const int64_t w = is_v ? r - p.block_vec : r;
-      const int64_t s = p.src[pair], d = p.dst[pair];
-      if (s < 0 || s >= p.src_blocks || d < 0 || d >= p.dst_blocks) {
-        if (w == 0 && !is_v) record_error(p.err, kDevErrBlockId);
-        continue;
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int i = threadIdx.x + u * kCopyThreads;
+        if (i < n) v[u] = src[i];
       }
-      const uint4* src = static_cast<const uint4*>(is_v ? p.v_src : p.k_src) + s * p.block_vec + w;
-      v[u] = *src;
-      dst[u] = static_cast<uint4*>(is_v ? p.v_dst : p.k_dst) + d * p.block_vec + w;
-    }
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u)
-      if (dst[u] != nullptr) *dst[u] = v[u];
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int i = threadIdx.x + u * kCopyThreads;
+        if (i < n) dst[i] = v[u];
+      }
+    }
+    c = c_next;
+    s = s_next;
+    d = d_next;
   }
 }
 
@@ -80,7 +94,7 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     resident[dev] = sms * (per_sm > 0 ? per_sm : 1);
   }
-  const int64_t want = (words + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
+  const int64_t want = p.n_pairs * 2 * ((p.block_vec + kChunkWords - 1) / kChunkWords);  // chunks
   int64_t cap = resident[dev];
   if (p.max_ctas > 0 && p.max_ctas < cap) cap = p.max_ctas;
   const int blocks = static_cast<int>(want < cap ? want : cap);
