@@ -11,9 +11,10 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
   names E4M3 with per-head scaling factors for KV blocks; the encoding itself
   is the OCP definition.
 
-Encoders here are deliberately brute force: they enumerate candidate codes
-and pick the nearest by exact float64 distance, so a reader can check them
-against the definition by eye.
+Encoders here pick the nearest code by exact float64 distance to decoded
+candidate codes, so a reader can check them against the definition by eye
+(the E4M3 one compares the two codes that bracket the value; an exhaustive
+twin compares all 127 and checks it).
 """
 
 import numpy as np
@@ -101,15 +102,41 @@ def e4m3_to_f64(codes):
     return E4M3_VALUES[np.asarray(codes).astype(np.uint8)]
 
 
-def e4m3_encode(y, chunk=1 << 16):
+def e4m3_encode(y):
     """Encode binary32 values to E4M3 with round-to-nearest-even, saturating.
 
-    Brute force: the distance from |y| to every one of the 127 non-negative
-    finite magnitudes is measured in float64 and the nearest code wins; on a
-    tie the even code (even last mantissa bit) wins.  Magnitudes at or beyond
-    448, infinities included, saturate to 448 (code 0x7E).  The sign is kept,
-    so a negative value that rounds to zero gives 0x80.  NaN gives 0x7F.
+    The nearest of the 127 non-negative finite magnitudes to |y| is taken,
+    distances measured exactly in float64; on a tie the code with an even last
+    mantissa bit wins.  Only the two magnitudes that bracket |y| can be
+    nearest (the magnitudes are sorted), so those two are compared.
+    Magnitudes at or beyond 448, infinities included, saturate to 448 (code
+    0x7E).  The sign is kept, so a negative value that rounds to zero gives
+    0x80.  NaN gives 0x7F.  ``e4m3_encode_exhaustive`` measures the distance to
+    every magnitude instead and gives the same codes.
     """
+    y = np.asarray(y, dtype=np.float32)
+    v = y.ravel()
+    neg = np.signbit(v)
+    a = np.abs(v.astype(np.float64))
+    top = _E4M3_POS_CODES.size - 1
+    hi = np.minimum(np.searchsorted(_E4M3_POS_VALUES, a, side="left"), top)   # first magnitude >= |y|
+    lo = np.maximum(hi - 1, 0)                                                  # the one below it
+    d_lo = np.abs(a - _E4M3_POS_VALUES[lo])
+    d_hi = np.abs(_E4M3_POS_VALUES[hi] - a)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((_E4M3_POS_CODES[hi] & 1) == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a >= E4M3_MAX, np.uint8(0x7E), code)                       # satfinite
+    code = code | (neg.astype(np.uint8) << np.uint8(7))
+    code = np.where(np.isnan(v), np.uint8(E4M3_NAN_CODE), code)
+    return code.reshape(y.shape)
+
+
+def e4m3_encode_exhaustive(y, chunk=1 << 16):
+    """Brute-force E4M3 encoder: the distance from |y| to every one of the 127
+    non-negative finite magnitudes is measured in float64 and the nearest code
+    wins; on a tie the even code wins.  Saturation, sign and NaN as
+    ``e4m3_encode``.  Slow (one row of 127 distances per value): it checks the
+    bracketing encoder on sweeps."""
     y = np.asarray(y, dtype=np.float32)
     flat = y.ravel()
     out = np.empty(flat.shape, dtype=np.uint8)

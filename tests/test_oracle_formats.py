@@ -86,26 +86,28 @@ def test_e4m3_encode_round_trip_all_codes():
     assert np.array_equal(F.e4m3_encode(vals), codes)
 
 
-def test_e4m3_encode_midpoints_tie_to_even():
+@pytest.mark.parametrize("enc_fn", [F.e4m3_encode, F.e4m3_encode_exhaustive])
+def test_e4m3_encode_midpoints_tie_to_even(enc_fn):
     pos = F.E4M3_VALUES[:0x7F]
     mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
     assert np.array_equal(mids.astype(np.float64), (pos[:-1] + pos[1:]) / 2)   # exact in fp32
-    enc = F.e4m3_encode(mids)
+    enc = enc_fn(mids)
     lower = np.arange(0x7E, dtype=np.uint8)
     expect = np.where(lower % 2 == 0, lower, lower + 1).astype(np.uint8)
     assert np.array_equal(enc, expect)
-    assert np.array_equal(F.e4m3_encode(-mids), expect | 0x80)
+    assert np.array_equal(enc_fn(-mids), expect | 0x80)
     # one fp32 ulp either side of a midpoint rounds to the nearer code
     up = np.nextafter(mids, np.float32(np.inf))
     dn = np.nextafter(mids, np.float32(0))
-    assert np.array_equal(F.e4m3_encode(up), lower + 1)
-    assert np.array_equal(F.e4m3_encode(dn), lower)
+    assert np.array_equal(enc_fn(up), lower + 1)
+    assert np.array_equal(enc_fn(dn), lower)
 
 
-def test_e4m3_encode_saturation_and_specials():
+@pytest.mark.parametrize("enc_fn", [F.e4m3_encode, F.e4m3_encode_exhaustive])
+def test_e4m3_encode_saturation_and_specials(enc_fn):
     x = np.array([448, 449, 464, 480, 1e6, np.inf, -np.inf, -1e30, np.nan, 0.0, -0.0,
                   2.0 ** -10, 2.0 ** -10 * 1.0000001, -(2.0 ** -11)], dtype=np.float32)
-    enc = F.e4m3_encode(x)
+    enc = enc_fn(x)
     assert list(enc[:8]) == [0x7E] * 6 + [0xFE, 0xFE]
     assert enc[8] == 0x7F
     assert enc[9] == 0x00 and enc[10] == 0x80
@@ -143,3 +145,29 @@ def test_f32_div_is_binary32():
 def test_e4m3_encode_decode_consistency(code):
     v = np.float32(F.E4M3_VALUES[code])
     assert F.e4m3_encode(np.array([v]))[0] == code
+
+
+def test_e4m3_bracketing_encoder_equals_exhaustive_encoder():
+    """The encoder that compares only the two magnitudes bracketing |y| gives
+    the code the all-127-magnitude brute force gives: random fp32 bit patterns
+    over every exponent, values within a few ulps of every code and of every
+    midpoint between neighbouring codes, both signs, zeros, infinities, NaN."""
+    rng = np.random.default_rng(20260502)
+    bits = rng.integers(0, 2 ** 32, 1_500_000, dtype=np.uint64).astype(np.uint32)
+    pos = F.E4M3_VALUES[:0x7F].astype(np.float32)
+    mids = ((F.E4M3_VALUES[:0x7E] + F.E4M3_VALUES[1:0x7F]) / 2).astype(np.float32)
+    near = []
+    for base in (pos, mids, np.float32([448.0, 464.0, 480.0])):
+        v = base.copy()
+        for _ in range(4):
+            v = np.nextafter(v, np.float32(np.inf))
+            near.append(v)
+        v = base.copy()
+        for _ in range(4):
+            v = np.nextafter(v, np.float32(0))
+            near.append(v)
+        near.append(base)
+    near = np.concatenate(near)
+    x = np.concatenate([bits.view(np.float32), near, -near,
+                        np.float32([0.0, -0.0, np.inf, -np.inf, np.nan, 1e38, -1e-45])])
+    assert np.array_equal(F.e4m3_encode(x), F.e4m3_encode_exhaustive(x))
