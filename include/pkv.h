@@ -112,6 +112,33 @@ pkv_status pkv_append(const void* k_new, const void* v_new, int32_t src_dtype,
                       int64_t scale_row_stride, pkv_stream_t stream);
 
 /*
+ * pkv_slot_mapping — the flat cache slot of each new token, from the block
+ * tables: token i of sequence s at logical position pos goes to
+ *   block_tables[s, pos / block_size] * block_size + pos % block_size
+ * ([SC] "PagedAttention & Memory Management (vLLM)": logical block j of a
+ * sequence lives in the physical block its table names; [FN] "Paged KV-Cache
+ * with Radix Tree Prefix Cache": fixed-size blocks reached through a
+ * per-sequence table).  The result is pkv_append's slot_mapping.
+ *
+ *   block_tables   int32 [num_seqs, max_blocks_per_seq] (device).
+ *   seq_index      int64 [n_tokens] (device): the sequence of token i, or NULL
+ *                  when token i belongs to sequence i (one new token per
+ *                  sequence; then n_tokens <= num_seqs).
+ *   positions      int64 [n_tokens] (device): logical position of token i; a
+ *                  negative position is padding and gives slot -1.
+ *   cache          the cache the slots address (block size; num_blocks bounds
+ *                  the table entries).
+ *   slot_mapping   int64 [n_tokens] (device), written.
+ * A sequence index outside [0, num_seqs) or a position at or beyond
+ * max_blocks_per_seq * block_size records PKV_DEVERR_CONTEXT_LEN; a table
+ * entry outside [0, num_blocks) records PKV_DEVERR_BLOCK_ID; either gives
+ * slot -1 (which pkv_append skips).  n_tokens == 0 is a no-op.
+ */
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                            const int64_t* seq_index, const int64_t* positions, int64_t n_tokens,
+                            const pkv_cache_desc* cache, int64_t* slot_mapping, pkv_stream_t stream);
+
+/*
  * pkv_decode_attention — single-token decode attention over a paged cache
  * ([SC] "Why We Need the Key-Value (KV) Cache" and step 4 "Decode Phase";
  * [UI] "High-Throughput Paged Attention Kernel Integration" for the argument
@@ -211,7 +238,10 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
  * (every GPU that loads the library holds it until the process exits).  A call
  * whose plan needs more scratch than that (see pkv_decode_plan with
  * split_tokens 0) returns PKV_ERR_WORKSPACE without launching anything.  The
- * call makes no cudaMalloc, cudaFree or other allocating call.
+ * call makes no cudaMalloc, cudaFree or other allocating call.  (With the
+ * kernel timing trace switched on by pkv_trace_enable, which is off by
+ * default, every library launch also records two CUDA events taken from a
+ * host-side event pool; no device memory is allocated for them either.)
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
@@ -219,6 +249,8 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
  * call's contents (nothing in it needs to start at zero): calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race on
  * it and give wrong results.  Serialise them, or use pkv_decode_attention_ex.
+ * A caller that resets the device (cudaDeviceReset) calls pkv_shutdown first;
+ * the next call then looks the array's address up again.
  */
 pkv_status pkv_decode_attention_noalloc(const void* q, int32_t batch, int32_t num_q_heads,
                                         const void* k_cache, const void* v_cache,
@@ -370,7 +402,7 @@ int32_t pkv_abi_version(void);
  * pkv_trace_read synchronises those events and returns, per kernel kind,
  * the number of launches and their summed device time; it then clears the
  * buffer.  Kinds: 0 append, 1 decode split, 2 combine, 3 cascade prefix,
- * 4 block copy, 5 multi-token query.
+ * 4 block copy, 5 multi-token query, 6 slot mapping.
  */
 typedef struct {
   int32_t kind;
@@ -381,7 +413,13 @@ typedef struct {
 pkv_status pkv_trace_enable(int32_t on);
 int32_t pkv_trace_read(pkv_trace_entry* entries, int32_t capacity);
 
-/* Frees library-owned device memory (workspace pools, trace events). */
+/*
+ * Frees library-owned device memory and objects (workspace pools, the side
+ * streams of the cascade call, trace events) and forgets every per-device
+ * address and launch limit looked up so far, so that the next call sets them
+ * up again.  Call it before a cudaDeviceReset if the library is used after
+ * the reset.  No call of the library may run concurrently with it.
+ */
 pkv_status pkv_shutdown(void);
 
 #ifdef __cplusplus

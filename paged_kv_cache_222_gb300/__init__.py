@@ -22,14 +22,14 @@ from . import _lib
 from ._lib import (PKV_BF16, PKV_E4M3, PKV_F32, CacheDesc, DecodePlan, PkvError,  # noqa: F401
                    TraceEntry)
 
-__all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slots_for_positions",
+__all__ = ["append", "decode_attention", "decode_plan", "cache_desc", "slot_mapping",
            "cascade_plan", "cascade_decode_attention", "multi_query_plan", "multi_query_attention",
            "BlockManager", "OutOfBlocks", "copy_blocks",
            "host_pool_like", "copy_blocks_between",
            "device_error", "trace_enable", "trace_read", "library", "PkvError"]
 
 KERNEL_KINDS = {0: "append", 1: "decode_split", 2: "combine", 3: "cascade_prefix", 4: "block_copy",
-                5: "multi_query"}
+                5: "multi_query", 6: "slot_mapping"}
 
 
 def library():
@@ -141,8 +141,9 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_s
 
     q [B, H_q, D] bf16; block_tables [B, MB] int32; context_lens [B] int32
     (tokens attended, the appended one included); returns out [B, H_q, D]
-    float32.  `max_context_len` is a host bound on context_lens (if None it is
-    read from the device, which synchronises).  E4M3 caches take k_scale /
+    float32.  `max_context_len` is a host bound on context_lens (if None, the
+    block tables' capacity MB * block_size, which plans more splits than a
+    tighter bound).  E4M3 caches take k_scale /
     v_scale float32 [B, H_kv] (or [H_kv] for one scale per head).
     """
     lib = library()
@@ -158,7 +159,7 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_s
     if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
         raise ValueError("block_tables must be [B, MB] and context_lens [B]")
     if max_context_len is None:
-        max_context_len = int(context_lens.max().item()) if b > 0 else 0
+        max_context_len = block_tables.shape[1] * desc.block_size if b > 0 else 0
     if out is None:
         out = torch.empty((b, hq, d), dtype=torch.float32, device=dev)
     else:
@@ -289,15 +290,34 @@ def multi_query_attention(q, k_cache, v_cache, block_tables, context_lens, scale
     return out
 
 
-def slots_for_positions(block_tables, seq_index, positions, block_size):
-    """Flat cache slots of logical token `positions` of sequences `seq_index`:
-    block_tables[s, p // block_size] * block_size + p % block_size (int64).
-    The block manager's addressing rule, computed with tensor ops on the
-    tables' device."""
-    seq_index = seq_index.to(block_tables.device, torch.int64)
-    positions = positions.to(block_tables.device, torch.int64)
-    phys = block_tables.to(torch.int64)[seq_index, positions // block_size]
-    return phys * block_size + positions % block_size
+def slot_mapping(block_tables, positions, k_cache, seq_index=None, out=None):
+    """Flat cache slots (int64, on the cache's device) of new tokens at logical
+    `positions` (int64; < 0 = padding, slot -1) of sequences `seq_index`
+    (int64, or None: token i belongs to sequence i), computed by the library's
+    kernel from `block_tables` (int32 [num_seqs, MB]); the slot_mapping that
+    `append` takes."""
+    dev = k_cache.device
+    desc = cache_desc(k_cache)
+    _contig(block_tables, torch.int32, "block_tables", dev)
+    _contig(positions, torch.int64, "positions", dev)
+    if block_tables.dim() != 2 or positions.dim() != 1:
+        raise ValueError("block_tables must be [num_seqs, MB] and positions 1-D")
+    n = positions.numel()
+    if seq_index is not None:
+        _contig(seq_index, torch.int64, "seq_index", dev)
+        if seq_index.shape != positions.shape:
+            raise ValueError("seq_index and positions differ in shape")
+    if out is None:
+        out = torch.empty(n, dtype=torch.int64, device=dev)
+    else:
+        _contig(out, torch.int64, "out", dev)
+        if out.numel() != n:
+            raise ValueError("out must have one entry per position")
+    with torch.cuda.device(dev):
+        _lib.check(library().pkv_slot_mapping(
+            _ptr(block_tables), block_tables.shape[0], max(1, block_tables.shape[1]), _ptr(seq_index),
+            _ptr(positions), n, ctypes.byref(desc), _ptr(out), _stream(dev)), "pkv_slot_mapping")
+    return out
 
 
 def device_error(device=None):

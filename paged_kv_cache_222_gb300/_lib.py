@@ -49,6 +49,7 @@ _F = ctypes.c_float
 
 SIGNATURES = {
     "pkv_append": (_I32, [_P, _P, _I32, _I64, _P, _P, _P, ctypes.POINTER(CacheDesc), _P, _P, _I64, _P]),
+    "pkv_slot_mapping": (_I32, [_P, _I32, _I32, _P, _P, _I64, ctypes.POINTER(CacheDesc), _P, _P]),
     "pkv_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32, _P,
                                     _I32, _F, _P, _P, _P, _I64, _P]),
     "pkv_decode_plan": (_I32, [_I32, _I32, ctypes.POINTER(CacheDesc), _I32, _I32, _I32,

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -31,6 +32,12 @@ thread_local std::string t_last_error;
 }  // namespace
 
 void pkv::set_last_error(const char* msg) { t_last_error = msg; }
+
+namespace {
+std::atomic<int> g_config_epoch{1};
+}  // namespace
+
+int pkv::config_epoch() { return g_config_epoch.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -69,6 +76,9 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+// Device address of the no-allocation entry point's scratch array, looked up
+// once per device (under g_mu); cleared by pkv_shutdown.
+void* g_noalloc_ptr[kMaxDevices] = {};
 std::mutex g_fork_mu;  // one fork / join on the side streams at a time
 
 // The device's side stream and events, made on first use.
@@ -468,6 +478,44 @@ pkv_status pkv_append(const void* k_new, const void* v_new, int32_t src_dtype, i
   return PKV_OK;
 }
 
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                            const int64_t* seq_index, const int64_t* positions, int64_t n_tokens,
+                            const pkv_cache_desc* cache, int64_t* slot_mapping, pkv_stream_t stream) {
+  pkv_status s = check_cache(cache);
+  if (s != PKV_OK) return s;
+  if (n_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "n_tokens %lld", static_cast<long long>(n_tokens));
+  if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", num_seqs);
+  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+  if (n_tokens == 0) return PKV_OK;
+  if (positions == nullptr || slot_mapping == nullptr || (num_seqs > 0 && block_tables == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (seq_index == nullptr && n_tokens > num_seqs)
+    return fail(PKV_ERR_INVALID_ARG, "without seq_index token i is sequence i: n_tokens %lld > num_seqs %d",
+                static_cast<long long>(n_tokens), num_seqs);
+  if (!aligned(positions, 8) || !aligned(slot_mapping, 8) || (seq_index != nullptr && !aligned(seq_index, 8)) ||
+      !aligned(block_tables, 4))
+    return fail(PKV_ERR_INVALID_ARG, "positions, seq_index, slot_mapping must be 8-byte aligned, tables 4");
+  int dev;
+  DeviceState* st;
+  s = current_device(&dev, &st);
+  if (s != PKV_OK) return s;
+  pkv::SlotParams p = {};
+  p.block_tables = block_tables;
+  p.seq_index = seq_index;
+  p.positions = positions;
+  p.slots = slot_mapping;
+  p.n = n_tokens;
+  p.num_blocks = cache->num_blocks;
+  p.num_seqs = num_seqs;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = cache->block_size;
+  p.err = st->err;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(pkv::kKindSlotMapping, cs, [&] { return pkv::launch_slot_mapping(p, cs); });
+  if (e != cudaSuccess) return cuda_fail(e, "slot mapping launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
                            const int32_t* src_blocks, const int32_t* dst_blocks, int32_t n_pairs,
                            pkv_stream_t stream) {
@@ -707,7 +755,15 @@ pkv_status pkv_shutdown(void) {
     g_trace.clear();
   }
   std::lock_guard<std::mutex> lk(g_mu);
+  // Addresses and limits looked up in the current context are forgotten, so
+  // that a device reset after this call leaves nothing stale: the next call
+  // looks up the error word and the scratch array again and sets the kernels'
+  // shared-memory limits again.
+  g_config_epoch.fetch_add(1, std::memory_order_relaxed);
+  for (auto& p : g_noalloc_ptr) p = nullptr;
   for (auto& s : g_dev) {
+    s.ready = false;
+    s.err = nullptr;
     if (s.pool != nullptr) {
       cudaMemPoolDestroy(s.pool);
       s.pool = nullptr;
@@ -1089,12 +1145,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
 // Once per device, with that device current: the device address of the array.
 pkv_status noalloc_scratch(int dev, void** ptr) {
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  std::lock_guard<std::mutex> lk(g_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);

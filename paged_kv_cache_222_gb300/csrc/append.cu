@@ -11,6 +11,11 @@
 // warp moves 2 (D=128) or 4 (D=64) whole rows with 16-byte (bf16) or 8-byte
 // (E4M3) stores; loads are 16-byte (bf16 source) or 2x16-byte (f32 source).
 // Grid-stride, so any number of rows fits a bounded grid.
+//
+// The slot-mapping kernel turns (sequence, logical position) pairs into those
+// flat slots through the block tables ([SC] "PagedAttention & Memory
+// Management (vLLM)": logical block j of a sequence lives in the physical
+// block its table names).
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -111,7 +116,52 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   }
 }
 
+// Slot of each new token: the block table's entry for the token's logical
+// block, times the block size, plus its offset in the block.  One thread per
+// token; a negative position is padding (slot -1, nothing recorded).
+__global__ void __launch_bounds__(256) slot_mapping_kernel(SlotParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += stride) {
+    const int64_t pos = p.positions[i];
+    int64_t slot = -1;
+    if (pos >= 0) {
+      const int64_t seq = p.seq_index != nullptr ? p.seq_index[i] : i;
+      if (seq < 0 || seq >= p.num_seqs || pos >= cap) {
+        record_error(p.err, kDevErrContextLen);
+      } else {
+        const int64_t j = pos / p.block_size;
+        const int32_t blk = p.block_tables[seq * p.max_blocks + j];
+        if (blk < 0 || blk >= p.num_blocks)
+          record_error(p.err, kDevErrBlockId);
+        else
+          slot = static_cast<int64_t>(blk) * p.block_size + (pos - j * p.block_size);
+      }
+    }
+    p.slots[i] = slot;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_slot_mapping(const SlotParams& p, cudaStream_t stream) {
+  if (p.n == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (p.n + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 152 * 8 ? want : 152 * 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, slot_mapping_kernel, p);
+}
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int64_t work = p.n_tokens * p.num_kv_heads * (p.head_dim / 8);

@@ -1054,7 +1054,7 @@ cudaError_t launch_mq_tc_t(const DecodeParams& p, const CUtensorMap& tk, const C
                            cudaStream_t stream) {
   auto kern = mq_tc_kernel<D>;
   const int smem = mq_tc_smem_bytes<D>();
-  static bool configured[64] = {};
+  static int configured[64] = {};
   cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
   // plain launches: the order kernel writes the unit order and zeroes the
@@ -1070,7 +1070,7 @@ cudaError_t launch_cascade_t(const DecodeParams& p, const CUtensorMap& tk, const
   auto kern = cascade_prefix_kernel<D>;
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
   const int smem = CascadeShape<D>::BYTES > 120 * 1024 ? CascadeShape<D>::BYTES : 120 * 1024;
-  static bool configured[64] = {};
+  static int configured[64] = {};
   cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, grid, dim3(CascadeShape<D>::THREADS), smem, stream, tk, tv, p);

@@ -366,7 +366,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
 
   const int ctx_raw = p.context_lens[b];
   const int ctx = clamp_ctx(p, ctx_raw);
-  if (ctx != ctx_raw && split == 0 && h == 0 && threadIdx.x == 0)
+  // a cascade call's sequences must hold the whole shared prefix
+  // (token_offset); the prefix kernel attends it for every row
+  if ((ctx != ctx_raw || ctx_raw < p.token_offset) && split == 0 && h == 0 && threadIdx.x == 0)
     record_error(p.err, kDevErrContextLen);
   const int64_t row0 = static_cast<int64_t>(b) * p.num_q_heads + static_cast<int64_t>(h) * G;
 
@@ -1122,16 +1124,9 @@ cudaError_t launch_split_t(const DecodeParams& p, const CUtensorMap& tk, const C
                            cudaStream_t stream) {
   auto kern = decode_split_kernel<D, FP8, NT>;
   constexpr int smem = Smem<D, FP8, NT>::TOTAL;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static int configured[64] = {};
+  cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  static bool configured[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   return launch_pdl(kern, dim3(p.max_splits, p.num_kv_heads, p.batch), dim3(kDecodeWarps * 32),
                     smem, stream, tk, tv, p);
 }
@@ -1142,17 +1137,9 @@ cudaError_t launch_streamk_t(const DecodeParams& p, const CUtensorMap& tk, const
   using Shape = StreamKShape<D, FP8>;
   auto kern = decode_streamk_kernel<D, FP8, NT, Shape::NW, Shape::NS, Shape::MINB>;
   const int smem = streamk_smem_bytes_t<D, FP8>(p.batch);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static int configured[64] = {};
+  cudaError_t e = set_smem_once(kern, streamk_smem_bytes_t<D, FP8>(kMaxStreamKBatch), configured);
   if (e != cudaSuccess) return e;
-  static bool configured[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             streamk_smem_bytes_t<D, FP8>(kMaxStreamKBatch));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   const int ctas = p.workers / Shape::NW;
   return launch_pdl(kern, dim3(ctas), dim3(Shape::NW * 32), smem, stream, tk, tv, p);
 }

@@ -78,17 +78,20 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, int
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device.
+// Raise a kernel's dynamic shared-memory limit once per device (again after
+// pkv_shutdown, which starts a new configuration epoch: a caller may reset the
+// device after it, and a reset drops the limits set in the old context).
 template <class K>
-cudaError_t set_smem_once(K kern, int smem, bool (&configured)[64]) {
+cudaError_t set_smem_once(K kern, int smem, int (&configured)[64]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  const int epoch = config_epoch();
+  if (configured[dev] != epoch) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev] = epoch;
   }
   return cudaSuccess;
 }

@@ -355,7 +355,7 @@ cudaError_t launch_mq_t(const DecodeParams& p, const CUtensorMap& tk, const CUte
   auto kern = multi_query_kernel<D, TL>;
   const int stage = (kMultiQueryTile / kTileTokens) * 2 * kTileTokens * D * 2;
   const int smem = MqShape<TL>::NS * stage + 4 * MqShape<TL>::NS * 8 + kMultiQueryMaxSplitBlocks * 4 + 1024;
-  static bool configured[64] = {};
+  static int configured[64] = {};
   cudaError_t e = set_smem_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const int rows = p.q_len * p.group;

@@ -26,6 +26,7 @@ enum KernelKind {
   kKindCascadePrefix = 3,
   kKindBlockCopy = 4,
   kKindMultiQuery = 5,
+  kKindSlotMapping = 6,
   kNumKernelKinds = 8  // room for later kinds; the trace aggregates by kind
 };
 
@@ -53,6 +54,20 @@ struct AppendParams {
   int32_t head_dim;
   int32_t src_dtype;    // PKV_BF16 / PKV_F32
   int32_t cache_dtype;  // PKV_BF16 / PKV_E4M3
+  int* err;
+};
+
+// Flat cache slots of new tokens from the block tables.
+struct SlotParams {
+  const int32_t* block_tables;  // [num_seqs, max_blocks]
+  const int64_t* seq_index;     // [n] sequence of token i, or NULL: token i is sequence i
+  const int64_t* positions;     // [n] logical position of token i (< 0: padding)
+  int64_t* slots;               // [n] out: block * block_size + offset, -1 for padding
+  int64_t n;
+  int64_t num_blocks;
+  int32_t num_seqs;
+  int32_t max_blocks;
+  int32_t block_size;
   int* err;
 };
 
@@ -118,9 +133,14 @@ struct CopyParams {
 // Message returned by pkv_last_error() on this host thread.
 void set_last_error(const char* msg);
 
+// Configuration epoch (>= 1): pkv_shutdown starts a new one, after which every
+// per-device set-up the launchers cached (shared-memory limits) is made again.
+int config_epoch();
+
 // Launchers (return the launch's cudaError_t; nothing is synchronised).
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_slot_mapping(const SlotParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tmap_k,
                                 const CUtensorMap& tmap_v, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);

@@ -56,7 +56,7 @@ def fill_fp8_cache(case):
     seq = case["fill_seq"].to(dev)
     pos = case["fill_pos"].to(dev)
     bt = case["block_tables"].to(dev)
-    slots = pkv.slots_for_positions(bt, seq, pos, case["bs"])
+    slots = pkv.slot_mapping(bt, pos, case["k_cache"], seq_index=seq)
     ks = case["k_scale"][seq].contiguous()
     vs = case["v_scale"][seq].contiguous()
     pkv.append(case["fill_k"], case["fill_v"], slots, case["k_cache"], case["v_cache"], ks, vs)
@@ -70,7 +70,7 @@ def run_step(case, s, split_tokens=0, out=None):
     bt = case["block_tables"].to(dev)
     ctx = case["ctx"].to(dev)
     pos = ctx.to(torch.int64) + s
-    slots = pkv.slots_for_positions(bt, torch.arange(B, device=dev), pos, case["bs"])
+    slots = pkv.slot_mapping(bt, pos, case["k_cache"])
     fp8 = case["kv"] == "e4m3"
     pkv.append(case["k_new"][s].contiguous(), case["v_new"][s].contiguous(), slots,
                case["k_cache"], case["v_cache"],

@@ -193,19 +193,6 @@ def test_workspace_too_small_is_reported(lib):
     assert st in (L.PKV_ERR_WORKSPACE, L.PKV_ERR_CUDA)
 
 
-def test_slot_helper_matches_oracle_addressing():
-    import paged_kv_cache_222_gb300 as pkv
-    from oracle import paged_attention as PA
-    import workloads as W
-    case = W.make_case("tiny")
-    bt = case["block_tables"]
-    seq = torch.tensor([0, 0, 1, 1, 1])
-    pos = torch.tensor([0, 37, 5, 16, 100])
-    got = pkv.slots_for_positions(bt, seq, pos, case["bs"])
-    want = [PA.slot_of(bt[s].numpy(), int(p), case["bs"]) for s, p in zip(seq, pos)]
-    assert got.tolist() == want
-
-
 def _cplan(lib, desc, batch, hq, prefix, max_ctx, sms=152):
     p = L.DecodePlan()
     st = lib.pkv_cascade_plan(batch, hq, ctypes.byref(desc), prefix, max_ctx, sms, ctypes.byref(p))

@@ -34,7 +34,7 @@ def run_cascade(case):
     B, bs = case["B"], case["bs"]
     bt = case["block_tables"].to(dev)
     ctx = case["ctx"].to(dev)
-    slots = pkv.slots_for_positions(bt, torch.arange(B, device=dev), ctx.to(torch.int64), bs)
+    slots = pkv.slot_mapping(bt, ctx.to(torch.int64), case["k_cache"])
     pkv.append(case["k_new"][0].contiguous(), case["v_new"][0].contiguous(), slots, case["k_cache"],
                case["v_cache"])
     lens = (ctx + 1).to(torch.int32)
@@ -106,17 +106,43 @@ def test_cascade_sequences_that_attend_only_the_prefix(B, prefix, suffix, G, H_k
             assert np.max(np.abs(got[b, h * G:(h + 1) * G] - want)) <= 2e-3, (b, h, int(lens_h[b]))
 
 
-def test_cascade_full_size_shared_prefix_workload():
+def test_cascade_full_size_shared_prefix_workload_every_unit():
+    """B=128 sequences sharing 4096 tokens (128 blocks of 32) plus private
+    suffixes of U[64, 1024]: all 1024 (sequence, KV head) units against the
+    oracle's plain decode of each whole sequence, and against the plain
+    decode call."""
+    from tests import oracle_pool as OP
     case = W.make_case("shared_prefix", device=DEV)
-    units = [(0, 0), (77, 5), (127, 7)]
-    snaps = {u: S.snapshot_sequence(case, *u) for u in units}
+    src = OP.UnitSource(case)
     out_c, out_p = run_cascade(case)
     assert torch.max(torch.abs(out_c - out_p)) < 1e-4
     got = out_c.cpu().numpy()
-    G = case["H_q"] // case["H_kv"]
-    for (b, h) in units:
-        ref = S.oracle_unit(case, b, h, 0, snaps[(b, h)])
-        assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+    units = [(b, h) for b in range(case["B"]) for h in range(case["H_kv"])]
+    res = OP.run_units(src, units, 1, [0])
+    assert res["units"] == 1024
+    assert OP.max_abs_err(got, res["outputs"], case["H_q"] // case["H_kv"]) <= 2e-3
+
+
+def test_cascade_sequence_shorter_than_the_prefix_is_recorded():
+    """A cascade call's sequences must each hold the whole shared prefix: one
+    that is shorter is reported in the device error word (the prefix kernel
+    attends the prefix for every row); a correct call afterwards reports
+    nothing."""
+    case = shared_case(4, 128, (1, 100), 8, 2, 128, 16, seed=4242)
+    bt = case["block_tables"].to(DEV)
+    lens = (case["ctx"] + 1).to(torch.int32)
+    mx = int(lens.max())
+    pblocks = bt[0, :128 // 16].contiguous()
+    q = case["q"][0].contiguous()
+    short = lens.clone()
+    short[2] = 128 - 5
+    pkv.cascade_decode_attention(q, case["k_cache"], case["v_cache"], pblocks, 128, bt, short.to(DEV),
+                                 case["scale"], mx)
+    assert pkv.device_error(DEV) == 3
+    out = pkv.cascade_decode_attention(q, case["k_cache"], case["v_cache"], pblocks, 128, bt, lens.to(DEV),
+                                       case["scale"], mx)
+    assert pkv.device_error(DEV) == 0
+    assert torch.all(torch.isfinite(out))
 
 
 def test_cascade_sharp_softmax():

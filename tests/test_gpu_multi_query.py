@@ -118,23 +118,18 @@ def test_split_count_does_not_change_the_result():
 
 
 @pytest.mark.parametrize("q_len", [2, 4, 16])   # mma.sync; persistent tcgen05 (x2)
-def test_full_size_gqa_workload_sampled(q_len):
+def test_full_size_gqa_workload_every_unit(q_len):
     """B=64, H_q=64, H_kv=8, D=128, bs=16, contexts U[512, 8192]: the q_len
     new tokens of every sequence are appended by pkv.append, then attended
-    causally; 24 sampled (sequence, KV head) units are checked."""
+    causally; all 512 (sequence, KV head) units are checked against the
+    oracle (run on the host cores from the generator's inputs)."""
+    from tests import oracle_pool as OP
     case = W.make_case("gqa_bf16", device=DEV, steps=q_len)
-    B, bs, G = case["B"], case["bs"], case["H_q"] // case["H_kv"]
-    rng = np.random.default_rng(q_len)
-    units = [(int(b), int(h)) for b, h in zip(rng.integers(0, B, 24), rng.integers(0, case["H_kv"], 24))]
+    src = OP.UnitSource(case)
     bt = case["block_tables"].to(DEV)
-    snap = {}
-    for b, h in units:
-        n = case["blocks_needed"][b]
-        ids = case["block_tables"][b, :n].to(torch.int64).to(DEV)
-        snap[(b, h)] = (bits16(case["k_cache"][ids][:, h:h + 1]), bits16(case["v_cache"][ids][:, h:h + 1]))
     ctx = case["ctx"].to(DEV).to(torch.int64)
     for s in range(q_len):
-        slots = pkv.slots_for_positions(bt, torch.arange(B, device=DEV), ctx + s, bs)
+        slots = pkv.slot_mapping(bt, ctx + s, case["k_cache"])
         pkv.append(case["k_new"][s].contiguous(), case["v_new"][s].contiguous(), slots,
                    case["k_cache"], case["v_cache"])
     lens = (ctx + q_len).to(torch.int32)
@@ -143,19 +138,11 @@ def test_full_size_gqa_workload_sampled(q_len):
                                     max_context_len=int(lens.max()))
     assert pkv.device_error(DEV) == 0
     out = out.cpu().numpy()
-    for b, h in units:
-        n = case["blocks_needed"][b]
-        kc, vc = (a.copy() for a in snap[(b, h)])
-        table = np.arange(n, dtype=np.int32)[None, :]
-        c0 = int(case["ctx"][b])
-        for s in range(q_len):
-            slot = np.array([PA.slot_of(table[0], c0 + s, bs)])
-            kc, vc = PA.append(bits16(case["k_new"][s, b, h:h + 1])[None], bits16(case["v_new"][s, b, h:h + 1])[None],
-                               PA.BF16, slot, kc, vc, PA.BF16)
-        qq = bits16(q[b:b + 1, :, h * G:(h + 1) * G])
-        want = PA.multi_query_attention(qq, kc, vc, PA.BF16, table, np.array([c0 + q_len]), case["scale"])
-        got = out[b, :, h * G:(h + 1) * G]
-        assert np.abs(got - want[0]).max() <= 2e-3, (b, h)
+    assert np.isfinite(out).all()
+    units = [(b, h) for b in range(case["B"]) for h in range(case["H_kv"])]
+    res = OP.run_units(src, units, q_len, list(range(q_len)))
+    assert res["units"] == 512
+    assert OP.max_abs_err(out, res["outputs"], case["H_q"] // case["H_kv"], multi=True) <= 2e-3
 
 
 @pytest.mark.parametrize("q_len,H_q,H_kv", [(8, 16, 1), (16, 8, 1)])

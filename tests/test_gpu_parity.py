@@ -16,6 +16,7 @@ import workloads as W
 from oracle import formats as F
 from oracle import paged_attention as PA
 from tests import gpu_support as S
+from tests import oracle_pool as OP
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -279,7 +280,8 @@ def test_balanced_split_with_empty_sequences_between_others():
     dev = DEV
     bt = case["block_tables"].to(dev)
     lens = torch.tensor([0, 0, 3001, 0, 18, 0], dtype=torch.int32, device=dev)
-    slots = pkv.slots_for_positions(bt, torch.tensor([2, 4], device=dev), torch.tensor([3000, 17], device=dev), 16)
+    slots = pkv.slot_mapping(bt, torch.tensor([3000, 17], device=dev), case["k_cache"],
+                             seq_index=torch.tensor([2, 4], device=dev))
     pkv.append(case["k_new"][0][[2, 4]].contiguous(), case["v_new"][0][[2, 4]].contiguous(), slots,
                case["k_cache"], case["v_cache"])
     out = pkv.decode_attention(case["q"][0], case["k_cache"], case["v_cache"], bt, lens, case["scale"],
@@ -399,61 +401,107 @@ def test_device_error_word_reports_bad_values_without_faulting():
 
 
 # ------------------------------------------------------------ full-size workloads
-
-def _sample_units(case, n, seed):
-    rng = np.random.default_rng(seed)
-    bs = rng.choice(case["B"], size=n, replace=False)
-    return [(int(b), int(rng.integers(case["H_kv"]))) for b in bs]
+# Every (sequence, KV head) unit of each workload is compared with the oracle,
+# which runs on the host cores in a spawn pool (tests/oracle_pool.py) from the
+# generator's inputs taken before the GPU touched the caches.
 
 
-@pytest.mark.parametrize("name", ["gqa_bf16", "shared_prefix"])
-def test_full_size_bf16_workloads_sampled(name):
+def _all_units(case):
+    return [(b, h) for b in range(case["B"]) for h in range(case["H_kv"])]
+
+
+@pytest.mark.parametrize("name,units", [("gqa_bf16", 512), ("shared_prefix", 1024)])
+def test_full_size_bf16_workloads_every_unit(name, units):
     case = W.make_case(name, device=DEV)
-    units = _sample_units(case, 4, 1) + [(int(np.argmax(case["ctx"].numpy())), 0)]
-    snaps = snaps_for(case, units)
+    src = OP.UnitSource(case)
     out = S.run_step(case, 0).cpu().numpy()
-    G = case["H_q"] // case["H_kv"]
-    for b, h in units:
-        ref = S.oracle_unit(case, b, h, 0, snaps[(b, h)])
-        assert np.max(np.abs(out[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+    assert pkv.device_error(DEV) == 0
     assert np.all(np.isfinite(out))
-    assert pkv.device_error(DEV) == 0
+    res = OP.run_units(src, _all_units(case), 1, [0])
+    assert res["units"] == units
+    assert OP.max_abs_err(out, res["outputs"], case["H_q"] // case["H_kv"]) <= 2e-3
 
 
-def test_full_size_fp8_workload_fill_and_decode_sampled():
+def test_full_size_fp8_workload_fill_bit_exact_and_decode_every_unit():
+    """B=256, contexts U[2048, 4096], E4M3 cache written by pkv.append from
+    fp32 rows with per-(sequence, KV head) scales: every code the GPU wrote
+    (the fill and the step's new token, all 2048 units) equals the oracle's
+    encoding, and every unit's decode is within 5e-3 of the oracle on the
+    oracle's own cache."""
     case = W.make_case("fp8", device=DEV)
-    slots = S.fill_fp8_cache(case)
-    # bit-exact fill on sampled rows (every head), encoded by the oracle
-    rng = np.random.default_rng(2)
-    rows = rng.choice(case["fill_k"].shape[0], size=512, replace=False)
-    rows_t = torch.from_numpy(rows).to(DEV)
-    sl = slots[rows_t]
-    bs = case["bs"]
-    got_k = S.bytes8(case["k_cache"][sl // bs, :, sl % bs])           # [n, H, D]
-    seq = case["fill_seq"][rows].numpy()
-    ks = case["k_scale"].cpu().numpy()[seq]                            # [n, H]
-    want_k = PA.encode_rows(case["fill_k"][rows_t].cpu().numpy(), PA.F32, PA.E4M3, ks)
-    assert np.array_equal(got_k, want_k)
+    src = OP.UnitSource(case)
+    S.fill_fp8_cache(case)
     out = S.run_step(case, 0).cpu().numpy()
-    G = case["H_q"] // case["H_kv"]
-    for b, h in _sample_units(case, 3, 3):
-        ref = S.oracle_unit(case, b, h, 0)
-        assert np.max(np.abs(out[b, h * G:(h + 1) * G] - ref)) <= 5e-3
     assert pkv.device_error(DEV) == 0
+    res = OP.run_units(src, _all_units(case), 1, [0], want_codes=True)
+    assert res["units"] == 2048
+    assert OP.max_abs_err(out, res["outputs"], case["H_q"] // case["H_kv"]) <= 5e-3
+    bs, D, H = case["bs"], case["D"], case["H_kv"]
+    compared = 0
+    for b in range(case["B"]):
+        n = case["blocks_needed"][b]
+        tokens = int(case["ctx"][b]) + 1
+        ids = case["block_tables"][b, :n].to(torch.int64).to(DEV)
+        gk = S.bytes8(case["k_cache"][ids].permute(1, 0, 2, 3).reshape(H, n * bs, D)[:, :tokens])
+        gv = S.bytes8(case["v_cache"][ids].permute(1, 0, 2, 3).reshape(H, n * bs, D)[:, :tokens])
+        for h in range(H):
+            wk, wv = res["codes"][(b, h)]
+            assert np.array_equal(gk[h], wk) and np.array_equal(gv[h], wv), (b, h)
+            compared += 1
+    assert compared == 2048
 
 
-def test_full_size_long_context_steps_sampled():
+def test_full_size_long_context_steps_every_unit():
+    """B=8 sequences of 131,072 tokens, q drawn x4 (a sharp softmax), 32
+    append + decode steps with the context growing by one: all 64 units at
+    steps 0, 15 and 31."""
     case = W.make_case("long_ctx", device=DEV)
-    units = [(0, 0), (5, 7)]
-    snaps = snaps_for(case, units)
-    G = case["H_q"] // case["H_kv"]
+    src = OP.UnitSource(case)
     checked = {}
     for s in range(case["steps"]):
         out = S.run_step(case, s)
-        if s in (0, case["steps"] - 1):
+        if s in (0, 15, case["steps"] - 1):
             checked[s] = out.cpu().numpy()
-    for s, out in checked.items():
-        for b, h in units:
-            ref = S.oracle_unit(case, b, h, s, snaps[(b, h)])
-            assert np.max(np.abs(out[b, h * G:(h + 1) * G] - ref)) <= 2e-3
     assert pkv.device_error(DEV) == 0
+    G = case["H_q"] // case["H_kv"]
+    for s, got in checked.items():
+        res = OP.run_units(src, _all_units(case), s + 1, [s])
+        assert res["units"] == 64
+        assert OP.max_abs_err(got, res["outputs"], G) <= 2e-3, s
+
+
+# ------------------------------------------------------------ slot mapping
+
+
+def test_slot_mapping_matches_oracle_addressing():
+    """pkv_slot_mapping against the oracle's slot rule on random tables:
+    every valid (sequence, position) pair bit-exact, padding gives -1 with no
+    error, and a position past the table or a table entry outside the pool
+    gives -1 and its error code."""
+    g = torch.Generator().manual_seed(31337)
+    nb, nseq, mb = 500, 7, 20
+    for bs in (16, 32):
+        table = torch.randperm(nb, generator=g)[:nseq * mb].reshape(nseq, mb).to(torch.int32)
+        kc = torch.empty((nb, 1, bs, 64), dtype=torch.bfloat16, device=DEV)
+        n = 4000
+        seq = torch.randint(0, nseq, (n,), generator=g)
+        pos = torch.randint(0, mb * bs, (n,), generator=g)
+        pos[::97] = -1
+        got = pkv.slot_mapping(table.to(DEV), pos.to(DEV), kc, seq_index=seq.to(DEV)).cpu().tolist()
+        want = [PA.slot_of(table[s].numpy(), p, bs) if p >= 0 else -1 for s, p in zip(seq.tolist(), pos.tolist())]
+        assert got == want
+        pos1 = torch.randint(0, mb * bs, (nseq,), generator=g)
+        got1 = pkv.slot_mapping(table.to(DEV), pos1.to(DEV), kc).cpu().tolist()
+        assert got1 == [PA.slot_of(table[s].numpy(), int(pos1[s]), bs) for s in range(nseq)]
+        assert pkv.device_error(DEV) == 0
+    t = table.to(DEV)
+    got = pkv.slot_mapping(t, torch.tensor([mb * bs, 3], device=DEV), kc, seq_index=torch.tensor([0, 9], device=DEV))
+    assert got.cpu().tolist() == [-1, -1]
+    assert pkv.device_error(DEV) == 3
+    bad = table.clone()
+    bad[1, 0] = nb + 5
+    bad[2, 0] = -1
+    got = pkv.slot_mapping(bad.to(DEV), torch.tensor([3, 5], device=DEV), kc,
+                           seq_index=torch.tensor([1, 2], device=DEV))
+    assert got.cpu().tolist() == [-1, -1]
+    assert pkv.device_error(DEV) == 2

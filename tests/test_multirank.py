@@ -49,3 +49,24 @@ def test_single_process_reduction_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_throughput(2e9, 10, 1, 20.0) == pytest.approx(1000.0)
+
+
+def test_bench_gpus_2_launches_two_ranks_itself():
+    """`bench.py --gpus 2` run without a launcher starts two ranks itself
+    (torch.distributed.run on 127.0.0.1); the dry run swaps the GPU work for
+    a host loop, so the launch, the gloo barrier and the reductions run here
+    without a GPU.  Both ranks report, and n_gpus is the ranks that ran."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--dry-run",
+                        "--steps", "3", "--warmup", "1"], capture_output=True, text=True, timeout=240,
+                       env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["dry_run"] and line["n_gpus"] == 2 and line["ranks_reported"] == 2
+    assert len(line["rank_ms"]) == 2 and line["slowest_ms"] == max(line["rank_ms"])

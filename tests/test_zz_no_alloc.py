@@ -62,23 +62,41 @@ def test_noalloc_matches_caller_workspace_entry_point_on_two_calls(lib):
         ref = pkv.decode_attention(case["q"][0], case["k_cache"], case["v_cache"], bt, lens,
                                    case["scale"], max_context_len=max_len)
         out = torch.full_like(ref, float("nan"))
+        torch.cuda.synchronize()
+        free_before, _ = torch.cuda.mem_get_info(DEV)
         st = _noalloc(lib, case, bt, lens, max_len, out)
         assert st == L.PKV_OK, lib.pkv_last_error()
         torch.cuda.synchronize()
+        free_after, _ = torch.cuda.mem_get_info(DEV)
+        assert free_after == free_before                          # the call took no device memory
         assert torch.all(torch.isfinite(out))
         assert float((out - ref).abs().max()) <= TOL_BF16
     assert pkv.device_error(DEV) == 0
 
 
 def test_noalloc_refuses_more_scratch_than_it_has(lib):
+    """A decode whose split-KV plan needs more than the 32 MiB array is
+    refused before anything is launched.  The arguments are real device
+    buffers that a launch could read safely (a one-block cache, an all-zero
+    table, one token per sequence), so that if the refusal ever stopped
+    happening the call would still only touch valid memory and the test
+    would fail on the status, not on the GPU."""
     torch.cuda.set_device(DEV)
-    desc = L.CacheDesc(1 << 20, 16, 8, 128, L.PKV_BF16)
-    fake = ctypes.c_void_p(0x10000)           # never dereferenced: refused before any launch
-    plan = pkv.decode_plan(4000, 64, desc, 65536)          # above the balanced-split batch limit
+    B, H_q, H_kv, D, bs, mb = 4000, 64, 8, 128, 16, 4096
+    kc = torch.zeros((1, H_kv, bs, D), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    q = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device=DEV)
+    bt = torch.zeros((B, mb), dtype=torch.int32, device=DEV)
+    lens = torch.ones(B, dtype=torch.int32, device=DEV)
+    out = torch.empty((B, H_q, D), dtype=torch.float32, device=DEV)
+    desc = pkv.cache_desc(kc)
+    plan = pkv.decode_plan(B, H_q, desc, 65536)            # above the balanced-split batch limit
     assert plan.workspace_bytes > (32 << 20)
     stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
-    st = lib.pkv_decode_attention_noalloc(fake, 4000, 64, fake, fake, ctypes.byref(desc), fake, 4096,
-                                          fake, 65536, 0.088, fake, ctypes.c_void_p(0),
+    st = lib.pkv_decode_attention_noalloc(_p(q), B, H_q, _p(kc), _p(vc), ctypes.byref(desc), _p(bt), mb,
+                                          _p(lens), 65536, 0.088, _p(out), ctypes.c_void_p(0),
                                           ctypes.c_void_p(0), 0, stream)
     assert st == L.PKV_ERR_WORKSPACE
     assert b"no-allocation" in lib.pkv_last_error()
+    torch.cuda.synchronize()
+    assert pkv.device_error(DEV) == 0
