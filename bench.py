@@ -75,6 +75,9 @@ def parse_args(argv=None):
                     help="decode (the headline step) or one of the other hot-path operations")
     ap.add_argument("--q-len", type=int, default=4, help="new tokens per sequence for --op multi_query")
     ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="decode: run the workload with its first BATCH sequences only (0: all); "
+                         "for smaller profiler captures")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle (CPU baseline and parity)")
@@ -217,9 +220,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, algo_bytes=None):
     """DRAM bytes per launch of the split kernel from a committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+    if it was taken on the current kernel source; else None.  A capture of a
+    smaller batch of the same workload is scaled to `algo_bytes` by its ratio
+    of DRAM bytes to algorithmic K/V bytes (traffic grows with the bytes
+    attended)."""
     path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
     if not os.path.exists(path):
         return None
@@ -227,7 +233,10 @@ def recorded_traffic(workload):
         rec = json.load(f)
     for r in rec.get("records", []):
         if r.get("workload") == workload and r.get("kernel_src") == kernel_source_hash():
-            return r.get("dram_bytes_per_launch_full")
+            if r.get("dram_bytes_per_launch_full") is not None:
+                return r["dram_bytes_per_launch_full"]
+            if algo_bytes is not None and r.get("algorithmic_bytes"):
+                return (r["dram_read"] + r["dram_write"]) / r["algorithmic_bytes"] * algo_bytes
     return None
 
 
@@ -239,7 +248,7 @@ def hbm_roofline(kernel, algo_bytes, avg_ms, workload=None):
             "frac_vs_nominal": achieved / NOMINAL_HBM_GBS if achieved else None,
             "peak_source": f"{kind} (hbm_gbs, copy bandwidth); frac_vs_nominal against 8000 GB/s",
             "kernel": kernel, "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_ms": avg_ms,
-            "traffic": recorded_traffic(workload) if workload else None}
+            "traffic": recorded_traffic(workload, algo_bytes) if workload else None}
 
 
 # ---------------------------------------------------------------- decode steps
@@ -254,13 +263,17 @@ class DecodeRun:
     from the library's slot-mapping kernel, once for all steps, at set-up.
     """
 
-    def __init__(self, name, steps, device, seed_offset=0, split_tokens=0, parity=True):
+    def __init__(self, name, steps, device, seed_offset=0, split_tokens=0, parity=True, batch=0):
         import torch
         import paged_kv_cache_222_gb300 as pkv
         import workloads as W
         from tests import oracle_pool as OP
         self.pkv, self.torch, self.dev = pkv, torch, device
         spec = W.spec(name)
+        if 0 < batch < spec["B"]:
+            spec["B"] = batch
+            if "ctx" in spec:
+                spec["ctx"] = tuple(spec["ctx"][:batch])
         grows = spec.get("steps", 1) > 1
         spec["steps"] = steps if grows else 1
         spec["seed"] = spec["seed"] + seed_offset
@@ -637,7 +650,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
     cpu = not args.no_cpu_baseline and world == 1
     run = DecodeRun(args.workload, args.steps, dev, seed_offset=replica_seed(0, rank),
-                    split_tokens=args.split_tokens, parity=cpu)
+                    split_tokens=args.split_tokens, parity=cpu, batch=args.batch)
     m = measure_workload(run, args, dist, dev, world, rank, with_e2e=True)
     dtype = "e4m3" if run.fp8 else "bf16"
     cascade = cascade_on(run, args, dev) if run.case.get("prefix", 0) else None
