@@ -829,7 +829,8 @@ pkv_status cascade_plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc
     }
   }
   int64_t pst = ceil_div(ceil_div(prefix_len, nps), pkv::kCascadeTile) * pkv::kCascadeTile;
-  const int64_t max_pst = 1024LL * c->block_size / pkv::kCascadeTile * pkv::kCascadeTile;
+  const int64_t max_pst =
+      static_cast<int64_t>(pkv::kCascadeMaxRangeBlocks) * c->block_size / pkv::kCascadeTile * pkv::kCascadeTile;
   if (pst > max_pst) pst = max_pst;
   nps = ceil_div(prefix_len, pst);
   // Suffix splits, sized for the SMs the prefix CTAs leave free and for two

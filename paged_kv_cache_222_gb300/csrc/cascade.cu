@@ -90,23 +90,28 @@ struct TcTile {
 };
 
 // Cascade prefix CTA: two 128-row groups (their rows all read the same
-// prefix tiles), Q of both in shared memory, four K/V stages, and threads:
-// 4 softmax warps per group, two TMA producer warps, one MMA issuer per
-// group.  One CTA per SM with all 512 TMEM columns, 256 per group: O and a
-// double buffer of S that P overwrites in place.
+// prefix tiles), Q of both in shared memory, five K/V stages, and threads:
+// 4 softmax warps per group, two TMA producer warps, an S issuer and a P.V
+// issuer.  One CTA per SM with all 512 TMEM columns, 256 per group: O, S and
+// P in columns of their own, so that S(k+1) waits only for the softmax to
+// have read S(k), and P(k).V for the softmax to have written P(k).
 template <int D>
 struct CascadeShape : TcTile<D> {
   using T = TcTile<D>;
   static constexpr int GROUPS = 2;
   static constexpr int QBYTES = GROUPS * T::HALVES * T::QHALF;
-  static constexpr int NS = 4;
-  // full, empty; sfull, pfull, pfree x2 per group; done per group
-  static constexpr int NBARS = 2 * NS + 6 * GROUPS + GROUPS;
-  static constexpr int BYTES = QBYTES + NS * T::STAGE + NBARS * 8 + 16 + 1024 * 4 + 1024;
+  // the tiles come from L2, about 5000 cycles from issue to arrival while the
+  // suffix decode streams from HBM beside this kernel: five stages (the most
+  // that fit beside Q) keep four in flight while one is computed on
+  static constexpr int NS = 5;
+  // full, empty; sfull, sfree, pfull, pfree per group; done per issuer
+  static constexpr int NBARS = 2 * NS + 4 * GROUPS + 2;
+  static constexpr int BYTES = QBYTES + NS * T::STAGE + NBARS * 8 + 16 + kCascadeMaxRangeBlocks * 4 + 1024;
+  static_assert(BYTES <= 232448, "shared memory per CTA");
   // two producer warps issue a tile's boxes in parallel (one warp issuing a
   // tile's boxes was measured to hold an SM to about 12-19 bytes per cycle)
   static constexpr int NPROD = 2;
-  static constexpr int THREADS = 32 * (4 * GROUPS + NPROD + GROUPS);
+  static constexpr int THREADS = 32 * (4 * GROUPS + NPROD + 2);
 };
 
 // Rows (b, g) of KV head blockIdx.y, 256 per CTA (blockIdx.x), over prefix
@@ -119,15 +124,16 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
   using L = Layout<D, false>;
   using C = CascadeShape<D>;
   constexpr int M = C::M, NKEY = C::NKEY, NS = C::NS, GROUPS = C::GROUPS;
-  constexpr int kMaxBlocks = 1024;                    // block ids of one range, in shared memory
+  constexpr int kMaxBlocks = kCascadeMaxRangeBlocks;  // block ids of one range, in shared memory
   constexpr uint32_t GCOLS = 512 / GROUPS;            // TMEM columns of one group
-  // within a group's columns: O, then the S double buffer (P over S)
-  constexpr uint32_t COL_O = 0, COL_S = D, COL_P = D;
+  // within a group's columns: O, S (fp32, one column per key), P (bf16 hi
+  // then lo pairs, half a column per key each)
+  constexpr uint32_t COL_O = 0, COL_S = D, COL_P = D + NKEY;
   constexpr uint32_t IDESC_S = idesc_bf16(M, NKEY, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(M, D, true);
   constexpr int PRODUCER = 4 * GROUPS;                // first producer warp
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(COL_S + 2 * NKEY <= GCOLS, "TMEM columns");
+  static_assert(COL_P + NKEY <= GCOLS, "TMEM columns");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.group;
@@ -141,25 +147,28 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::QBYTES + NS * C::STAGE);
   uint64_t* full = bars;
   uint64_t* empty = full + NS;
-  uint64_t* sfull = empty + NS;       // [GROUPS][2]
-  uint64_t* pfull = sfull + 2 * GROUPS;
-  uint64_t* pfree = pfull + 2 * GROUPS;
-  uint64_t* done = pfree + 2 * GROUPS;  // [GROUPS]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + GROUPS);
+  uint64_t* sfull = empty + NS;       // [GROUPS]: S(k) is in TMEM
+  uint64_t* sfree = sfull + GROUPS;   // [GROUPS]: the softmax has read S(k)
+  uint64_t* pfull = sfree + GROUPS;   // [GROUPS]: P(k) is in TMEM
+  uint64_t* pfree = pfull + GROUPS;   // [GROUPS]: P(k).V has completed
+  uint64_t* done = pfree + GROUPS;    // [2]: the S and the P.V issuer's last MMAs
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 2);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_blk = reinterpret_cast<int*>(s_tmem + 4);
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(full + s), C::NPROD);
-      mbar_init(smem_u32(empty + s), GROUPS);
+      mbar_init(smem_u32(empty + s), 1);
     }
-    for (int i = 0; i < 2 * GROUPS; ++i) {
+    for (int i = 0; i < GROUPS; ++i) {
       mbar_init(smem_u32(sfull + i), 1);
+      mbar_init(smem_u32(sfree + i), 4);
       mbar_init(smem_u32(pfull + i), 4);
       mbar_init(smem_u32(pfree + i), 1);
     }
-    for (int i = 0; i < GROUPS; ++i) mbar_init(smem_u32(done + i), 1);
+    mbar_init(smem_u32(done), 1);
+    mbar_init(smem_u32(done + 1), 1);
     *s_abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_k);
@@ -170,8 +179,12 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     tmem_relinquish();
   }
   wait_prior_grid();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_tmem;
 
-  // ---- the CTA's rows, token range [t0, t1) and block list
+  // ---- the CTA's rows, token range [t0, t1) and tiles
   const int h = blockIdx.y;
   const int rows = p.batch * G;
   const int row0 = blockIdx.x * (GROUPS * M);
@@ -179,51 +192,33 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
   const int t1 = min(p.prefix_len, t0 + p.prefix_split_tokens);
   const int32_t* blocks = p.prefix_blocks;
   const int nblk = (t1 - t0 + p.block_size - 1) / p.block_size;
-  for (int i = tid; i < nblk && i < kMaxBlocks; i += blockDim.x) {
-    int phys = blocks[t0 / p.block_size + i];
-    if (phys < 0 || phys >= p.num_blocks) {
-      record_error(p.err, kDevErrBlockId);
-      phys = -1;
-    }
-    s_blk[i] = phys;
-  }
   const int ntile = (t1 - t0 + NKEY - 1) / NKEY;
   // k-th tile processed = tile (k + first) % ntile of the range: the CTAs of
   // one head start at different tiles (they all read the same prefix)
   const int first = ntile > 0 ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * ntile) / gridDim.x) : 0;
 
-  // ---- Q rows into shared memory: group g, row r, 16-byte chunk c of d-half
-  // hf at g * HALVES * QHALF + hf * QHALF + r * 128 + ((c ^ (r % 8)) * 16)
-  // (the 128-byte swizzle)
   const int grp = warp / 4;                            // softmax warps only
   const int r_in = (warp % 4) * 32 + lane;             // row within the group
   const int row = row0 + grp * M + r_in;
   const bool row_ok = warp < PRODUCER && row < rows;
   const int64_t orow = static_cast<int64_t>(row / G) * H_q + h * G + row % G;  // output row (b, hq)
-  if (warp < PRODUCER) {
-    const uint16_t* qr = row_ok ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
-    uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
-    uint4 w[D / 8];  // every load issued before the first store
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c)
-      w[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const int hf = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
-    }
-    fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *s_tmem;
-
+  // The producers start loading tiles at once; the softmax warps put Q into
+  // shared memory meanwhile and hand it to the S issuer at named barrier 2.
+  constexpr uint32_t kQBar = 2, kQThreads = 32 * (4 * GROUPS + 1);
   if (warp >= PRODUCER && warp < PRODUCER + C::NPROD) {
     // ------------------------------------------------------------ producers
     // A tile's TMA boxes (K then V; d-half; block) are split evenly over the
     // producer warps, one box per lane.
     const int pw = warp - PRODUCER;
+    for (int i = pw * 32 + lane; i < nblk && i < kMaxBlocks; i += 32 * C::NPROD) {
+      int phys = blocks[t0 / p.block_size + i];
+      if (phys < 0 || phys >= p.num_blocks) {
+        record_error(p.err, kDevErrBlockId);
+        phys = -1;
+      }
+      s_blk[i] = phys;
+    }
+    named_bar_sync(1, 32 * C::NPROD);
     const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
     const int per_half = NKEY / box;
     const int nbox = 2 * C::HALVES * per_half / C::NPROD;        // boxes of a tile per warp (<= 32)
@@ -257,46 +252,55 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
       for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
         mbar_wait(smem_u32(full + k % NS), static_cast<uint32_t>((k / NS) & 1), nullptr);
     }
-  } else if (warp >= PRODUCER + C::NPROD) {
-    // ------------------------------------------------------------ MMA issuers
-    // one per group: S(k) = Q K(k)^T, then O += P(k-1) V(k-1)
-    const int g = warp - PRODUCER - C::NPROD;
-    const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
-    const uint32_t tg = tbase + g * GCOLS;
-    for (int k = 0; k <= ntile; ++k) {
-      if (k < ntile) {
-        const int s = k % NS, b = k & 1;
-        bool ok = true;
-        if (lane == 0) {
-          ok = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
-          // buffer b: P(k-2).V has completed (P lives over S)
-          if (ok && k >= 2)
-            ok = wait_or_abort(smem_u32(pfree + 2 * g + b), static_cast<uint32_t>(((k - 2) >> 1) & 1), p.err,
-                               s_abort);
-        }
-        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
-        if (lane == 0) {
+  } else if (warp == PRODUCER + C::NPROD) {
+    // ------------------------------------------------------------ S issuer
+    // S_g(k) = Q_g K(k)^T for both groups, once the tile has arrived and the
+    // group's softmax has read S_g(k-1)
+    named_bar_sync(kQBar, kQThreads);                  // Q is in shared memory
+    for (int k = 0; k < ntile; ++k) {
+      const int s = k % NS;
+      bool ok = true;
+      if (lane == 0) ok = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((k / NS) & 1), p.err, s_abort);
+#pragma unroll
+      for (int g = 0; g < GROUPS; ++g) {
+        if (lane == 0 && ok && k >= 1)
+          ok = wait_or_abort(smem_u32(sfree + g), static_cast<uint32_t>((k - 1) & 1), p.err, s_abort);
+        if (lane == 0 && ok) {
           tc_fence_after();
+          const uint32_t qa = smem_u32(q_sm + g * C::HALVES * C::QHALF);
           const uint32_t kst = stage0 + s * C::STAGE;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(qa + (kk / 4) * C::QHALF + (kk % 4) * 32, 0, 1024);
             const uint64_t bd = smem_desc_sw128(kst + (kk / 4) * C::HALF_BYTES + (kk % 4) * 32, 0, 1024);
-            tc_mma_ss(tg + COL_S + b * NKEY, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+            tc_mma_ss(tbase + g * GCOLS + COL_S, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(sfull + 2 * g + b));
+          tc_commit(smem_u32(sfull + g));
         }
       }
-      if (k >= 1) {
-        const int j = k - 1, sj = j % NS, bj = j & 1;
-        bool ok = true;
-        if (lane == 0)
-          ok = wait_or_abort(smem_u32(pfull + 2 * g + bj), static_cast<uint32_t>((j >> 1) & 1), p.err, s_abort);
-        if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
-        if (lane == 0) {
+      if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0) {  // nothing of this thread's may still be running when TMEM is freed
+      tc_commit(smem_u32(done));
+      mbar_wait(smem_u32(done), 0u, nullptr);
+    }
+  } else if (warp == PRODUCER + C::NPROD + 1) {
+    // ------------------------------------------------------------ P.V issuer
+    // O_g += P_g(j) V(j) for both groups as each group's softmax hands over
+    // P_g(j); then the stage goes back to the producers.  Separate from the S
+    // issuer, so that a ready P.V never waits behind the next tile's arrival.
+    for (int j = 0; j < ntile; ++j) {
+      const int sj = j % NS;
+      bool ok = true;
+      if (lane == 0) ok = wait_or_abort(smem_u32(full + sj), static_cast<uint32_t>((j / NS) & 1), p.err, s_abort);
+#pragma unroll
+      for (int g = 0; g < GROUPS; ++g) {
+        if (lane == 0 && ok) ok = wait_or_abort(smem_u32(pfull + g), static_cast<uint32_t>(j & 1), p.err, s_abort);
+        if (lane == 0 && ok) {
           tc_fence_after();
+          const uint32_t tg = tbase + g * GCOLS;
           const uint32_t vst = stage0 + sj * C::STAGE + C::KREG;
-          const uint32_t pa = tg + COL_P + bj * NKEY;
+          const uint32_t pa = tg + COL_P;
 #pragma unroll
           for (int kk = 0; kk < NKEY / 16; ++kk) {
             // MN-major V: 8-key groups 1024 B apart, d-halves HALF_BYTES apart
@@ -304,36 +308,55 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
             tc_mma_ts(tg + COL_O, pa + kk * 8, vd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
             tc_mma_ts(tg + COL_O, pa + NKEY / 2 + kk * 8, vd, IDESC_PV, 1u);
           }
-          tc_commit(smem_u32(pfree + 2 * g + bj));
-          tc_commit(smem_u32(empty + sj));
+          tc_commit(smem_u32(pfree + g));
         }
       }
+      if (lane == 0 && ok) tc_commit(smem_u32(empty + sj));
+      if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
     }
-    if (lane == 0) {  // nothing of this thread's may still be running when TMEM is freed
-      tc_commit(smem_u32(done + g));
-      mbar_wait(smem_u32(done + g), 0u, nullptr);
+    if (lane == 0) {
+      tc_commit(smem_u32(done + 1));
+      mbar_wait(smem_u32(done + 1), 0u, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
+    {
+      // Q rows into shared memory: group g, row r, 16-byte chunk c of d-half
+      // hf at g * HALVES * QHALF + hf * QHALF + r * 128 + ((c ^ (r % 8)) * 16)
+      // (the 128-byte swizzle)
+      const uint16_t* qr = row_ok ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
+      uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
+      uint4 w[D / 8];  // every load issued before the first store
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        w[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const int hf = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
+      }
+      fence_proxy_async_smem();  // the tensor core reads Q through the async proxy
+      named_bar_sync(kQBar, kQThreads);
+    }
     const uint32_t tl = tbase + grp * GCOLS + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-    uint64_t* g_sfull = sfull + 2 * grp;
-    uint64_t* g_pfull = pfull + 2 * grp;
-    uint64_t* g_pfree = pfree + 2 * grp;
+    const uint32_t g_sfull = smem_u32(sfull + grp), g_sfree = smem_u32(sfree + grp);
+    const uint32_t g_pfull = smem_u32(pfull + grp), g_pfree = smem_u32(pfree + grp);
     const float qk_mult = p.qk_log2_scale;
     float m_used = -CUDART_INF_F, lsum = 0.f;
     bool ok = true;
     for (int k = 0; k < ntile && ok; ++k) {
-      const int b = k & 1;
-      ok = __all_sync(kFull, wait_or_abort(smem_u32(g_sfull + b), static_cast<uint32_t>((k >> 1) & 1), p.err,
-                                           s_abort));
+      ok = __all_sync(kFull, wait_or_abort(g_sfull, static_cast<uint32_t>(k & 1), p.err, s_abort));
       if (!ok) break;
       tc_fence_after();
       float x[NKEY];
       {
         uint32_t v[NKEY / 16][16];
 #pragma unroll
-        for (int c = 0; c < NKEY / 16; ++c) tmem_ld16(tl + COL_S + b * NKEY + 16 * c, v[c]);
+        for (int c = 0; c < NKEY / 16; ++c) tmem_ld16(tl + COL_S + 16 * c, v[c]);
         tmem_wait_ld();
+        tc_fence_before();  // S may be overwritten by S(k+1)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(g_sfree);
 #pragma unroll
         for (int c = 0; c < NKEY / 16; ++c)
 #pragma unroll
@@ -368,12 +391,15 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
         m_used = mt;
         resc = true;
       }
+      // P(k-1).V must have completed before O is rescaled (O then holds
+      // tiles 0..k-1) and before P(k) is written over P(k-1); the wait comes
+      // as late as possible, so that it overlaps this tile's exponentials
+      bool pv_done = k == 0;
       if (__any_sync(kFull, resc)) {
-        // O holds tiles 0..k-1 once P(k-1).V has completed
-        ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + ((k - 1) & 1)),
-                                             static_cast<uint32_t>(((k - 1) >> 1) & 1), p.err, s_abort));
+        ok = __all_sync(kFull, wait_or_abort(g_pfree, static_cast<uint32_t>((k - 1) & 1), p.err, s_abort));
         if (!ok) break;
         tc_fence_after();
+        pv_done = true;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t v[2][16];
@@ -393,54 +419,71 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
       const float2 neg_mu = make_float2(-mu, -mu);
       float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t hi[NKEY / 32][16], lo[NKEY / 32][16];
 #pragma unroll
-      for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
-        uint32_t hi[16], lo[16];
+      for (int c = 0; c < NKEY / 32; ++c)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 e = __fadd2_rn(make_float2(x[2 * (c0 + i)], x[2 * (c0 + i) + 1]), neg_mu);
+          const int j = 16 * c + i;                      // key pair j: keys 2j, 2j + 1
+          const float2 e = __fadd2_rn(make_float2(x[2 * j], x[2 * j + 1]), neg_mu);
           const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
           ls[i & 1] = __fadd2_rn(ls[i & 1], pp);
-          hi[i] = pack_bf16x2(pp.x, pp.y);
-          const float2 r = __fadd2_rn(pp, make_float2(-bf16lo_to_f32(hi[i]), -bf16hi_to_f32(hi[i])));
-          lo[i] = pack_bf16x2(r.x, r.y);
+          hi[c][i] = pack_bf16x2(pp.x, pp.y);
+          const float2 r = __fadd2_rn(pp, make_float2(-bf16lo_to_f32(hi[c][i]), -bf16hi_to_f32(hi[c][i])));
+          lo[c][i] = pack_bf16x2(r.x, r.y);
         }
-        tmem_st16(tl + COL_P + b * NKEY + c0, hi);
-        tmem_st16(tl + COL_P + b * NKEY + NKEY / 2 + c0, lo);
-      }
       lsum += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
+      if (!__all_sync(kFull, pv_done)) {
+        ok = __all_sync(kFull, wait_or_abort(g_pfree, static_cast<uint32_t>((k - 1) & 1), p.err, s_abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < NKEY / 32; ++c) {
+        tmem_st16(tl + COL_P + 16 * c, hi[c]);
+        tmem_st16(tl + COL_P + NKEY / 2 + 16 * c, lo[c]);
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(g_pfull + b));   // P(k) is in TMEM
+      if (lane == 0) mbar_arrive(g_pfull);   // P(k) is in TMEM
     }
     if (ok && ntile > 0)
-      ok = __all_sync(kFull, wait_or_abort(smem_u32(g_pfree + ((ntile - 1) & 1)),
-                                           static_cast<uint32_t>(((ntile - 1) >> 1) & 1), p.err, s_abort));
-    // ---- this row's (acc, m, l) piece of the prefix range
+      ok = __all_sync(kFull, wait_or_abort(g_pfree, static_cast<uint32_t>((ntile - 1) & 1), p.err, s_abort));
+    // ---- this row's (acc, m, l) piece of the prefix range.  O leaves through
+    // shared memory, the group's Q region (every S of the group has
+    // completed), one bulk copy per row and pass: 16-byte stores straight
+    // from the TMEM rows would scatter each warp instruction over 32 rows.
     const int64_t piece = orow * p.slots_per_row + p.extra_slot + blockIdx.z;
     if (ok && ntile > 0) {
       tc_fence_after();
+      constexpr int CP = C::HALVES * 32;                 // columns per pass (half a row)
+      uint8_t* srow = q_sm + grp * C::HALVES * C::QHALF + r_in * (CP * 4);
       float* dst_row = p.ws_o + piece * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[2][16];
-        tmem_ld16(tl + COL_O + c0, v[0]);
-        tmem_ld16(tl + COL_O + c0 + 16, v[1]);
-        tmem_wait_ld();
-        if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(dst_row + c0);
+      for (int c0 = 0; c0 < D; c0 += CP) {
+        if (c0 > 0) bulk_wait_read_all();                // the previous pass has left srow
+        uint32_t v[CP / 16][16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]), __uint_as_float(v[i / 4][4 * (i % 4) + 1]),
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 2]),
-                                 __uint_as_float(v[i / 4][4 * (i % 4) + 3]));
+        for (int c = 0; c < CP / 16; ++c) tmem_ld16(tl + COL_O + c0 + 16 * c, v[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < CP / 16; ++c)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(srow + (16 * c + 4 * i) * 4) =
+                make_uint4(v[c][4 * i], v[c][4 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3]);
+        fence_proxy_async_smem();
+        if (row_ok) {
+          bulk_store_s2g(dst_row + c0, smem_u32(srow), CP * 4);
+          bulk_commit();
         }
       }
       if (row_ok) {
         p.ws_ml[piece * 2] = m_used;
         p.ws_ml[piece * 2 + 1] = lsum;
       }
+      bulk_wait_read_all();  // the writes complete with the grid
     }
   }
   allow_next_grid();

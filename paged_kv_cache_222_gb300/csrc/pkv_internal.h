@@ -173,6 +173,9 @@ inline int multi_query_lanes(int rows) { return rows <= 16 ? 4 : (rows <= 32 ? 2
 constexpr int kCascadeRowsTc = 256;
 // Keys per cascade prefix tile (4 sub-tiles of kTileTokens).
 constexpr int kCascadeTile = 64;
+// Blocks of one cascade prefix range (their ids are staged in shared memory):
+// a range holds at most this many times the block size of tokens.
+constexpr int kCascadeMaxRangeBlocks = 256;
 
 // Dynamic shared memory the split kernel needs for (head_dim, dtype, groups).
 int decode_smem_bytes(int head_dim, int cache_dtype, int n_tiles8);
