@@ -560,12 +560,19 @@ __global__ void __launch_bounds__(128) wait_selftest_kernel(int which, uint64_t 
 // buffers keep their phases across units.  Every wait is bounded; a time-out
 // records the error and raises the CTA's abort flag, which ends every loop.
 // ----------------------------------------------------------------------------
-// Keys per tile and K/V stages of the persistent kernel: its tiles come from
-// HBM, where the bytes in flight set the speed, and Q in TMEM leaves it the
-// shared memory (192 KB of stages).  Twelve stages of 32-key tiles measured
-// 38 % slower than six of 64 (per-tile costs double).
+// Keys per tile and the depths of the persistent kernel's K and V rings: its
+// tiles come from HBM, where the bytes in flight set the speed, and Q in TMEM
+// leaves it the shared memory (192 KB of K and V tiles).  A K tile goes back
+// to its producer as soon as S has read it, a V tile after P.V; with rings
+// of their own the K tiles of later tiles arrive earlier and S is ready when
+// the softmax wants it (q_len 4: 4.69 -> 4.81 TB/s against one ring of six
+// K+V stages).  Measured on the GQA workload: 6 + 6 slots beat 4 + 8 and
+// 8 + 4 (-6 %), every other split of 12 or 13 slots (-11 %).  Twelve stages
+// of 32-key tiles measured 38 % slower than six of 64 (per-tile costs
+// double).
 constexpr int kMqTile = 64;
-constexpr int kMqStages = 6 * 64 / kMqTile;
+constexpr int kMqKStages = 6;
+constexpr int kMqVStages = 6;
 
 struct MqUnit {
   int b, h, row0, t0, t1, ctx, nsplit, split, ntile;
@@ -642,7 +649,7 @@ __global__ void __launch_bounds__(256, 1)
                  const DecodeParams p) {
   using L = Layout<D, false>;
   using C = TcTile<D, kMqTile>;
-  constexpr int M = 128, NKEY = C::NKEY, NS = kMqStages;
+  constexpr int M = 128, NKEY = C::NKEY, NK = kMqKStages, NV = kMqVStages;
   constexpr int R = 8;                                // unit ring slots
   constexpr int READERS = 7;                          // warps 0-3, 5, 6, 7
   constexpr uint32_t COL_O = 0, COL_S = D, COL_P = D + 2 * NKEY, COL_Q = COL_P + 2 * NKEY;
@@ -658,11 +665,14 @@ __global__ void __launch_bounds__(256, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t stage0 = smem_u32(smem);
-  int* s_ids = reinterpret_cast<int*>(smem + NS * C::STAGE);  // [2][1024] each producer's block ids
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_ids + 2 * kMultiQueryMaxSplitBlocks);  // [NS]
-  uint64_t* empty = full + NS;                        // [NS]
-  uint64_t* sfull = empty + NS;                       // [2]
+  const uint32_t kring = smem_u32(smem);             // [NK] K tiles
+  const uint32_t vring = kring + NK * C::KREG;        // [NV] V tiles
+  int* s_ids = reinterpret_cast<int*>(smem + (NK + NV) * C::KREG);  // [2][1024] each producer's block ids
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(s_ids + 2 * kMultiQueryMaxSplitBlocks);  // [NK]
+  uint64_t* kempty = kfull + NK;                      // [NK]
+  uint64_t* vfull = kempty + NK;                      // [NV]
+  uint64_t* vempty = vfull + NV;                      // [NV]
+  uint64_t* sfull = vempty + NV;                      // [2]
   uint64_t* sfree = sfull + 2;                        // [2]
   uint64_t* pfull = sfree + 2;                        // [2]
   uint64_t* pfree = pfull + 2;                        // [2]
@@ -675,9 +685,13 @@ __global__ void __launch_bounds__(256, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(full + s), 2);
-      mbar_init(smem_u32(empty + s), 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(smem_u32(kfull + s), 1);
+      mbar_init(smem_u32(kempty + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(smem_u32(vfull + s), 1);
+      mbar_init(smem_u32(vempty + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(sfull + i), 1);
@@ -711,7 +725,7 @@ __global__ void __launch_bounds__(256, 1)
     const int pw = warp - 4;
     const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
     const int per_half = NKEY / box;
-    const int nbox = C::HALVES * per_half;                       // boxes of a tile per warp
+    const int nbox = C::HALVES * per_half;                       // boxes of a K (or V) tile
     int g = 0;
     for (int n = 0;; ++n) {
       int u;
@@ -747,40 +761,45 @@ __global__ void __launch_bounds__(256, 1)
         ids[j] = phys;
       }
       __syncwarp();
-      // this lane's box of each tile: K or V, d-half, block within the tile
-      const int gi = pw * nbox + lane;
-      const int v = gi / (C::HALVES * per_half);
-      const int bx = (gi / per_half) % C::HALVES;
-      const int i = gi % per_half;
+      // this lane's box of each tile: d-half, block within the tile (warp 4
+      // loads the K ring, warp 5 the V ring)
+      const int bx = lane / per_half;
+      const int i = lane % per_half;
+      const int nring = pw == 0 ? NK : NV;
+      const uint32_t ring = pw == 0 ? kring : vring;
+      uint64_t* rfull = pw == 0 ? kfull : vfull;
+      uint64_t* rempty = pw == 0 ? kempty : vempty;
       bool ok = true;
       for (int k = 0; k < w.ntile; ++k, ++g) {
-        const int s = g % NS;
+        const int s = g % nring;
         bool go = true;
-        if (lane == 0 && g >= NS)
-          go = wait_or_abort(smem_u32(empty + s), static_cast<uint32_t>((g / NS - 1) & 1), p.err, s_abort);
+        if (lane == 0 && g >= nring)
+          go = wait_or_abort(smem_u32(rempty + s), static_cast<uint32_t>((g / nring - 1) & 1), p.err, s_abort);
         if (!__shfl_sync(kFull, go ? 1 : 0, 0)) {
           ok = false;
           break;
         }
-        const uint32_t dst = stage0 + s * C::STAGE;
-        const uint32_t bar = smem_u32(full + s);
+        const uint32_t dst = ring + s * C::KREG;
+        const uint32_t bar = smem_u32(rfull + s);
         if (lane == 0) {
           fence_proxy_async_smem();
-          mbar_arrive_expect_tx(bar, C::STAGE / 2);
+          mbar_arrive_expect_tx(bar, C::KREG);
         }
         __syncwarp();
         if (lane < nbox) {
           const int t = w.t0 + k * NKEY + i * box;
           const int phys = t < w.t1 ? ids[(t - w.t0) / p.block_size] : -1;  // past the range: zeros
-          const uint32_t off = v * C::KREG + bx * C::HALF_BYTES + i * box * 128;
-          tma_load_4d(dst + off, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, w.h, phys);
+          const uint32_t off = bx * C::HALF_BYTES + i * box * 128;
+          tma_load_4d(dst + off, pw ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, w.h, phys);
         }
       }
       if (!ok) break;
     }
     if (lane == 0 && *s_abort) {  // the copies in flight land before the stages are released
-      for (int k = g > NS ? g - NS : 0; k < g; ++k)
-        mbar_wait(smem_u32(full + k % NS), static_cast<uint32_t>((k / NS) & 1), nullptr);
+      const int nring = pw == 0 ? NK : NV;
+      uint64_t* rfull = pw == 0 ? kfull : vfull;
+      for (int k = g > nring ? g - nring : 0; k < g; ++k)
+        mbar_wait(smem_u32(rfull + k % nring), static_cast<uint32_t>((k / nring) & 1), nullptr);
     }
   } else if (warp == 6) {
     // ------------------------------------------------------------ S issuer
@@ -793,23 +812,24 @@ __global__ void __launch_bounds__(256, 1)
       if (lane == 0) ok = wait_or_abort(smem_u32(qready), static_cast<uint32_t>(n & 1), p.err, s_abort);
       ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
       for (int k = 0; k < w.ntile && ok; ++k, ++g) {
-        const int s = g % NS, b = g & 1;
+        const int s = g % NK, b = g & 1;
         bool ok2 = true;
         if (lane == 0) {
-          ok2 = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((g / NS) & 1), p.err, s_abort);
+          ok2 = wait_or_abort(smem_u32(kfull + s), static_cast<uint32_t>((g / NK) & 1), p.err, s_abort);
           if (ok2 && g >= 2)  // the softmax has read S(g-2) out of buffer b
             ok2 = wait_or_abort(smem_u32(sfree + b), static_cast<uint32_t>(((g - 2) >> 1) & 1), p.err, s_abort);
         }
         ok = __shfl_sync(kFull, ok2 ? 1 : 0, 0) != 0;
         if (ok && lane == 0) {
           tc_fence_after();
-          const uint32_t kst = stage0 + s * C::STAGE;
+          const uint32_t kst = kring + s * C::KREG;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t bd = smem_desc_sw128(kst + (kk / 4) * C::HALF_BYTES + (kk % 4) * 32, 0, 1024);
             tc_mma_ts(tbase + COL_S + b * NKEY, tbase + COL_Q + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(sfull + b));
+          tc_commit(smem_u32(kempty + s));  // S(g) has read the K tile
         }
       }
     }
@@ -826,21 +846,21 @@ __global__ void __launch_bounds__(256, 1)
       if (u < 0) break;
       const MqUnit w = mq_unit(p, u, nrb, false);
       for (int k = 0; k < w.ntile && ok; ++k, ++g) {
-        const int s = g % NS, b = g & 1;
+        const int s = g % NV, b = g & 1;
         bool ok2 = true;
         if (lane == 0) {
           ok2 = wait_or_abort(smem_u32(pfull + b), static_cast<uint32_t>((g >> 1) & 1), p.err, s_abort);
-          if (ok2)  // complete already (S read the stage); orders the V bytes before the zeroing below
-            ok2 = wait_or_abort(smem_u32(full + s), static_cast<uint32_t>((g / NS) & 1), p.err, s_abort);
+          if (ok2)  // the V tile has arrived (also orders its bytes before the zeroing below)
+            ok2 = wait_or_abort(smem_u32(vfull + s), static_cast<uint32_t>((g / NV) & 1), p.err, s_abort);
         }
         ok = __shfl_sync(kFull, ok2 ? 1 : 0, 0) != 0;
         if (!ok) break;
-        const uint32_t vst = stage0 + s * C::STAGE + C::KREG;
+        const uint32_t vst = vring + s * C::KREG;
         // rows of the last block past the sequence end may hold anything (NaN
         // included): zero them in the V tile, P is 0 there
         const int vr0 = w.ctx - (w.t0 + k * NKEY);
         if (vr0 < NKEY) {
-          uint8_t* vt = smem + (vst - stage0);
+          uint8_t* vt = smem + (vst - kring);
           const int first_row = vr0 > 0 ? vr0 : 0;
           const int chunks = (NKEY - first_row) * 8;   // 16-byte chunks per d-half
           for (int c = lane; c < C::HALVES * chunks; c += 32) {
@@ -862,7 +882,7 @@ __global__ void __launch_bounds__(256, 1)
             tc_mma_ts(tbase + COL_O, pa + NKEY / 2 + kk * 8, vd, IDESC_PV, 1u);
           }
           tc_commit(smem_u32(pfree + b));
-          tc_commit(smem_u32(empty + s));
+          tc_commit(smem_u32(vempty + s));
         }
       }
     }
@@ -1088,7 +1108,8 @@ __global__ void __launch_bounds__(256, 1)
 template <int D>
 int mq_tc_smem_bytes() {
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
-  const int need = kMqStages * TcTile<D, kMqTile>::STAGE + 2 * kMultiQueryMaxSplitBlocks * 4 + 128 * 8 + 1024 + 1024;
+  const int need = (kMqKStages + kMqVStages) * TcTile<D, kMqTile>::KREG + 2 * kMultiQueryMaxSplitBlocks * 4 +
+                   128 * 8 + 1024 + 1024;
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 
