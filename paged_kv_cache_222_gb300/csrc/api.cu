@@ -235,6 +235,24 @@ int32_t auto_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, 
 
 int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
+// Tokens per split of a plain decode call.  One split per (sequence, KV head)
+// when those alone give four waves of three CTAs per SM: every CTA then writes
+// its output rows directly and no combine runs (the FP8 workload, 2048 units:
+// the split kernel takes 248 us either way and the step goes from 259.6 to
+// 252.8 us).  Otherwise the six-wave power-of-two rule of auto_split_tokens,
+// with a last split shorter than an eighth of the others folded into them
+// (8193 tokens: eight splits of 1088 rather than eight of 1024 and one of 1).
+int32_t decode_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int32_t sms) {
+  const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
+  if (units >= static_cast<int64_t>(4) * 3 * sms)
+    return static_cast<int32_t>(max_ctx > 64 ? ceil_div(max_ctx, 64) * 64 : 64);
+  int32_t st = auto_split_tokens(batch, num_kv_heads, max_ctx, sms);
+  const int64_t n = ceil_div(max_ctx, st);
+  if (n >= 2 && max_ctx - (n - 1) * st < st / 8)
+    st = static_cast<int32_t>(ceil_div(ceil_div(max_ctx, n - 1), 64) * 64);
+  return st;
+}
+
 pkv_status plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int32_t max_ctx,
                 int32_t split_tokens, int32_t sms, pkv_decode_plan_t* out) {
   pkv_status s = check_cache(c);
@@ -266,7 +284,7 @@ pkv_status plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int
     return PKV_OK;
   }
   const int32_t st =
-      split_tokens > 0 ? split_tokens : auto_split_tokens(batch, c->num_kv_heads, max_ctx, sms);
+      split_tokens > 0 ? split_tokens : decode_split_tokens(batch, c->num_kv_heads, max_ctx, sms);
   const int64_t splits = max_ctx > 0 ? ceil_div(max_ctx, st) : 1;
   if (splits > 0x7FFFFFFFll) return fail(PKV_ERR_INVALID_ARG, "too many splits");
   out->mode = pkv::kModeFixedSplit;

@@ -143,15 +143,35 @@ def _plan(lib, desc, batch, hq, max_ctx, split=0, sms=152):
     return p
 
 
+def _auto_split(batch, hkv, max_ctx, sms=152):
+    """The automatic split length, restated: one split per (sequence, KV head)
+    when those give four waves of three CTAs per SM, else the largest power of
+    two (256..4096) giving six waves, with a last split shorter than an
+    eighth of the others folded into them."""
+    units = batch * hkv
+    if units >= 4 * 3 * sms:
+        return max(64, -(-max_ctx // 64) * 64)
+    st = 4096
+    while st > 256 and units * -(-max_ctx // st) < sms * 3 * 6:
+        st //= 2
+    n = -(-max_ctx // st)
+    if n >= 2 and max_ctx - (n - 1) * st < st // 8:
+        st = -(-(-(-max_ctx // (n - 1))) // 64) * 64
+    return st
+
+
 def test_fixed_split_plan_covers_the_context_and_sizes_the_workspace(lib):
     d = _desc()
     for batch, max_ctx, split in [(64, 8193, 1024), (256, 4097, 512), (8, 131104, 2048), (2, 101, 64),
-                                  (1, 1, 256), (3000, 4097, 0)]:
+                                  (1, 1, 256), (3000, 4097, 0), (64, 8193, 0), (256, 4097, 0),
+                                  (8, 131092, 0), (8, 131104, 0), (3, 4001, 0), (128, 5121, 0)]:
         p = _plan(lib, d, batch, 64, max_ctx, split=split)
         assert p.mode == 1 and p.workers == 0
-        assert p.split_tokens % 64 == 0 and 64 <= p.split_tokens <= 4096
+        assert p.split_tokens % 64 == 0 and p.split_tokens >= 64
         if split:
             assert p.split_tokens == split
+        else:
+            assert p.split_tokens == _auto_split(batch, 8, max_ctx), (batch, max_ctx, p.split_tokens)
         assert p.max_splits == -(-max_ctx // p.split_tokens)
         assert (p.max_splits - 1) * p.split_tokens < max_ctx <= p.max_splits * p.split_tokens
         rows = batch * 64 * p.max_splits
@@ -180,7 +200,16 @@ def test_balanced_plan_on_request_up_to_2048_sequences(lib):
 
 def test_fixed_split_auto_size_gives_enough_ctas_for_long_contexts(lib):
     p = _plan(lib, _desc(), 3000, 64, 4097)
-    assert p.mode == 1 and 3000 * 8 * p.max_splits >= 152 * 3 * 6
+    assert p.mode == 1 and 3000 * 8 * p.max_splits >= 152 * 3 * 4
+    # enough (sequence, KV head) units alone: one split, no scratch, no combine
+    assert p.max_splits == 1 and p.workspace_bytes == 0
+    p = _plan(lib, _desc(), 256, 64, 4097)                   # the FP8 workload's shape
+    assert p.max_splits == 1 and p.workspace_bytes == 0
+    # otherwise six waves, and no nearly empty last split
+    p = _plan(lib, _desc(), 64, 64, 8193)
+    assert 64 * 8 * p.max_splits >= 152 * 3 * 6 and p.max_splits == 8 and p.split_tokens == 1088
+    p = _plan(lib, _desc(), 8, 64, 131092)                   # the long-context workload at 20 steps
+    assert 8 * 8 * p.max_splits >= 152 * 3 * 6 and p.max_splits < -(-131092 // 2048)
 
 
 def test_workspace_too_small_is_reported(lib):
