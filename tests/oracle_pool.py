@@ -41,8 +41,10 @@ class UnitSource:
         self.tables = case["block_tables"].cpu()
         self.q = case["q"].cpu()                                  # [steps, B, H_q, D] bf16
         if self.kv == "bf16":
-            self.k_cache = case["k_cache"].cpu()
-            self.v_cache = case["v_cache"].cpu()
+            # head-major copies [H_kv, num_blocks, bs, D]: one head's blocks
+            # gather as contiguous rows
+            self.k_cache = case["k_cache"].cpu().transpose(0, 1).contiguous()
+            self.v_cache = case["v_cache"].cpu().transpose(0, 1).contiguous()
             self.k_new = case["k_new"].cpu()
             self.v_new = case["v_new"].cpu()
         else:
@@ -67,7 +69,10 @@ class UnitSource:
         q = _bits16(self.q[q_steps, b, g])                      # [len(q_steps), G, D]
         if self.kv == "bf16":
             ids = self.tables[b, :n].to(torch.int64)
-            raw = dict(k=_bits16(self.k_cache[ids][:, h:h + 1]), v=_bits16(self.v_cache[ids][:, h:h + 1]),
+            # only head h of the sequence's blocks: [n, 1, bs, D]
+            kb = torch.index_select(self.k_cache[h], 0, ids).unsqueeze(1)
+            vb = torch.index_select(self.v_cache[h], 0, ids).unsqueeze(1)
+            raw = dict(k=_bits16(kb), v=_bits16(vb),
                        k_new=_bits16(self.k_new[:n_new, b, h:h + 1]),
                        v_new=_bits16(self.v_new[:n_new, b, h:h + 1]))
         else:
