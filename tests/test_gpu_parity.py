@@ -505,3 +505,33 @@ def test_slot_mapping_matches_oracle_addressing():
                            seq_index=torch.tensor([1, 2], device=DEV))
     assert got.cpu().tolist() == [-1, -1]
     assert pkv.device_error(DEV) == 2
+
+
+# ------------------------------------------------------------ shutdown
+
+
+def test_calls_after_shutdown_set_the_library_up_again():
+    """pkv_shutdown frees the library's pool and side stream and forgets the
+    device addresses and kernel limits it looked up; the next calls set them
+    up again and give the same results (the pool path, the cascade call with
+    its side stream, a multi-token call with shared memory beyond the
+    default limit)."""
+    case = small_case(kv="bf16", D=128, G=8, H_kv=2, bs=16, B=4, ctx_range=(300, 2000), seed=77)
+    bt = case["block_tables"].to(DEV)
+    lens = (case["ctx"] + 1).to(DEV)
+    mx = int(lens.max())
+    q = case["q"][0].contiguous()
+
+    def calls():
+        out = torch.empty((4, 16, 128), dtype=torch.float32, device=DEV)
+        pkv.decode_attention_pooled(q, case["k_cache"], case["v_cache"], bt, lens, case["scale"], mx, out)
+        qm = case["q"][0].unsqueeze(1).repeat(1, 4, 1, 1).contiguous()          # [B, 4, H_q, D]
+        om = pkv.multi_query_attention(qm, case["k_cache"], case["v_cache"], bt, lens, case["scale"], mx)
+        torch.cuda.synchronize()
+        return out.cpu(), om.cpu()
+
+    a = calls()
+    assert pkv.library().pkv_shutdown() == 0
+    b = calls()
+    assert pkv.device_error(DEV) == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

@@ -100,3 +100,26 @@ def test_noalloc_refuses_more_scratch_than_it_has(lib):
     assert b"no-allocation" in lib.pkv_last_error()
     torch.cuda.synchronize()
     assert pkv.device_error(DEV) == 0
+
+
+def test_noalloc_after_shutdown_looks_the_array_up_again(lib):
+    """pkv_shutdown forgets the array's device address (a caller may reset
+    the device after it); the next call looks it up again and gives the same
+    result as before."""
+    torch.cuda.set_device(DEV)
+    spec = dict(B=3, H_q=16, H_kv=2, D=128, bs=16, kv="bf16", free_frac=0.1, steps=1, seed=303,
+                ctx=(2500, 900, 3100))
+    case = W.make_case(spec, device=DEV)
+    bt = case["block_tables"].to(DEV)
+    lens = (case["ctx"] + 1).to(DEV)
+    max_len = int(lens.max())
+    outs = []
+    for i in range(2):
+        out = torch.full((3, 16, 128), float("nan"), dtype=torch.float32, device=DEV)
+        assert _noalloc(lib, case, bt, lens, max_len, out) == L.PKV_OK, lib.pkv_last_error()
+        torch.cuda.synchronize()
+        outs.append(out.cpu())
+        if i == 0:
+            assert lib.pkv_shutdown() == L.PKV_OK
+    assert torch.all(torch.isfinite(outs[0])) and torch.equal(outs[0], outs[1])
+    assert pkv.device_error(DEV) == 0
