@@ -162,19 +162,7 @@ pkv_status pkv_bm_table_entries(pkv_block_manager* bm, int64_t seq_id, int32_t c
                                 int32_t* ids, int32_t* on_host, int32_t* n_entries);
 
 /*
- * Salience-driven eviction candidates ([UI] "Predictive Prefetching and
- * Attention-Salience Eviction Policy"): the device entries j of a sequence
- * with salience[j] < threshold, excluding logical block 0 (it holds the sink
- * tokens, positions < 4) and every block holding one of the last
- * `local_window` tokens; ordered by salience, ties by index.
- *   salience  float [entries of the sequence], host memory.
- */
-pkv_status pkv_bm_eviction_candidates(pkv_block_manager* bm, int64_t seq_id, const float* salience,
-                                      float threshold, int32_t local_window, int32_t capacity,
-                                      int32_t* logical, int32_t* n_out);
-
-/*
- * Prefetch candidates, the other half of the same policy ([UI] "Predictive
+ * Prefetch candidates ([UI] "Predictive
  * Prefetching and Attention-Salience Eviction Policy": an evicted block whose
  * predicted activation exceeds the prefetch threshold is staged some steps
  * ahead of the decode step that needs it): the host entries j of a sequence

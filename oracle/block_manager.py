@@ -45,10 +45,10 @@ Readings where the pages leave a step open (also listed in the design notes):
 Host tier (swap / stage / evict), from [UI] "Architecting Multi-Tier
 Disaggregated KV-Cache Hierarchies...", "C++ Block Scheduler and Asynchronous
 Fetch Kernel" (promote a block from host memory to HBM, demote it back; an
-already resident block is left alone, a pinned one is never demoted) and
-"Predictive Prefetching and Attention-Salience Eviction Policy" (sink blocks
-and the local recency window stay in HBM; other blocks whose salience is below
-a threshold are demoted), and [SC] "9. Failure modes and limitations", item 2
+already resident block is left alone) and
+"Predictive Prefetching and Attention-Salience Eviction Policy" (evicted
+blocks predicted to be needed soon are staged ahead of the step that reads
+them), and [SC] "9. Failure modes and limitations", item 2
 (swap a preempted request's blocks to host memory):
 
 6. A second pool of host blocks with its own free stack (same order rule).
@@ -60,11 +60,11 @@ a threshold are demoted), and [SC] "9. Failure modes and limitations", item 2
    entries already in the target tier are skipped.
 7. A sequence with any host entry cannot be appended to, forked or attended
    (its block table is not handed out) until it is staged back.
-8. Pinned entries for the salience policy: logical block 0 (it holds the
-   sink tokens, positions < 4) and every block that holds a position in the
-   last `local_window` tokens.  Candidates for eviction are the other device
-   entries whose salience is below the threshold, lowest salience first (ties
-   by logical index).
+8. Prefetch candidates: the host entries whose predicted activation is
+   above the threshold, most probable first (ties by logical index), no
+   more than the caller's capacity nor the free device blocks.  Which
+   entries to evict is the caller's choice (a salience statistic needs a
+   real model's attention weights).
 """
 
 import copy
@@ -189,20 +189,6 @@ class BlockManagerModel:
 
     def swap_in(self, seq_id):
         return self.stage(seq_id, range(len(self.tables[seq_id])))
-
-    def pinned(self, seq_id, local_window):
-        n, bs, L = len(self.tables[seq_id]), self.block_size, self.lens[seq_id]
-        pin = {0} if n else set()
-        if local_window > 0:                  # blocks holding positions L-W .. L-1
-            pin |= set(range(max(L - local_window, 0) // bs, n))
-        return pin
-
-    def eviction_candidates(self, seq_id, salience, threshold, local_window):
-        pin = self.pinned(seq_id, local_window)
-        host = self.on_host[seq_id]
-        c = [j for j in range(len(self.tables[seq_id]))
-             if j not in pin and j not in host and salience[j] < threshold]
-        return sorted(c, key=lambda j: (salience[j], j))
 
     def prefetch_candidates(self, seq_id, activation, threshold, capacity=None):
         """Host entries with activation above the threshold, most probable

@@ -477,15 +477,6 @@ class BlockManager:
     def swap_in(self, seq_id):
         return self.stage(seq_id, np.arange(len(self.table_entries(seq_id)[0])))
 
-    def eviction_candidates(self, seq_id, salience, threshold, local_window):
-        sal = np.ascontiguousarray(salience, dtype=np.float32)
-        out = np.empty(max(len(sal), 1), dtype=np.int32)
-        n = ctypes.c_int32()
-        _bm_check(library().pkv_bm_eviction_candidates(self._h, int(seq_id), _np_ptr(sal), float(threshold),
-                                                       int(local_window), len(out), _np_ptr(out),
-                                                       ctypes.byref(n)), "pkv_bm_eviction_candidates")
-        return out[:n.value].copy()
-
     def prefetch_candidates(self, seq_id, activation, threshold, capacity=None):
         """Host entries to stage ahead: activation > threshold, most probable
         first, at most `capacity` and the free device blocks."""

@@ -85,7 +85,6 @@ SIGNATURES = {
     "pkv_bm_evict": (_I32, [_P, _I64, _I32, _P, _P, _P, ctypes.POINTER(_I32)]),
     "pkv_bm_stage": (_I32, [_P, _I64, _I32, _P, _P, _P, ctypes.POINTER(_I32)]),
     "pkv_bm_table_entries": (_I32, [_P, _I64, _I32, _P, _P, ctypes.POINTER(_I32)]),
-    "pkv_bm_eviction_candidates": (_I32, [_P, _I64, _P, _F, _I32, _I32, _P, ctypes.POINTER(_I32)]),
     "pkv_bm_prefetch_candidates": (_I32, [_P, _I64, _P, _F, _I32, _P, ctypes.POINTER(_I32)]),
     "pkv_copy_blocks_between": (_I32, [_P, _P, _I64, _P, _P, _I64, ctypes.POINTER(CacheDesc), _P, _P, _I32, _I32,
                                        _P]),

@@ -443,33 +443,6 @@ pkv_status pkv_bm_table_entries(pkv_block_manager* bm, int64_t seq_id, int32_t c
   return PKV_OK;
 }
 
-pkv_status pkv_bm_eviction_candidates(pkv_block_manager* bm, int64_t seq_id, const float* salience,
-                                      float threshold, int32_t local_window, int32_t capacity,
-                                      int32_t* logical, int32_t* n_out) {
-  if (bm == nullptr || n_out == nullptr) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
-  if (local_window < 0) return fail(PKV_ERR_INVALID_ARG, "local_window %d", local_window);
-  std::lock_guard<std::mutex> lk(bm->mu);
-  Manager::Seq* sq;
-  pkv_status s = find_seq(bm, seq_id, &sq);
-  if (s != PKV_OK) return s;
-  const int64_t n = static_cast<int64_t>(sq->blocks.size());
-  if (n > 0 && salience == nullptr) return fail(PKV_ERR_INVALID_ARG, "salience is NULL");
-  // pinned: block 0 (sink tokens) and the blocks of the last local_window tokens
-  const int64_t first_local =
-      local_window > 0 ? (sq->len > local_window ? sq->len - local_window : 0) / bm->block_size : n;
-  std::vector<int32_t> c;
-  for (int64_t j = 1; j < n && j < first_local; ++j) {
-    if (sq->on_host[static_cast<size_t>(j)]) continue;
-    if (salience[j] < threshold) c.push_back(static_cast<int32_t>(j));
-  }
-  std::stable_sort(c.begin(), c.end(), [&](int32_t a, int32_t b) { return salience[a] < salience[b]; });
-  if (static_cast<int64_t>(c.size()) > capacity || (!c.empty() && logical == nullptr))
-    return fail(PKV_ERR_INVALID_ARG, "%zu candidates, capacity %d", c.size(), capacity);
-  for (size_t i = 0; i < c.size(); ++i) logical[i] = c[i];
-  *n_out = static_cast<int32_t>(c.size());
-  return PKV_OK;
-}
-
 pkv_status pkv_bm_prefetch_candidates(pkv_block_manager* bm, int64_t seq_id, const float* activation,
                                       float threshold, int32_t capacity, int32_t* logical, int32_t* n_out) {
   if (bm == nullptr || n_out == nullptr) return fail(PKV_ERR_INVALID_ARG, "NULL argument");

@@ -203,10 +203,6 @@ def test_native_host_tier_matches_the_model(seed):
         elif op < 0.62:
             s = rng.choice(live)
             n = len(model.table(s))
-            sal = [rng.choice([0.0, 0.01, 0.2, 0.5, 0.05]) for _ in range(n)]
-            w = rng.choice([0, 1, bs, 3 * bs])
-            assert native.eviction_candidates(s, sal, 0.1, w).tolist() == \
-                model.eviction_candidates(s, sal, 0.1, w)
             act = [rng.choice([0.0, 0.2, 0.35, 0.6, 0.9]) for _ in range(n)]
             cap = rng.randint(0, n + 1)
             assert native.prefetch_candidates(s, act, 0.3, cap).tolist() == \

@@ -233,20 +233,6 @@ def test_tier_moves_are_all_or_nothing():
     assert m.on_host[0] == {1, 2}
 
 
-def test_eviction_candidates_keep_sinks_and_the_local_window():
-    # [UI] "Predictive Prefetching and Attention-Salience Eviction Policy":
-    # blocks with tokens j < 4 are never evicted, nor the local window; the
-    # others go when their salience is under the threshold.
-    m = BlockManagerModel(32, 16)
-    m.add_sequence(0)
-    m.append([0], [16 * 10 + 3])              # 11 blocks, last one partial
-    sal = [0.0, 0.3, 0.01, 0.5, 0.02, 0.02, 0.9, 0.0, 0.0, 0.0, 0.0]
-    got = m.eviction_candidates(0, sal, 0.1, local_window=40)
-    # local window: positions 123..162 -> blocks 7..10
-    assert got == [2, 4, 5]
-    assert m.eviction_candidates(0, sal, 0.1, local_window=0) == [7, 8, 9, 10, 2, 4, 5]
-
-
 def test_prefetch_candidates_most_probable_first_within_the_free_blocks():
     # [UI] "Predictive Prefetching and Attention-Salience Eviction Policy":
     # an evicted block whose predicted activation is above the prefetch
