@@ -58,6 +58,8 @@ def run_cascade(case):
     (16, 128, (1, 3000), 8, 1, 128, 16),   # two one-tile ranges beside long suffixes
     (4, 256, (1, 1000), 8, 2, 128, 16),    # 8 slots per row: 4 suffix splits + 4 prefix ranges
     (8, 192, (1, 900), 8, 2, 64, 16),      # 5-8 slots per row, D = 64
+    (50, 128, (1, 100), 6, 1, 64, 32),     # sequence 42's rows straddle two prefix row blocks
+    (100, 64, (1, 700), 3, 2, 128, 16),    # G = 3: several straddling sequences, several splits
 ])
 def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, bs):
     case = shared_case(B, prefix, suffix, G, H_kv, D, bs, seed=500 + B + prefix)
@@ -196,4 +198,30 @@ def test_cascade_under_graph_capture_and_on_two_streams():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(outs[2].cpu(), want)
+    assert pkv.device_error(DEV) == 0
+
+
+def test_cascade_calls_sharing_one_workspace():
+    """Back-to-back calls on one workspace (filled with garbage first), with
+    lengths that alternate between two sets (some sequences with no private
+    token), each give the plain decode's result: no piece of an earlier call
+    leaks into a later one."""
+    case = shared_case(40, 128, (1, 600), 8, 2, 128, 16, seed=31337)
+    out_c, out_p = run_cascade(case)                  # appends the new token
+    bs = case["bs"]
+    bt = case["block_tables"].to(DEV)
+    lens = (case["ctx"].to(DEV) + 1).to(torch.int32)
+    mx = int(case["ctx"].max()) + 1
+    prefix = case["prefix"]
+    pblocks = bt[0, : prefix // bs].contiguous()
+    q = case["q"][0].contiguous()
+    plan = pkv.cascade_plan(q.shape[0], q.shape[1], pkv.cache_desc(case["k_cache"]), prefix, mx)
+    ws = torch.full((int(plan.workspace_bytes),), 0x7F, dtype=torch.uint8, device=DEV)
+    short = torch.clamp(lens - 37, min=prefix).to(torch.int32)   # fewer private tokens, some none
+    for ln in (lens, short, lens, short):
+        got = pkv.cascade_decode_attention(q, case["k_cache"], case["v_cache"], pblocks, prefix, bt, ln,
+                                           case["scale"], mx, workspace=ws)
+        want = pkv.decode_attention(q, case["k_cache"], case["v_cache"], bt, ln, case["scale"], max_context_len=mx)
+        assert torch.max(torch.abs(got - want)) < 1e-4
+    assert torch.max(torch.abs(out_c - out_p)) < 1e-4
     assert pkv.device_error(DEV) == 0
