@@ -117,7 +117,7 @@ def test_split_count_does_not_change_the_result():
         assert np.abs(o - outs[0]).max() <= 1e-5
 
 
-@pytest.mark.parametrize("q_len", [2, 4, 16])   # mma.sync; persistent tcgen05 (x2)
+@pytest.mark.parametrize("q_len", [2, 3, 4, 8, 16])   # mma.sync; persistent tcgen05 (24 .. 128 rows)
 def test_full_size_gqa_workload_every_unit(q_len):
     """B=64, H_q=64, H_kv=8, D=128, bs=16, contexts U[512, 8192]: the q_len
     new tokens of every sequence are appended by pkv.append, then attended
