@@ -250,6 +250,27 @@ int32_t decode_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx
   const int64_t n = ceil_div(max_ctx, st);
   if (n >= 2 && max_ctx - (n - 1) * st < st / 8)
     st = static_cast<int32_t>(ceil_div(ceil_div(max_ctx, n - 1), 64) * 64);
+  // Long contexts (more than 16 splits of the longest sequence): the split
+  // CTAs then mostly take the same time, and the SMs of a GB300 do not all
+  // stream at the same rate, so a grid's tail is set by how full its last
+  // wave is.  On 8 sequences of 131k tokens the decode kernel ran at 7.15 TB/s
+  // with the six-wave rule's 63 splits (8.8 waves of three CTAs per SM), in
+  // troughs of 7.01-7.09 wherever the last wave was nearly full (28, 35, 42
+  // splits) and at 7.25-7.32 where it was about half full (25, 32, 38
+  // splits).  Take the fewest splits that give at least three waves with a
+  // last wave 40-70 % full.
+  if (n > 16) {
+    const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
+    const int64_t slots = static_cast<int64_t>(3) * sms;
+    for (int64_t s = 2; s < n; ++s) {
+      const int64_t waves100 = units * s * 100 / slots;  // waves of the grid x 100
+      const int64_t frac = waves100 % 100;
+      if (waves100 >= 300 && frac >= 40 && frac <= 70) {
+        st = static_cast<int32_t>(ceil_div(ceil_div(max_ctx, s), 64) * 64);
+        break;
+      }
+    }
+  }
   return st;
 }
 

@@ -157,6 +157,12 @@ def _auto_split(batch, hkv, max_ctx, sms=152):
     n = -(-max_ctx // st)
     if n >= 2 and max_ctx - (n - 1) * st < st // 8:
         st = -(-(-(-max_ctx // (n - 1))) // 64) * 64
+    if n > 16:          # long contexts: >= 3 waves, the last 40-70 % full, fewest splits
+        for s in range(2, n):
+            w100 = units * s * 100 // (3 * sms)
+            if w100 >= 300 and 40 <= w100 % 100 <= 70:
+                st = -(-(-(-max_ctx // s)) // 64) * 64
+                break
     return st
 
 
@@ -208,8 +214,12 @@ def test_fixed_split_auto_size_gives_enough_ctas_for_long_contexts(lib):
     # otherwise six waves, and no nearly empty last split
     p = _plan(lib, _desc(), 64, 64, 8193)
     assert 64 * 8 * p.max_splits >= 152 * 3 * 6 and p.max_splits == 8 and p.split_tokens == 1088
-    p = _plan(lib, _desc(), 8, 64, 131092)                   # the long-context workload at 20 steps
-    assert 8 * 8 * p.max_splits >= 152 * 3 * 6 and p.max_splits < -(-131092 // 2048)
+    # long contexts: the fewest splits giving >= 3 waves with the last wave 40-70 % full
+    for max_ctx in (131092, 131104, 131136):                 # the long-context workload's steps
+        p = _plan(lib, _desc(), 8, 64, max_ctx)
+        w100 = 8 * 8 * p.max_splits * 100 // (152 * 3)
+        assert w100 >= 300 and 40 <= w100 % 100 <= 70, (max_ctx, p.max_splits)
+        assert p.max_splits == 25
 
 
 def test_workspace_too_small_is_reported(lib):
