@@ -341,6 +341,12 @@ def test_multi_query_plan_shapes(lib):
     assert r == L.PKV_OK and p.workers == 0
     r, p = _mqplan(lib, desc, 2, 2, 64, 100)
     assert r == L.PKV_OK and p.workers == 4
+    # long contexts on the mma.sync kernel: the decode planner's long-context
+    # rule (>= 3 waves of three CTAs per SM, the last 40-70 % full)
+    r, p = _mqplan(lib, _desc(block_size=32), 8, 2, 64, 131074)
+    assert r == L.PKV_OK and p.workers == 4 and p.max_splits == 25
+    w100 = 8 * 8 * p.max_splits * 100 // (3 * 152)
+    assert w100 >= 300 and 40 <= w100 % 100 <= 70
 
 
 @pytest.mark.parametrize("kw,code", [
