@@ -242,20 +242,21 @@ int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 // 252.8 us).  Otherwise the six-wave power-of-two rule of auto_split_tokens,
 // with a last split shorter than an eighth of the others folded into them
 // (8193 tokens: eight splits of 1088 rather than eight of 1024 and one of 1).
-// Long contexts (more than 16 splits of the longest sequence) on grids of
-// three CTAs per SM: the split CTAs then mostly take the same time, and the
-// SMs of a GB300 do not all stream at the same rate, so a grid's tail is set
-// by how full its last wave is.  On 8 sequences of 131k tokens the decode
-// kernel ran at 7.15 TB/s with the six-wave rule's 63 splits (8.8 waves), in
-// troughs of 7.01-7.09 wherever the last wave was nearly full (28, 35, 42
-// splits) and at 7.25-7.32 where it was about half full (25, 32, 38 splits);
-// the multi-token mma.sync kernel (q_len 2) showed the same period.  Take the
-// fewest splits that give at least three waves with a last wave 40-70 %
-// full; `st` (splitting the longest context `max_ctx` into more than 16
-// pieces) otherwise stays.
-int32_t long_context_split(int64_t units, int32_t max_ctx, int32_t sms, int32_t st) {
+// Split length for grids of three CTAs per SM, given the six-wave rule's
+// `st` (which cuts the longest context `max_ctx` into n pieces): when n is
+// above `min_splits`, the fewest splits that give at least three waves with
+// a last wave 40-70 % full.  The SMs of a GB300 do not all stream at the same
+// rate, so a grid's tail is set by how full its last wave is: on 8 sequences
+// of 131k tokens the decode kernel ran at 7.15 TB/s with the six-wave rule's
+// 63 splits (8.8 waves), in troughs of 7.01-7.09 wherever the last wave was
+// nearly full (28, 35, 42 splits) and at 7.25-7.32 where it was about half
+// full (25, 32, 38 splits); the multi-token mma.sync kernel (q_len 2) showed
+// the same period.  The shared-prefix batch (128 sequences of 4.2-5.1k
+// tokens) took 2 splits instead of 3 (+2.6 %); the GQA batch 4 instead of 8
+// (no change).
+int32_t half_wave_split(int64_t units, int32_t max_ctx, int32_t sms, int32_t st, int64_t min_splits) {
   const int64_t n = ceil_div(max_ctx, st);
-  if (n <= 16) return st;
+  if (n <= min_splits) return st;
   const int64_t slots = static_cast<int64_t>(3) * sms;
   for (int64_t s = 2; s < n; ++s) {
     const int64_t waves100 = units * s * 100 / slots;  // waves of the grid x 100
@@ -273,7 +274,7 @@ int32_t decode_split_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_ctx
   const int64_t n = ceil_div(max_ctx, st);
   if (n >= 2 && max_ctx - (n - 1) * st < st / 8)
     st = static_cast<int32_t>(ceil_div(ceil_div(max_ctx, n - 1), 64) * 64);
-  return long_context_split(static_cast<int64_t>(batch) * num_kv_heads, max_ctx, sms, st);
+  return half_wave_split(static_cast<int64_t>(batch) * num_kv_heads, max_ctx, sms, st, 1);
 }
 
 pkv_status plan(int32_t batch, int32_t num_q_heads, const pkv_cache_desc* c, int32_t max_ctx,
@@ -1048,11 +1049,13 @@ pkv_status mq_plan(int32_t batch, int32_t q_len, int32_t num_q_heads, const pkv_
     const int64_t want = static_cast<int64_t>(sms) * (tc ? 3 : 18);
     st = tc ? static_cast<int32_t>(max_st) : 4096;
     while (st > 256 && units * ceil_div(max_ctx, st) < want) st /= 2;
-    // long contexts on the mma.sync kernel (three CTAs per SM): as for decode
-    // (q_len 2 on 8 sequences of 131k tokens: 6.94 TB/s at 25 splits, 6.75 at
-    // the six-wave rule's 65)
+    // long contexts (more than 16 splits) on the mma.sync kernel (three CTAs
+    // per SM): as for decode (q_len 2 on 8 sequences of 131k tokens: 6.94 TB/s
+    // at 25 splits, 6.75 at the six-wave rule's 65); on the GQA batch the
+    // half-wave choice measured 1-1.5 % slower, so shorter contexts keep the
+    // six-wave rule
     if (!tc) {
-      const int64_t lc = long_context_split(units, max_ctx, sms, st);
+      const int64_t lc = half_wave_split(units, max_ctx, sms, st, 16);
       st = static_cast<int32_t>(lc < max_st ? lc : max_st);
     }
   }

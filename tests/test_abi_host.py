@@ -147,7 +147,8 @@ def _auto_split(batch, hkv, max_ctx, sms=152):
     """The automatic split length, restated: one split per (sequence, KV head)
     when those give four waves of three CTAs per SM, else the largest power of
     two (256..4096) giving six waves, with a last split shorter than an
-    eighth of the others folded into them."""
+    eighth of the others folded into them; then, if that still splits, the
+    fewest splits giving at least three waves with the last 40-70 % full."""
     units = batch * hkv
     if units >= 4 * 3 * sms:
         return max(64, -(-max_ctx // 64) * 64)
@@ -157,7 +158,8 @@ def _auto_split(batch, hkv, max_ctx, sms=152):
     n = -(-max_ctx // st)
     if n >= 2 and max_ctx - (n - 1) * st < st // 8:
         st = -(-(-(-max_ctx // (n - 1))) // 64) * 64
-    if n > 16:          # long contexts: >= 3 waves, the last 40-70 % full, fewest splits
+    n = -(-max_ctx // st)
+    if n > 1:           # >= 3 waves, the last 40-70 % full, fewest splits
         for s in range(2, n):
             w100 = units * s * 100 // (3 * sms)
             if w100 >= 300 and 40 <= w100 % 100 <= 70:
@@ -211,9 +213,12 @@ def test_fixed_split_auto_size_gives_enough_ctas_for_long_contexts(lib):
     assert p.max_splits == 1 and p.workspace_bytes == 0
     p = _plan(lib, _desc(), 256, 64, 4097)                   # the FP8 workload's shape
     assert p.max_splits == 1 and p.workspace_bytes == 0
-    # otherwise six waves, and no nearly empty last split
+    # otherwise the fewest splits giving >= 3 waves with a half-full last wave
+    # (the six-wave rule's 8 splits of 1088 tokens before it)
     p = _plan(lib, _desc(), 64, 64, 8193)
-    assert 64 * 8 * p.max_splits >= 152 * 3 * 6 and p.max_splits == 8 and p.split_tokens == 1088
+    assert p.max_splits == 4 and p.split_tokens == 2112
+    p = _plan(lib, _desc(block_size=32), 128, 64, 5121)      # the shared-prefix batch
+    assert p.max_splits == 2
     # long contexts: the fewest splits giving >= 3 waves with the last wave 40-70 % full
     for max_ctx in (131092, 131104, 131136):                 # the long-context workload's steps
         p = _plan(lib, _desc(), 8, 64, max_ctx)

@@ -82,7 +82,9 @@ def test_noalloc_refuses_more_scratch_than_it_has(lib):
     happening the call would still only touch valid memory and the test
     would fail on the status, not on the GPU."""
     torch.cuda.set_device(DEV)
-    B, H_q, H_kv, D, bs, mb = 200, 64, 8, 128, 16, 4096
+    # 114 x 8 units = two waves of three CTAs on each of 152 SMs, so no split
+    # count leaves a half-full last wave and the planner keeps 16 splits
+    B, H_q, H_kv, D, bs, mb = 114, 64, 8, 128, 16, 4096
     kc = torch.zeros((1, H_kv, bs, D), dtype=torch.bfloat16, device=DEV)
     vc = torch.zeros_like(kc)
     q = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device=DEV)
