@@ -181,7 +181,12 @@ pkv_status pkv_decode_attention(const void* q, int32_t batch, int32_t num_q_head
  * `split_tokens` divides the work, and the scratch it needs.
  *   mode          1 = fixed splits of `split_tokens` tokens per sequence (the
  *                 default; split_tokens 0 picks the size), one CTA each, which
- *                 the hardware scheduler balances across SMs.
+ *                 the hardware scheduler balances across SMs.  The automatic
+ *                 size: one split per (sequence, KV head) when those alone
+ *                 give four waves of three CTAs per SM; else the fewest
+ *                 splits of max_context_len giving at least three waves with
+ *                 a last wave 40-70 % full, when such a count lies below the
+ *                 count of a six-wave power-of-two split; else that split.
  *                 0 = balanced ("stream-K"), on request with split_tokens -1
  *                 and batch <= 2048: the (sequence, KV head, 16-token tile)
  *                 space is cut into equal contiguous ranges, one per warp of a
