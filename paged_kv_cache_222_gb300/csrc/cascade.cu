@@ -604,7 +604,8 @@ __device__ __forceinline__ MqUnit mq_unit(const DecodeParams& p, int u, int nrb,
 
 // Work units in order of decreasing tile count (longest first, so that the
 // last units any CTA takes are short): a counting sort over the tile counts
-// into `perm`, by one CTA.  Also zeroes the unit counter.
+// into `perm`, by one CTA.  Also zeroes the unit counter and prefetches the
+// units' block-table rows into L2.
 __global__ void __launch_bounds__(1024) mq_order_kernel(const DecodeParams p, int* perm) {
   __shared__ int cnt[kMultiQueryMaxSplitBlocks + 1];
   const int rows = p.q_len * p.group, nrb = (rows + 127) / 128;
@@ -625,6 +626,16 @@ __global__ void __launch_bounds__(1024) mq_order_kernel(const DecodeParams p, in
   }
   __syncthreads();
   for (int u = threadIdx.x; u < U; u += blockDim.x) perm[atomicAdd(&cnt[mq_unit(p, u, nrb, false).ntile], 1)] = u;
+  // The producers read a unit's block ids with one dependent load per lane
+  // per 32 ids before its first tile: bring every unit's table row into L2
+  // now (+0.7-0.8 % at q_len 4-16 on the GQA batch).
+  for (int u = threadIdx.x; u < U; u += blockDim.x) {
+    const MqUnit w = mq_unit(p, u, nrb, false);
+    const int nblk = (w.t1 - w.t0 + p.block_size - 1) / p.block_size;
+    const char* row = reinterpret_cast<const char*>(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
+                                                     w.t0 / p.block_size);
+    for (int off = 0; off < nblk * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+  }
 }
 
 // Unit number n of this CTA from the ring (readers: one call per warp, lane
