@@ -222,6 +222,17 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     const int box = p.block_size < NKEY ? p.block_size : NKEY;  // token rows per TMA box
     const int per_half = NKEY / box;
     const int nbox = 2 * C::HALVES * per_half / C::NPROD;        // boxes of a tile per warp (<= 32)
+    // This lane's box of every tile, set up once.  Ranges start at multiples
+    // of 64 tokens and the block size (16 or 32) divides 64, so each box is a
+    // whole block: box i of tile kt is block kt * per_half + i of the range.
+    const int gi = pw * nbox + lane;                             // box of the tile
+    const int bv = gi / (C::HALVES * per_half);                  // 0: K, 1: V
+    const int bx = (gi / per_half) % C::HALVES;                  // d-half
+    const int bi = gi % per_half;                                // block within the half
+    const uint32_t off = bv * C::KREG + bx * C::HALF_BYTES + bi * box * 128;
+    const CUtensorMap* tmap = bv ? &tmap_v : &tmap_k;
+    const int c0 = bx * L::BOX_ELEMS;
+    int kt = first;                                              // tile of the range at step k
     int issued = 0;
     for (int k = 0; k < ntile; ++k) {
       const int s = k % NS;
@@ -237,15 +248,11 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
       }
       __syncwarp();
       if (lane < nbox) {
-        const int gi = pw * nbox + lane;                       // box of the tile
-        const int v = gi / (C::HALVES * per_half);             // 0: K, 1: V
-        const int bx = (gi / per_half) % C::HALVES;            // d-half
-        const int i = gi % per_half;                           // box within the half
-        const int t = t0 + ((k + first) % ntile) * NKEY + i * box;
-        const int phys = t < t1 ? s_blk[(t - t0) / p.block_size] : -1;  // past the range: zeros
-        const uint32_t off = v * C::KREG + bx * C::HALF_BYTES + i * box * 128;
-        tma_load_4d(dst + off, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, h, phys);
+        const int j = kt * per_half + bi;
+        const int phys = j < nblk ? s_blk[j] : -1;  // past the range: zeros
+        tma_load_4d(dst + off, tmap, bar, c0, 0, h, phys);
       }
+      if (++kt == ntile) kt = 0;
       issued = k + 1;
     }
     if (lane == 0 && *s_abort) {  // the copies in flight land before the stages are released
@@ -773,13 +780,21 @@ __global__ void __launch_bounds__(256, 1)
       }
       __syncwarp();
       // this lane's box of each tile: d-half, block within the tile (warp 4
-      // loads the K ring, warp 5 the V ring)
+      // loads the K ring, warp 5 the V ring).  A unit starts at a multiple of
+      // 64 tokens and the block size (16 or 32) divides 64, so every box is a
+      // whole block: box i of tile k is block k * per_half + i of the unit,
+      // from its first row.  The operands are set up once per unit: the issue
+      // loop shares its sub-partition with a softmax warp, and every
+      // instruction in it delays the next box.
       const int bx = lane / per_half;
       const int i = lane % per_half;
       const int nring = pw == 0 ? NK : NV;
       const uint32_t ring = pw == 0 ? kring : vring;
       uint64_t* rfull = pw == 0 ? kfull : vfull;
       uint64_t* rempty = pw == 0 ? kempty : vempty;
+      const CUtensorMap* tmap = pw ? &tmap_v : &tmap_k;
+      const uint32_t off = bx * C::HALF_BYTES + i * box * 128;
+      const int c0 = bx * L::BOX_ELEMS;
       bool ok = true;
       for (int k = 0; k < w.ntile; ++k, ++g) {
         const int s = g % nring;
@@ -798,10 +813,9 @@ __global__ void __launch_bounds__(256, 1)
         }
         __syncwarp();
         if (lane < nbox) {
-          const int t = w.t0 + k * NKEY + i * box;
-          const int phys = t < w.t1 ? ids[(t - w.t0) / p.block_size] : -1;  // past the range: zeros
-          const uint32_t off = bx * C::HALF_BYTES + i * box * 128;
-          tma_load_4d(dst + off, pw ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS, t % p.block_size, w.h, phys);
+          const int j = k * per_half + i;
+          const int phys = j < nblk ? ids[j] : -1;  // past the range: zeros
+          tma_load_4d(dst + off, tmap, bar, c0, 0, w.h, phys);
         }
       }
       if (!ok) break;
