@@ -55,6 +55,13 @@ namespace {
 
 // Wait for a barrier phase; false once the CTA aborts (or on time-out, which
 // records the error and raises the abort flag).
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err, volatile int* abort,
                                               uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -578,6 +585,11 @@ __global__ void __launch_bounds__(128) wait_selftest_kernel(int which, uint64_t 
 // of 32-key tiles measured 38 % slower than six of 64 (per-tile costs
 // double).
 constexpr int kMqTile = 64;
+// Bytes of the barrier / unit-ring block after the block ids, and the stride
+// of one row of the output staging after it: 32 floats (128 B) and 16 B of
+// padding, so that the 16-byte stores of a quarter warp hit distinct banks.
+constexpr int kMqBarBytes = 1024;
+constexpr int kMqStageRow = 144;
 constexpr int kMqKStages = 6;
 constexpr int kMqVStages = 6;
 
@@ -701,6 +713,9 @@ __global__ void __launch_bounds__(256, 1)
   int* s_unit = reinterpret_cast<int*>(done + 2);     // [R]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_unit + R);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  static_assert((2 * NK + 2 * NV + 8 + 1 + 2 * R + 2) * 8 + R * 4 + 8 <= kMqBarBytes, "barrier block");
+  // [128][kMqStageRow] the softmax rows' output staging
+  uint8_t* s_stage = smem + (NK + NV) * C::KREG + 2 * kMultiQueryMaxSplitBlocks * 4 + kMqBarBytes;
 
   if (tid == 0) {
     for (int s = 0; s < NK; ++s) {
@@ -770,13 +785,24 @@ __global__ void __launch_bounds__(256, 1)
       const int32_t* blocks = p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks + w.t0 / p.block_size;
       int* ids = s_ids + pw * kMultiQueryMaxSplitBlocks;
       const int nblk = (w.t1 - w.t0 + p.block_size - 1) / p.block_size;
-      for (int j = lane; j < nblk; j += 32) {
-        int phys = blocks[j];
-        if (phys < 0 || phys >= p.num_blocks) {
-          if (pw == 0) record_error(p.err, kDevErrBlockId);
-          phys = -1;  // fully outside the tensor: the TMA unit fills zeros
+      // eight independent loads per lane in flight at a time (the table row
+      // is in L2: the unit-order kernel prefetched it)
+      for (int j0 = lane; j0 < nblk; j0 += 32 * 8) {
+        int ph[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ph[q] = j0 + 32 * q < nblk ? __ldg(blocks + j0 + 32 * q) : 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int j = j0 + 32 * q;
+          if (j < nblk) {
+            int phys = ph[q];
+            if (phys < 0 || phys >= p.num_blocks) {
+              if (pw == 0) record_error(p.err, kDevErrBlockId);
+              phys = -1;  // fully outside the tensor: the TMA unit fills zeros
+            }
+            ids[j] = phys;
+          }
         }
-        ids[j] = phys;
       }
       __syncwarp();
       // this lane's box of each tile: d-half, block within the tile (warp 4
@@ -919,7 +945,13 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ softmax
     const int r_in = warp * 32 + lane;                 // row within the unit's row block
     const uint32_t tl = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    const float qk_mult = p.qk_log2_scale;
+    // The softmax works on the raw products S = Q K^T and applies the logit
+    // multiplier (scale x log2 e) inside the exponent's FMA; a negative scale
+    // enters as negated Q (exact in bf16), so that the multiplier is positive
+    // and the row maximum of S maps to the maximum logit.  A zero scale takes
+    // the smallest normal multiplier: every logit rounds to 0 all the same.
+    const float qk_mult = fmaxf(fabsf(p.qk_log2_scale), 1.17549435e-38f);
+    const uint32_t q_sign = p.qk_log2_scale < 0.f ? 0x80008000u : 0u;
     uint4 qw[D / 8];                                   // the next unit's Q row
     // load this thread's Q row of unit w (zeros past the rows)
     auto load_q = [&](const MqUnit& w) {
@@ -927,8 +959,13 @@ __global__ void __launch_bounds__(256, 1)
       const int64_t orow = (static_cast<int64_t>(w.b) * QL + row / G) * H_q + w.h * G + row % G;
       const uint16_t* qr = row < rows ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c)
+      for (int c = 0; c < D / 8; ++c) {
         qw[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+        qw[c].x ^= q_sign;
+        qw[c].y ^= q_sign;
+        qw[c].z ^= q_sign;
+        qw[c].w ^= q_sign;
+      }
     };
     // row r of Q into TMEM lane r as bf16 pairs (element 2j in the low half
     // of column j, the memory order of the loaded words), then tell the S issuer
@@ -965,7 +1002,28 @@ __global__ void __launch_bounds__(256, 1)
       const int64_t orow = (static_cast<int64_t>(w.b) * QL + row / G) * H_q + w.h * G + row % G;
       // tokens this row may attend: [0, lim)
       const int lim = row_ok ? min(w.t1, w.ctx - QL + row / G + 1) : w.t0;
+      // a warp past the unit's last query row (q_len x G rows fill only part
+      // of the 128-row block) keeps the barrier phases and computes nothing:
+      // its P rows feed only O rows that are never written
+      const bool idle = w.row0 + warp * 32 >= rows;
       float m_used = -CUDART_INF_F, lsum = 0.f;
+      if (idle) {
+        for (int k = 0; k < w.ntile; ++k, ++g) {
+          const int b = g & 1;
+          ok = __all_sync(kFull, wait_or_abort(smem_u32(sfull + b), static_cast<uint32_t>((g >> 1) & 1), p.err,
+                                               s_abort));
+          if (!ok) break;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(sfree + b));
+          if (g >= 2) {  // the phase order of P[b]: P(g-2).V has been issued and read it
+            ok = __all_sync(kFull, wait_or_abort(smem_u32(pfree + b), static_cast<uint32_t>(((g - 2) >> 1) & 1),
+                                                 p.err, s_abort));
+            if (!ok) break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(pfull + b));
+        }
+      } else
       for (int k = 0; k < w.ntile; ++k, ++g) {
         const int b = g & 1;
         ok = __all_sync(kFull, wait_or_abort(smem_u32(sfull + b), static_cast<uint32_t>((g >> 1) & 1), p.err,
@@ -981,12 +1039,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int c = 0; c < NKEY / 16; ++c)
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {  // packed f32x2 multiplies
-              const float2 y = __fmul2_rn(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])),
-                                          make_float2(qk_mult, qk_mult));
-              x[16 * c + i] = y.x;
-              x[16 * c + i + 1] = y.y;
-            }
+            for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]);
         }
         tc_fence_before();  // S[b] may be overwritten
         __syncwarp();
@@ -998,13 +1051,17 @@ __global__ void __launch_bounds__(256, 1)
             if (i >= valid) x[i] = -CUDART_INF_F;
         }
         float mt;
-        {  // tree of partial maxima: a short dependency chain
+        {  // eight chains of three-input maxima, then their maximum (in log2 units)
+          static_assert(NKEY == 64, "eight chains of eight keys");
           float mp[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mp[i] = x[i];
-#pragma unroll
-          for (int i = 8; i < NKEY; ++i) mp[i & 7] = fmaxf(mp[i & 7], x[i]);
-          mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+          for (int j = 0; j < 8; ++j) {
+            mp[j] = max3f(x[j], x[8 + j], x[16 + j]);
+            mp[j] = max3f(mp[j], x[24 + j], x[32 + j]);
+            mp[j] = max3f(mp[j], x[40 + j], x[48 + j]);
+            mp[j] = fmaxf(mp[j], x[56 + j]);
+          }
+          mt = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * qk_mult;
         }
         float alpha = 1.f;
         bool resc = false;
@@ -1045,13 +1102,14 @@ __global__ void __launch_bounds__(256, 1)
         }
         const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
         const float2 neg_mu = make_float2(-mu, -mu);
+        const float2 mult2 = make_float2(qk_mult, qk_mult);
         float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c0 = 0; c0 < NKEY / 2; c0 += 16) {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 e = __fadd2_rn(make_float2(x[2 * (c0 + i)], x[2 * (c0 + i) + 1]), neg_mu);
+            const float2 e = __ffma2_rn(make_float2(x[2 * (c0 + i)], x[2 * (c0 + i) + 1]), mult2, neg_mu);
             const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
             ls[i & 1] = __fadd2_rn(ls[i & 1], pp);
             hi[i] = pack_bf16x2(pp.x, pp.y);
@@ -1068,9 +1126,9 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) mbar_arrive(smem_u32(pfull + b));   // P(g) is in TMEM
       }
       if (!ok) break;
-      // the next unit: its Q rows are loaded now, stored into TMEM after this
-      // unit's output (every S of this unit has completed: the loop above saw
-      // each one's sfull)
+      // the next unit: its Q rows are loaded now and go into TMEM once this
+      // unit's last P.V has completed (every S of this unit has completed
+      // too: the loop above saw each one's sfull)
       const int u_next = mq_read_unit(ufull, uempty, s_unit, n + 1, p.err, s_abort);
       MqUnit w_next;
       if (u_next >= 0) {
@@ -1081,13 +1139,31 @@ __global__ void __launch_bounds__(256, 1)
       if (w.ntile > 0)
         ok = __all_sync(kFull, wait_or_abort(smem_u32(pfree + ((g - 1) & 1)),
                                              static_cast<uint32_t>(((g - 1) >> 1) & 1), p.err, s_abort));
+      if (!ok) break;
+      // The next unit's Q goes in first, so that its first S runs beside this
+      // epilogue.  Its first P.V, which overwrites O, waits for P from these
+      // warps, which they write only after reading O below.
+      if (u_next >= 0) store_q();
       const bool writes = w.t0 < w.ctx || (w.ctx == 0 && w.split == 0);
       const bool direct = w.nsplit <= 1;
       const int64_t piece = orow * p.slots_per_row + w.split;
-      if (ok && writes) {
+      if (writes && !idle) {
         if (w.ntile > 0) tc_fence_after();
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float sc = direct ? inv : 1.f;
         float* dst_row = direct ? p.out + orow * D : p.ws_o + piece * D;
+        // O leaves through shared memory, 32 columns of the warp's 32 rows per
+        // pass: each thread stages its row piece, then every store
+        // instruction writes four whole 128-byte row pieces (16-byte stores
+        // straight from the TMEM rows would scatter each one over 32 rows).
+        // Lane l stores chunk l % 8 of rows l / 8 + 4 j; rd[j] is that row's
+        // destination (0: no such row).
+        uint8_t* swarp = s_stage + warp * 32 * kMqStageRow;
+        uint8_t* srow = swarp + lane * kMqStageRow;
+        const uint64_t my_dst = row_ok ? reinterpret_cast<uint64_t>(dst_row) : 0ull;
+        uint64_t rd[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) rd[j] = __shfl_sync(kFull, my_dst, (lane >> 3) + 4 * j);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t v[2][16];
@@ -1099,24 +1175,26 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
           }
-          if (row_ok) {
-            const float sc = direct ? inv : 1.f;
-            float4* dst = reinterpret_cast<float4*>(dst_row + c0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]) * sc,
-                                   __uint_as_float(v[i / 4][4 * (i % 4) + 1]) * sc,
-                                   __uint_as_float(v[i / 4][4 * (i % 4) + 2]) * sc,
-                                   __uint_as_float(v[i / 4][4 * (i % 4) + 3]) * sc);
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(srow + 16 * i) =
+                make_float4(__uint_as_float(v[i / 4][4 * (i % 4)]) * sc, __uint_as_float(v[i / 4][4 * (i % 4) + 1]) * sc,
+                            __uint_as_float(v[i / 4][4 * (i % 4) + 2]) * sc,
+                            __uint_as_float(v[i / 4][4 * (i % 4) + 3]) * sc);
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 val =
+                *reinterpret_cast<const float4*>(swarp + ((lane >> 3) + 4 * j) * kMqStageRow + (lane & 7) * 16);
+            if (rd[j] != 0ull) reinterpret_cast<float4*>(rd[j])[c0 / 4 + (lane & 7)] = val;
           }
+          __syncwarp();  // the warp has read the staging before the next pass
         }
         if (row_ok && !direct) {
           p.ws_ml[piece * 2] = m_used;
           p.ws_ml[piece * 2 + 1] = lsum;
         }
       }
-      if (!ok) break;
-      if (u_next >= 0) store_q();  // after O was read: P.V of the next unit overwrites O
       u = u_next;
       w = w_next;
     }
@@ -1134,7 +1212,7 @@ template <int D>
 int mq_tc_smem_bytes() {
   // at least 120 KB: one CTA per SM (it holds all 512 TMEM columns)
   const int need = (kMqKStages + kMqVStages) * TcTile<D, kMqTile>::KREG + 2 * kMultiQueryMaxSplitBlocks * 4 +
-                   128 * 8 + 1024 + 1024;
+                   kMqBarBytes + 128 * kMqStageRow + 1024;
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 

@@ -89,6 +89,21 @@ def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, bs, split_tokens):
     assert np.abs(out - want).max() <= 2e-3
 
 
+@pytest.mark.parametrize("scale", [-0.25, 0.0, 3.0])
+@pytest.mark.parametrize("q_len,H_q", [(2, 8), (4, 8), (16, 16)])   # mma.sync; tcgen05 (32 and 256 rows)
+def test_negative_zero_and_large_scales(q_len, H_q, scale):
+    # the tensor-core kernel applies the logit multiplier inside the
+    # exponent and folds a negative scale into Q; a zero scale gives the mean
+    # of V over each query's causal range
+    case = _small_case([q_len, 100, 700], q_len, H_q, 1, 128, 16, seed=20260310 + q_len)
+    case["scale"] = scale
+    for st in (0, 64):
+        out = _run(case, st)
+        want = _oracle(case)
+        assert np.isfinite(out).all()
+        assert np.abs(out - want).max() <= 2e-3
+
+
 def test_short_and_empty_contexts_give_zeros_for_unplaced_queries():
     q_len = 8
     case = _small_case([0, 3, 8, 9], q_len, 8, 2, 128, 16, seed=20260301)
