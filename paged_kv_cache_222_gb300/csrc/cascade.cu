@@ -340,12 +340,19 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
       // (the 128-byte swizzle)
       const uint16_t* qr = row_ok ? static_cast<const uint16_t*>(p.q) + orow * D : nullptr;
       uint8_t* qg = q_sm + grp * C::HALVES * C::QHALF;
+      // a negative scale enters as negated Q (exact in bf16): the softmax
+      // below applies a positive multiplier to the raw products
+      const uint32_t q_sign = p.qk_log2_scale < 0.f ? 0x80008000u : 0u;
       uint4 w[D / 8];  // every load issued before the first store
 #pragma unroll
       for (int c = 0; c < D / 8; ++c)
         w[c] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
+        w[c].x ^= q_sign;
+        w[c].y ^= q_sign;
+        w[c].z ^= q_sign;
+        w[c].w ^= q_sign;
         const int hf = c >> 3, cc = c & 7;
         *reinterpret_cast<uint4*>(qg + hf * C::QHALF + r_in * 128 + ((cc ^ (r_in & 7)) << 4)) = w[c];
       }
@@ -355,7 +362,9 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
     const uint32_t tl = tbase + grp * GCOLS + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const uint32_t g_sfull = smem_u32(sfull + grp), g_sfree = smem_u32(sfree + grp);
     const uint32_t g_pfull = smem_u32(pfull + grp), g_pfree = smem_u32(pfree + grp);
-    const float qk_mult = p.qk_log2_scale;
+    // the logit multiplier (scale x log2 e, made positive above) is applied
+    // inside the exponent's FMA; a zero scale takes the smallest normal one
+    const float qk_mult = fmaxf(fabsf(p.qk_log2_scale), 1.17549435e-38f);
     float m_used = -CUDART_INF_F, lsum = 0.f;
     bool ok = true;
     for (int k = 0; k < ntile && ok; ++k) {
@@ -374,12 +383,7 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < NKEY / 16; ++c)
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {  // packed f32x2 multiplies
-            const float2 y = __fmul2_rn(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])),
-                                        make_float2(qk_mult, qk_mult));
-            x[16 * c + i] = y.x;
-            x[16 * c + i + 1] = y.y;
-          }
+          for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[c][i]);
       }
       const int valid = t1 - (t0 + ((k + first) % ntile) * NKEY);  // the prefix has no causal limit
       if (__any_sync(kFull, valid < NKEY)) {
@@ -388,13 +392,17 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
           if (i >= valid) x[i] = -CUDART_INF_F;
       }
       float mt;
-      {  // tree of partial maxima: a short dependency chain
+      {  // eight chains of three-input maxima, then their maximum (in log2 units)
+        static_assert(NKEY == 64, "eight chains of eight keys");
         float mp[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = x[i];
-#pragma unroll
-        for (int i = 8; i < NKEY; ++i) mp[i & 7] = fmaxf(mp[i & 7], x[i]);
-        mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int j = 0; j < 8; ++j) {
+          mp[j] = max3f(x[j], x[8 + j], x[16 + j]);
+          mp[j] = max3f(mp[j], x[24 + j], x[32 + j]);
+          mp[j] = max3f(mp[j], x[40 + j], x[48 + j]);
+          mp[j] = fmaxf(mp[j], x[56 + j]);
+        }
+        mt = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * qk_mult;
       }
       float alpha = 1.f;
       bool resc = false;
@@ -432,6 +440,7 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
       lsum *= alpha;
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
       const float2 neg_mu = make_float2(-mu, -mu);
+      const float2 mult2 = make_float2(qk_mult, qk_mult);
       float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t hi[NKEY / 32][16], lo[NKEY / 32][16];
 #pragma unroll
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(CascadeShape<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int j = 16 * c + i;                      // key pair j: keys 2j, 2j + 1
-          const float2 e = __fadd2_rn(make_float2(x[2 * j], x[2 * j + 1]), neg_mu);
+          const float2 e = __ffma2_rn(make_float2(x[2 * j], x[2 * j + 1]), mult2, neg_mu);
           const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
           ls[i & 1] = __fadd2_rn(ls[i & 1], pp);
           hi[c][i] = pack_bf16x2(pp.x, pp.y);

@@ -73,6 +73,24 @@ def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, 
     assert torch.max(torch.abs(out_c - out_p)) < 1e-4
 
 
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 2.5])
+def test_cascade_negative_zero_and_large_scales(scale):
+    # the prefix kernel applies the logit multiplier inside the exponent and
+    # folds a negative scale into Q; a zero scale gives the mean of V
+    B, G, H_kv = 5, 8, 2
+    case = shared_case(B, 128, (1, 300), G, H_kv, 128, 16, seed=733)
+    case["scale"] = scale
+    S.poison_unused(case)
+    snaps = {(b, h): S.snapshot_sequence(case, b, h) for b in range(B) for h in range(H_kv)}
+    out_c, out_p = run_cascade(case)
+    got = out_c.cpu().numpy()
+    assert np.isfinite(got).all()
+    for (b, h), snap in snaps.items():
+        ref = S.oracle_unit(case, b, h, 0, snap)
+        assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+    assert torch.max(torch.abs(out_c - out_p)) < 1e-4
+
+
 @pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs,every", [
     (12, 128, (1, 200), 8, 2, 128, 16, 3),    # one suffix split per sequence
     (9, 64, (1, 700), 4, 2, 64, 16, 3),       # several suffix splits
