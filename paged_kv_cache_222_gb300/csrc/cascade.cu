@@ -1009,8 +1009,11 @@ __global__ void __launch_bounds__(256, 1)
       const int row = w.row0 + r_in;
       const bool row_ok = row < rows;
       const int64_t orow = (static_cast<int64_t>(w.b) * QL + row / G) * H_q + w.h * G + row % G;
-      // tokens this row may attend: [0, lim)
-      const int lim = row_ok ? min(w.t1, w.ctx - QL + row / G + 1) : w.t0;
+      // tokens this row may attend: [0, lim).  A padding row (past the
+      // unit's q_len x G rows) takes no mask: its P feeds only O rows that
+      // are never written, and a mask there would run the masking loop of
+      // its whole warp on every tile.
+      const int lim = row_ok ? min(w.t1, w.ctx - QL + row / G + 1) : w.t1 + NKEY;
       // a warp past the unit's last query row (q_len x G rows fill only part
       // of the 128-row block) keeps the barrier phases and computes nothing:
       // its P rows feed only O rows that are never written
