@@ -1,8 +1,11 @@
 """Benchmark: paged decode attention KV GB/s and sequences/s on one GB300.
 
 One step = one decode step of one attention layer for the whole batch:
-pkv_append of every sequence's new token (K/V scatter) followed by
-pkv_decode_attention (split-KV decode + LSE combine), all through the C ABI.
+pkv_decode_attention_append, all through the C ABI: every sequence's new
+token is written into its slot (K/V scatter, bf16 copy or E4M3 quantisation)
+by the decode launch itself, then the split-KV decode and the LSE combine.
+(With --split-tokens -1, whose balanced mode has no fused append, the step
+is pkv_append followed by pkv_decode_attention_ex.)
 
 Default workload (the largest one-GPU configuration): long-context split-KV
 decode, B=8 sequences of 131,072 tokens, H_q=64, H_kv=8, d_head=128, 32-token
@@ -317,16 +320,28 @@ class DecodeRun:
     def step_index(self, i):
         return i % self.S
 
+    @property
+    def fused(self):
+        """The step appends inside the decode launch (every mode but the
+        balanced one)."""
+        return self.split_tokens >= 0
+
     def step(self, i, q=None, kn=None, vn=None, slots=None, bt=None, lens=None, out=None):
         s = self.step_index(i)
         c = self.case
-        self.pkv.append(self.kn[s] if kn is None else kn, self.vn[s] if vn is None else vn,
-                        self.slots[s] if slots is None else slots, c["k_cache"], c["v_cache"], self.ks, self.vs)
+        kn = self.kn[s] if kn is None else kn
+        vn = self.vn[s] if vn is None else vn
+        extra = {}
+        if self.fused:
+            extra = dict(k_new=kn, v_new=vn)
+        else:
+            self.pkv.append(kn, vn, self.slots[s] if slots is None else slots, c["k_cache"], c["v_cache"],
+                            self.ks, self.vs)
         self.pkv.decode_attention(self.q[s] if q is None else q, c["k_cache"], c["v_cache"],
                                   self.bt if bt is None else bt, self.lens[s] if lens is None else lens,
                                   c["scale"], self.ks, self.vs, max_context_len=self.max_len,
                                   out=self.out if out is None else out, split_tokens=self.split_tokens,
-                                  workspace=self.ws)
+                                  workspace=self.ws, **extra)
 
     def region_bytes(self, k):
         return sum(self.step_bytes[self.step_index(i)] for i in range(k))
@@ -345,6 +360,7 @@ class DecodeRun:
                         else ("%d tokens x %d splits" % (p.split_tokens, p.max_splits)),
                "l2": "inputs larger than L2 (no flush)" if self.step_bytes[0] > L2_BYTES else
                      "L2 flushed between steps (258 MB write outside each step's events)",
+               "append": "fused into the decode launch" if self.fused else "a launch of its own",
                "parallelism": "replicas"}
         if c.get("prefix", 0):
             cfg["shared_prefix_tokens"] = int(c["prefix"])
@@ -433,8 +449,9 @@ def traced_region(run, k, dev):
 
 def e2e_region(run, k, repeats, dist, dev, world):
     """The same K steps end to end through the public API with host buffers:
-    every step copies its inputs (q, the new K/V rows, slots, block tables,
-    lengths) from pinned host memory and reads its output back, on a copy
+    every step copies its inputs (q, the new K/V rows, block tables, lengths;
+    the slots too when the append is a launch of its own) from pinned host
+    memory and reads its output back, on a copy
     stream one step ahead of the compute (two sets of device buffers); the
     timed region spans every copy.  Returns (GB/s of the median repeat,
     h2d bytes per step, d2h bytes per step)."""
@@ -442,8 +459,8 @@ def e2e_region(run, k, repeats, dist, dev, world):
     stream = torch.cuda.current_stream(dev)
     pin = lambda t: t.cpu().pin_memory()
     S = run.S
-    h_in = [[pin(run.q[s]), pin(run.kn[s]), pin(run.vn[s]), pin(run.slots[s]), pin(run.bt), pin(run.lens[s])]
-            for s in range(S)]
+    h_in = [[pin(run.q[s]), pin(run.kn[s]), pin(run.vn[s]), pin(run.bt), pin(run.lens[s])]
+            + ([] if run.fused else [pin(run.slots[s])]) for s in range(S)]
     h_outs = [torch.empty(run.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     d_in = [[torch.empty_like(t, device=dev) for t in h_in[0]] for _ in range(2)]
     d_out = [torch.empty_like(run.out) for _ in range(2)]
@@ -472,7 +489,8 @@ def e2e_region(run, k, repeats, dist, dev, world):
                 with torch.cuda.stream(cstream):
                     h2d_copy(i + 1)
             stream.wait_event(ev_in[i % 2])
-            q, kn, vn, sl, bt, ln = d_in[i % 2]
+            q, kn, vn, bt, ln = d_in[i % 2][:5]
+            sl = None if run.fused else d_in[i % 2][5]
             run.step(i, q=q, kn=kn, vn=vn, slots=sl, bt=bt, lens=ln, out=d_out[i % 2])
             ev_done[i % 2].record(stream)
             with torch.cuda.stream(cstream):

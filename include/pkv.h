@@ -8,6 +8,9 @@
  *   pkv_decode_attention  single-token attention of every sequence over its
  *                         paged K/V (GQA, split-KV flash-decoding + LSE combine).
  *
+ * pkv_decode_attention_append does both in one launch when each sequence
+ * appends one token.
+ *
  * Sources for what is computed (web pages, cited by title and section):
  *   [FN] FactNode, "Sub-Millisecond Token Scheduling: Inside Disaggregated
  *        KV-Cache Paging for Frontier LLMs".
@@ -230,6 +233,47 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
                                    int64_t scale_row_stride,
                                    void* workspace, size_t workspace_bytes,
                                    int32_t split_tokens, pkv_stream_t stream);
+
+/*
+ * pkv_decode_attention_append — one decode step: append each sequence's new
+ * token and attend, in one launch ([SC] "LLM inference: prefill, decode, KV
+ * cache", section 4, step 5: the new token's K/V join the cache, then the
+ * token attends the whole cache).  The result equals pkv_append of the new
+ * rows into the slots of positions context_lens[b] - 1 followed by
+ * pkv_decode_attention_ex, bit for bit in the cache and in `out`.
+ *
+ *   k_cache, v_cache  written: the new rows go into their slots.
+ *   k_new, v_new   [batch, num_kv_heads, head_dim] of type new_dtype
+ *                  (PKV_BF16 or PKV_F32), 16-byte aligned: the new token of
+ *                  sequence b, encoded as pkv_append encodes a row (bf16:
+ *                  bf16 copied, f32 rounded to nearest even; E4M3:
+ *                  RNE-satfinite(x / scale) with the scales below).
+ *   context_lens   as for decode: the new token included; the row of
+ *                  sequence b goes to position context_lens[b] - 1 through
+ *                  its block table.  A sequence with context_lens[b] == 0
+ *                  appends nothing (its output row is zeros); a length that
+ *                  is clamped (see pkv_decode_attention) appends nothing and
+ *                  is recorded.  A table entry outside [0, num_blocks) at the
+ *                  new position records PKV_DEVERR_BLOCK_ID and writes
+ *                  nothing.
+ *   k_scale, v_scale  E4M3: row b, KV head h use [b * scale_row_stride + h]
+ *                  for both the append and the attention.
+ *   split_tokens   0 (automatic) or a multiple of 64; the balanced mode (-1)
+ *                  is PKV_ERR_INVALID_ARG here.
+ * Other arguments and the workspace as pkv_decode_attention_ex.  The new
+ * token's slot is written by the one CTA that attends it, before that CTA
+ * loads its tiles; nothing else reads it during the call.
+ */
+pkv_status pkv_decode_attention_append(const void* q, int32_t batch, int32_t num_q_heads,
+                                       void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                       const void* k_new, const void* v_new, int32_t new_dtype,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t max_context_len,
+                                       float scale, float* out,
+                                       const float* k_scale, const float* v_scale,
+                                       int64_t scale_row_stride,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t split_tokens, pkv_stream_t stream);
 
 /*
  * pkv_decode_attention_noalloc — pkv_decode_attention without any allocation.

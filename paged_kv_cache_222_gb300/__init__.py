@@ -136,7 +136,7 @@ def decode_plan(batch, num_q_heads, k_cache_or_desc, max_context_len, split_toke
 
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=None,
                      v_scale=None, max_context_len=None, out=None, split_tokens=0,
-                     workspace=None, scale_row_stride=None):
+                     workspace=None, scale_row_stride=None, k_new=None, v_new=None):
     """Single-token decode attention over the paged cache.
 
     q [B, H_q, D] bf16; block_tables [B, MB] int32; context_lens [B] int32
@@ -145,6 +145,10 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_s
     block tables' capacity MB * block_size, which plans more splits than a
     tighter bound).  E4M3 caches take k_scale /
     v_scale float32 [B, H_kv] (or [H_kv] for one scale per head).
+
+    With k_new / v_new ([B, H_kv, D], bf16 or float32) the step's new tokens
+    are appended in the same launch (pkv_decode_attention_append): row b goes
+    to position context_lens[b] - 1, encoded as `append` encodes it.
     """
     lib = library()
     _check_pair(k_cache, v_cache)
@@ -181,6 +185,26 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, k_s
     ws_bytes = int(plan.workspace_bytes)
     if ws_bytes > 0 and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if k_new is not None or v_new is not None:
+        if k_new is None or v_new is None or k_new.shape != v_new.shape:
+            raise ValueError("k_new and v_new go together, both [B, H_kv, D]")
+        if tuple(k_new.shape) != (b, desc.num_kv_heads, desc.head_dim):
+            raise ValueError("k_new / v_new must be [B, H_kv, D]")
+        if k_new.dtype == torch.bfloat16:
+            src = PKV_BF16
+        elif k_new.dtype == torch.float32:
+            src = PKV_F32
+        else:
+            raise TypeError(f"k_new dtype {k_new.dtype}: expected bfloat16 or float32")
+        _contig(k_new, k_new.dtype, "k_new", dev)
+        _contig(v_new, k_new.dtype, "v_new", dev)
+        st = lib.pkv_decode_attention_append(
+            _ptr(q), b, hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(k_new), _ptr(v_new), src,
+            _ptr(block_tables), mb, _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+            _ptr(k_scale), _ptr(v_scale), int(stride), _ptr(workspace) if ws_bytes > 0 else ctypes.c_void_p(0),
+            ws_bytes if ws_bytes > 0 else 0, int(split_tokens), _stream(dev))
+        _lib.check(st, "pkv_decode_attention_append")
+        return out
     st = lib.pkv_decode_attention_ex(
         _ptr(q), b, hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(block_tables), mb,
         _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), _ptr(k_scale),

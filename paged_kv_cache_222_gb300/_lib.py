@@ -58,6 +58,9 @@ SIGNATURES = {
                                        _P, _I32, _F, _P, _P, _P, _I64, _P, ctypes.c_size_t, _I32, _P]),
     "pkv_decode_attention_noalloc": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,
                                             _P, _I32, _F, _P, _P, _P, _I64, _P]),
+    "pkv_decode_attention_append": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _P, _I32,
+                                           _P, _I32, _P, _I32, _F, _P, _P, _P, _I64, _P, ctypes.c_size_t,
+                                           _I32, _P]),
     "pkv_cascade_plan": (_I32, [_I32, _I32, ctypes.POINTER(CacheDesc), _I32, _I32, _I32,
                                 ctypes.POINTER(DecodePlan)]),
     "pkv_cascade_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, ctypes.POINTER(CacheDesc), _P, _I32,

@@ -336,6 +336,10 @@ struct DecodeArgs {
   const float* k_scale;
   const float* v_scale;
   int64_t scale_stride;
+  // fused append (pkv_decode_attention_append): one new token per sequence
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  int32_t new_dtype = -1;
 };
 
 pkv_status check_decode(const DecodeArgs& a) {
@@ -369,6 +373,13 @@ pkv_status check_decode(const DecodeArgs& a) {
     return fail(PKV_ERR_INVALID_ARG, "block_tables / context_lens must be 4-byte aligned");
   if (fp8 && (!aligned(a.k_scale, 4) || !aligned(a.v_scale, 4)))
     return fail(PKV_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  if (a.new_dtype != -1) {
+    if (a.new_dtype != PKV_BF16 && a.new_dtype != PKV_F32)
+      return fail(PKV_ERR_INVALID_ARG, "new_dtype %d (want PKV_BF16 or PKV_F32)", a.new_dtype);
+    if (a.k_new == nullptr || a.v_new == nullptr) return fail(PKV_ERR_INVALID_ARG, "NULL k_new / v_new");
+    if (!aligned(a.k_new, 16) || !aligned(a.v_new, 16))
+      return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  }
   return PKV_OK;
 }
 
@@ -381,6 +392,8 @@ pkv_status run_decode(const DecodeArgs& a, void* ws, size_t ws_bytes, int32_t sp
   pkv_decode_plan_t pl;
   s = plan(a.batch, a.num_q_heads, a.cache, a.max_ctx, split_tokens, st->sms, &pl);
   if (s != PKV_OK) return s;
+  if (a.new_dtype != -1 && pl.mode != pkv::kModeFixedSplit)
+    return fail(PKV_ERR_UNSUPPORTED, "the fused append takes fixed splits (split_tokens >= 0)");
   if (!own_workspace && pl.workspace_bytes > 0) {
     if (ws == nullptr || ws_bytes < static_cast<size_t>(pl.workspace_bytes))
       return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes, need %lld", ws_bytes,
@@ -450,6 +463,13 @@ pkv_status run_decode(const DecodeArgs& a, void* ws, size_t ws_bytes, int32_t sp
   p.workers = pl.workers;
   p.extra_slot = -1;
   p.slots_per_row = pl.max_splits;
+  if (a.new_dtype != -1) {
+    p.new_src = (a.new_dtype == PKV_BF16 ? pkv::kEncBF16 : pkv::kEncF32) + 1;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.k_cache = const_cast<void*>(a.k_cache);
+    p.v_cache = const_cast<void*>(a.v_cache);
+  }
   p.err = st->err;
 
   e = traced(pkv::kKindDecodeSplit, stream,
@@ -701,6 +721,28 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
   if (s != PKV_OK) return s;
   if (split_tokens < -1 || (split_tokens > 0 && split_tokens % 64 != 0))
     return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (-1, 0 or a multiple of 64)", split_tokens);
+  if (batch == 0) return PKV_OK;
+  return run_decode(a, workspace, workspace_bytes, split_tokens,
+                    reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+pkv_status pkv_decode_attention_append(const void* q, int32_t batch, int32_t num_q_heads, void* k_cache,
+                                       void* v_cache, const pkv_cache_desc* cache, const void* k_new,
+                                       const void* v_new, int32_t new_dtype, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float scale, float* out,
+                                       const float* k_scale, const float* v_scale,
+                                       int64_t scale_row_stride, void* workspace,
+                                       size_t workspace_bytes, int32_t split_tokens,
+                                       pkv_stream_t stream) {
+  DecodeArgs a = {q, batch, num_q_heads, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                  context_lens, max_context_len, scale, out, k_scale, v_scale, scale_row_stride,
+                  k_new, v_new, new_dtype};
+  if (new_dtype == -1) return fail(PKV_ERR_INVALID_ARG, "new_dtype -1");
+  pkv_status s = check_decode(a);
+  if (s != PKV_OK) return s;
+  if (split_tokens < 0 || split_tokens % 64 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "split_tokens %d (0 or a multiple of 64)", split_tokens);
   if (batch == 0) return PKV_OK;
   return run_decode(a, workspace, workspace_bytes, split_tokens,
                     reinterpret_cast<cudaStream_t>(stream), false);

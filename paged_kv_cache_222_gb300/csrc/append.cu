@@ -23,56 +23,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kBF16 = 0, kF32 = 1, kE4M3 = 2;
-
-// Eight source elements as floats (bf16 widening is exact).
-template <int SRC>
-__device__ __forceinline__ void load8(const void* base, int64_t elem, float (&x)[8], uint4& raw) {
-  if constexpr (SRC == kBF16) {
-    raw = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = bf16lo_to_f32(w[i]);
-      x[2 * i + 1] = bf16hi_to_f32(w[i]);
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
-    const float4 a = p[0], b = p[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  }
-}
-
-template <int SRC, int DST>
-__device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&x)[8], const uint4& raw,
-                                       float scale) {
-  if constexpr (DST == kBF16) {
-    uint4 o;
-    if constexpr (SRC == kBF16) {
-      o = raw;  // bit copy
-    } else {
-      o.x = pack_bf16x2(x[0], x[1]);
-      o.y = pack_bf16x2(x[2], x[3]);
-      o.z = pack_bf16x2(x[4], x[5]);
-      o.w = pack_bf16x2(x[6], x[7]);
-    }
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(cache) + elem) = o;
-  } else {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      // IEEE binary32 quotient, then one RNE-satfinite rounding to E4M3
-      const float lo = __fdiv_rn(x[2 * i], scale);
-      const float hi = __fdiv_rn(x[2 * i + 1], scale);
-      w[i] = f32x2_to_e4m3x2(lo, hi);
-    }
-    uint2 o;
-    o.x = w[0] | (w[1] << 16);
-    o.y = w[2] | (w[3] << 16);
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) = o;
-  }
-}
+constexpr int kBF16 = kEncBF16, kF32 = kEncF32, kE4M3 = kEncE4M3;
 
 template <int SRC, int DST>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
@@ -109,10 +60,10 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     }
     float x[8];
     uint4 raw;
-    load8<SRC>(p.k_new, src_elem, x, raw);
-    store8<SRC, DST>(p.k_cache, dst_elem, x, raw, ks);
-    load8<SRC>(p.v_new, src_elem, x, raw);
-    store8<SRC, DST>(p.v_cache, dst_elem, x, raw, vs);
+    enc_load8<SRC>(p.k_new, src_elem, x, raw);
+    enc_store8<SRC, DST>(p.k_cache, dst_elem, x, raw, ks);
+    enc_load8<SRC>(p.v_new, src_elem, x, raw);
+    enc_store8<SRC, DST>(p.v_cache, dst_elem, x, raw, vs);
   }
 }
 

@@ -385,6 +385,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
   const int n_tiles = (t_end - t_begin + kTileTokens - 1) / kTileTokens;
   const int nsplit = (ctx - p.token_offset + p.split_tokens - 1) / p.split_tokens;
 
+  // Fused append: the CTA that attends the sequence's newest token (position
+  // ctx - 1, in its last split) writes that token's K / V rows of head h into
+  // their slot, encoded as the append kernel does, so the step needs no
+  // separate append launch.  No other CTA reads the slot.  The warp whose
+  // tile holds the token writes it (after its first loads are in flight,
+  // unless that tile is one of them) and orders the writes before its own
+  // load of the tile with a proxy fence: no other warp waits.
+  const bool fuse_new = p.new_src != 0 && t_end == ctx && ctx == ctx_raw;
+  const int w_new = (n_tiles - 1) % NW, k_tok = (n_tiles - 1) / NW;  // owner warp, its tile index
+  auto write_new = [&]() {
+    constexpr int PER_ROW = D / 8;                  // lanes per row, eight elements each
+    if (lane < 2 * PER_ROW) {
+      const int pos = ctx - 1;
+      const int phys = p.block_tables[static_cast<int64_t>(b) * p.max_blocks + pos / p.block_size];
+      if (phys >= 0 && phys < p.num_blocks) {
+        const bool is_v = lane >= PER_ROW;
+        const int part = lane - (is_v ? PER_ROW : 0);
+        const int64_t src = (static_cast<int64_t>(b) * p.num_kv_heads + h) * D + part * 8;
+        const int64_t dst =
+            ((static_cast<int64_t>(phys) * p.num_kv_heads + h) * p.block_size + pos % p.block_size) * D + part * 8;
+        float sc = 1.f;
+        if constexpr (FP8) sc = (is_v ? p.v_scale : p.k_scale)[static_cast<int64_t>(b) * p.scale_stride + h];
+        constexpr int DST = FP8 ? kEncE4M3 : kEncBF16;
+        float x[8];
+        uint4 raw;
+        if (p.new_src == kEncBF16 + 1) {
+          enc_load8<kEncBF16>(is_v ? p.v_new : p.k_new, src, x, raw);
+          enc_store8<kEncBF16, DST>(is_v ? p.v_cache : p.k_cache, dst, x, raw, sc);
+        } else {
+          enc_load8<kEncF32>(is_v ? p.v_new : p.k_new, src, x, raw);
+          enc_store8<kEncF32, DST>(is_v ? p.v_cache : p.k_cache, dst, x, raw, sc);
+        }
+      } else if (lane == 0) {
+        record_error(p.err, kDevErrBlockId);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncwarp();
+  };
+
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BARS);
   float* s_ml = reinterpret_cast<float*>(smem + S::ML);
 
@@ -432,12 +472,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
     issue_tile<L>(wstage0 + s * L::STAGEB, wbar0 + 8 * s, &tmap_k, &tmap_v, t % p.block_size, h, phys);
   };
 
+  const bool writer = fuse_new && warp == w_new;
+  if (writer && k_tok < NS) write_new();   // the token's tile is one of the first loads
   int phys_reg = load_phys(0);
   const int npro = nk < NS ? nk : NS;
   for (int k = 0; k < npro; ++k) {
     const int ph = __shfl_sync(kFull, phys_reg, k);
     if (lane == 0) issue(k, ph);
   }
+  if (writer && k_tok >= NS) write_new();  // its load comes later in the loop below
 
   float m_run[NT][2], l_run[NT][2], o[KS][NT][4];
   reset_state<D, NT>(m_run, l_run, o);

@@ -211,6 +211,63 @@ __device__ __forceinline__ float f16hi_to_f32(uint32_t x) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
 }
 
+// ---------------------------------------------------------------- KV rows
+// Encoding of new K / V rows into the cache, shared by the append kernel and
+// the decode kernel's fused append: sources bf16 or f32, caches bf16 (bf16
+// sources copied bit for bit, f32 sources rounded to nearest even) or E4M3
+// (RNE-satfinite of x / scale, x / scale an IEEE binary32 quotient).  The
+// element types are kEncBF16 / kEncF32 / kEncE4M3 (pkv_internal.h).
+
+// Eight source elements as floats (bf16 widening is exact); `raw` keeps the
+// bf16 bits for the bit copy.
+template <int SRC>
+__device__ __forceinline__ void enc_load8(const void* base, int64_t elem, float (&x)[8], uint4& raw) {
+  if constexpr (SRC == kEncBF16) {
+    raw = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16lo_to_f32(w[i]);
+      x[2 * i + 1] = bf16hi_to_f32(w[i]);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+    const float4 a = p[0], b = p[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+// Eight elements into the cache at element `elem` (DST kEncBF16 or kEncE4M3).
+template <int SRC, int DST>
+__device__ __forceinline__ void enc_store8(void* cache, int64_t elem, const float (&x)[8], const uint4& raw,
+                                           float scale) {
+  if constexpr (DST == kEncBF16) {
+    uint4 o;
+    if constexpr (SRC == kEncBF16) {
+      o = raw;  // bit copy
+    } else {
+      o.x = pack_bf16x2(x[0], x[1]);
+      o.y = pack_bf16x2(x[2], x[3]);
+      o.z = pack_bf16x2(x[4], x[5]);
+      o.w = pack_bf16x2(x[6], x[7]);
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(cache) + elem) = o;
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __fdiv_rn(x[2 * i], scale);
+      const float hi = __fdiv_rn(x[2 * i + 1], scale);
+      w[i] = f32x2_to_e4m3x2(lo, hi);
+    }
+    uint2 o;
+    o.x = w[0] | (w[1] << 16);
+    o.y = w[2] | (w[3] << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) = o;
+  }
+}
+
 // 2^x on the special-function unit.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -71,6 +71,10 @@ struct SlotParams {
   int* err;
 };
 
+// Element types of K / V rows being encoded into the cache: the sources of
+// an append (bf16, f32) and the cache's own (bf16, E4M3).
+constexpr int kEncBF16 = 0, kEncF32 = 1, kEncE4M3 = 2;
+
 struct DecodeParams {
   const void* q;              // bf16 [B, H_q, D]
   const int32_t* block_tables;  // [B, MB]
@@ -110,6 +114,14 @@ struct DecodeParams {
   int32_t prefix_split_tokens;   // prefix tokens per prefix CTA (multiple of 64)
   // multi-token queries: q_len new tokens per sequence (1 for decode)
   int32_t q_len;
+  // fixed split, fused append: each sequence's newest token (position
+  // context_lens[b] - 1) is written from k_new / v_new [B, H_kv, D] into its
+  // slot by the CTA that attends it, before that CTA's first load
+  int32_t new_src;            // 0: no append; else kEncBF16 + 1 or kEncF32 + 1
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
   int* err;
 };
 

@@ -109,6 +109,37 @@ def test_decode_with_empty_batch_is_a_noop(lib):
     assert _decode(lib, _desc(), batch=0, q=NULL, out=NULL) == L.PKV_OK
 
 
+def _decode_append(lib, desc, **kw):
+    a = dict(q=FAKE, batch=4, hq=64, kc=FAKE, vc=FAKE, kn=FAKE, vn=FAKE, src=L.PKV_BF16, bt=FAKE, mb=8,
+             cl=FAKE, max_ctx=100, scale=0.125, out=FAKE, ks=NULL, vs=NULL, stride=0, ws=FAKE,
+             ws_bytes=1 << 20, split=0)
+    a.update(kw)
+    return lib.pkv_decode_attention_append(a["q"], a["batch"], a["hq"], a["kc"], a["vc"], ctypes.byref(desc),
+                                           a["kn"], a["vn"], a["src"], a["bt"], a["mb"], a["cl"],
+                                           a["max_ctx"], a["scale"], a["out"], a["ks"], a["vs"], a["stride"],
+                                           a["ws"], a["ws_bytes"], a["split"], NULL)
+
+
+@pytest.mark.parametrize("kw,desc_kw,code", [
+    (dict(src=L.PKV_E4M3), {}, L.PKV_ERR_INVALID_ARG),         # sources are bf16 or f32
+    (dict(src=-1), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(kn=NULL), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(vn=ctypes.c_void_p(0x10008)), {}, L.PKV_ERR_INVALID_ARG),   # misaligned
+    (dict(split=-1), {}, L.PKV_ERR_INVALID_ARG),              # the balanced mode has no fused append
+    (dict(split=100), {}, L.PKV_ERR_INVALID_ARG),
+    (dict(hq=60), {}, L.PKV_ERR_INVALID_ARG),                 # the decode checks apply too
+    (dict(), dict(dtype=L.PKV_E4M3), L.PKV_ERR_INVALID_ARG),    # E4M3 without scales
+])
+def test_decode_append_rejects_bad_arguments_on_host(lib, kw, desc_kw, code):
+    st = _decode_append(lib, _desc(**desc_kw), **kw)
+    assert st == code, lib.pkv_last_error()
+    assert lib.pkv_last_error()
+
+
+def test_decode_append_with_empty_batch_is_a_noop(lib):
+    assert _decode_append(lib, _desc(), batch=0, q=NULL, out=NULL) == L.PKV_OK
+
+
 def _append(lib, desc, **kw):
     a = dict(k=FAKE, v=FAKE, src=L.PKV_BF16, n=4, slots=FAKE, kc=FAKE, vc=FAKE, ks=NULL, vs=NULL,
              stride=0)
