@@ -261,8 +261,8 @@ pkv_status pkv_decode_attention_ex(const void* q, int32_t batch, int32_t num_q_h
  *   split_tokens   0 (automatic) or a multiple of 64; the balanced mode (-1)
  *                  is PKV_ERR_INVALID_ARG here.
  * Other arguments and the workspace as pkv_decode_attention_ex.  The new
- * token's slot is written by the one CTA that attends it, before that CTA
- * loads its tiles; nothing else reads it during the call.
+ * token's slot is written by the warp whose tile holds it, before that warp
+ * loads the tile; nothing else reads it during the call.
  */
 pkv_status pkv_decode_attention_append(const void* q, int32_t batch, int32_t num_q_heads,
                                        void* k_cache, void* v_cache, const pkv_cache_desc* cache,
