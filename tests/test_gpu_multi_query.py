@@ -78,6 +78,8 @@ def _oracle(case):
     (12, 16, 1, 128, 16),   # 192 rows: a partly filled second 128-row group
     (10, 32, 2, 64, 32),    # 160 rows, D = 64
     (16, 16, 1, 64, 16),    # 256 rows: two row blocks per head
+    (14, 8, 1, 128, 16),    # 112 rows: every warp has rows, the last one only half (no idle-warp path)
+    (15, 16, 1, 64, 32),    # 240 rows: a second row block of 112 rows
 ])
 @pytest.mark.parametrize("split_tokens", [0, 64, 192])
 def test_multi_query_matches_oracle(q_len, H_q, H_kv, D, bs, split_tokens):
