@@ -469,7 +469,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
   auto issue = [&](int k, int phys) {
     const int s = k % NS;
     const int t = t_begin + kTileTokens * (warp + k * NW);
-    issue_tile<L>(wstage0 + s * L::STAGEB, wbar0 + 8 * s, &tmap_k, &tmap_v, t % p.block_size, h, phys);
+    // token within its block: the block size is 16 or 32 (a power of two), so a
+    // mask instead of a run-time remainder (2 % on the issue-heavy E4M3 path)
+    issue_tile<L>(wstage0 + s * L::STAGEB, wbar0 + 8 * s, &tmap_k, &tmap_v, t & (p.block_size - 1), h, phys);
   };
 
   const bool writer = fuse_new && warp == w_new;

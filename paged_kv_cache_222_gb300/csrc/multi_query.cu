@@ -136,10 +136,12 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
       const int v = lane / L::NBOX;
       const int bx = lane % L::NBOX;
       const int t = t_begin + k * kMultiQueryTile + warp * kTileTokens;
-      const int bi = (t - t_begin) / p.block_size;
+      // block of the split and token within it: the block size is 16 or 32,
+      // so a shift and a mask instead of a run-time division per box
+      const int bi = (t - t_begin) >> (p.block_size == 16 ? 4 : 5);
       const int phys = (t < t_stop && bi < kMultiQueryMaxSplitBlocks) ? s_blk[bi] : -1;
       tma_load_4d(dst + v * L::TILEB + bx * L::BOX_BYTES, v ? &tmap_v : &tmap_k, bar, bx * L::BOX_ELEMS,
-                  t % p.block_size, h, phys);
+                  t & (p.block_size - 1), h, phys);
     }
   };
   int issued = 0;
