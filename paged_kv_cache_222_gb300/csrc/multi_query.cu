@@ -226,11 +226,13 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
       m_b = mn_b;
       float sum_a = 0.f, sum_b = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 2 * NSW; ++nt) {
-        sc[nt][0] = fast_exp2(sc[nt][0] - mu_a);
-        sc[nt][1] = fast_exp2(sc[nt][1] - mu_a);
-        sc[nt][2] = fast_exp2(sc[nt][2] - mu_b);
-        sc[nt][3] = fast_exp2(sc[nt][3] - mu_b);
+      for (int nt = 0; nt < 2 * NSW; ++nt) {  // packed f32x2 subtractions and multiplies below
+        const float2 ea = __fadd2_rn(make_float2(sc[nt][0], sc[nt][1]), make_float2(-mu_a, -mu_a));
+        const float2 eb = __fadd2_rn(make_float2(sc[nt][2], sc[nt][3]), make_float2(-mu_b, -mu_b));
+        sc[nt][0] = fast_exp2(ea.x);
+        sc[nt][1] = fast_exp2(ea.y);
+        sc[nt][2] = fast_exp2(eb.x);
+        sc[nt][3] = fast_exp2(eb.y);
         sum_a += sc[nt][0] + sc[nt][1];
         sum_b += sc[nt][2] + sc[nt][3];
       }
@@ -238,10 +240,12 @@ __global__ void __launch_bounds__(128, MqShape<TL>::MINB)
       l_b = l_b * al_b + sum_b;
 #pragma unroll
       for (int nt = 0; nt < D / 8; ++nt) {
-        o[nt][0] *= al_a;
-        o[nt][1] *= al_a;
-        o[nt][2] *= al_b;
-        o[nt][3] *= al_b;
+        const float2 u = __fmul2_rn(make_float2(o[nt][0], o[nt][1]), make_float2(al_a, al_a));
+        const float2 w = __fmul2_rn(make_float2(o[nt][2], o[nt][3]), make_float2(al_b, al_b));
+        o[nt][0] = u.x;
+        o[nt][1] = u.y;
+        o[nt][2] = w.x;
+        o[nt][3] = w.y;
       }
       // ---- O += P V, one 16-token k-step per sub-tile
 #pragma unroll
