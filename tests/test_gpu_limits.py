@@ -112,3 +112,33 @@ def test_multi_query_at_the_largest_batch(q_len, H_q, H_kv, D, bs):
                                    case["scale"])
     got = outs[0].cpu().numpy()[sel]
     assert np.max(np.abs(got - ref)) <= 2e-3
+
+
+def test_decode_over_a_million_tokens():
+    """One sequence of 2^20 + 1 tokens after the append, beside a short one,
+    8 KV heads: the pool's block ids pass 65,536 and cache byte offsets pass
+    2^31 (32 KB per block).  Append + decode and the fused one-launch step
+    agree bit for bit; units of the last head (the largest offsets), the
+    first head and the short sequence match the oracle."""
+    spec = dict(B=2, H_q=64, H_kv=8, D=128, bs=16, kv="bf16", free_frac=0.25, steps=1, seed=67,
+                q_mult=1.0, ctx=(1 << 20, 300))
+    case = W.make_case(spec, device=DEV)
+    kc = case["k_cache"]
+    assert kc.shape[0] * kc[0].numel() * kc.element_size() > 1 << 31
+    S.poison_unused(case)
+    units = [(0, 0), (0, 7), (1, 3)]
+    snaps = {u: S.snapshot_sequence(case, *u) for u in units}
+    out = S.run_step(case, 0)
+    dev = kc.device
+    lens = (case["ctx"] + 1).to(torch.int32).to(dev)
+    assert int(lens[0]) == (1 << 20) + 1 and int(case["block_tables"].max()) >= 65536
+    fused = pkv.decode_attention(case["q"][0].contiguous(), kc, case["v_cache"], case["block_tables"].to(dev),
+                                 lens, case["scale"], max_context_len=int(lens.max()),
+                                 k_new=case["k_new"][0].contiguous(), v_new=case["v_new"][0].contiguous())
+    assert pkv.device_error(DEV) == 0
+    assert torch.equal(out, fused)
+    got = out.cpu().numpy()
+    G = 8
+    for b, h in units:
+        ref = S.oracle_unit(case, b, h, 0, snaps[(b, h)])
+        assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3, (b, h)
