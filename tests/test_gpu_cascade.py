@@ -73,6 +73,28 @@ def test_cascade_matches_oracle_and_plain_decode(B, prefix, suffix, G, H_kv, D, 
     assert torch.max(torch.abs(out_c - out_p)) < 1e-4
 
 
+@pytest.mark.parametrize("B,prefix,suffix,G,H_kv,D,bs,ranges,range_tokens", [
+    (128, 16384, (1, 300), 8, 8, 128, 16, 4, 4096),   # ranges at their 256-block cap; 5 slots per row
+    (4, 16384, (1, 500), 8, 2, 128, 16, 64, 256),     # 64 ranges: 66 slots per row, the generic combine
+    (3, 40960, (1, 64), 4, 1, 64, 32, 64, 640),       # D = 64, 32-token blocks, 65 slots per row
+])
+def test_cascade_long_prefixes(B, prefix, suffix, G, H_kv, D, bs, ranges, range_tokens):
+    case = shared_case(B, prefix, suffix, G, H_kv, D, bs, seed=1500 + B)
+    S.poison_unused(case)
+    mx = int(case["ctx"].max()) + 1
+    plan = pkv.cascade_plan(B, G * H_kv, case["k_cache"], prefix, mx)
+    assert plan.workers == ranges and plan.prefix_split_tokens == range_tokens
+    units = [(b, h) for b in sorted({0, B // 2, B - 1}) for h in sorted({0, H_kv - 1})]
+    snaps = {u: S.snapshot_sequence(case, *u) for u in units}
+    out_c, out_p = run_cascade(case)
+    assert pkv.device_error(DEV) == 0
+    got = out_c.cpu().numpy()
+    for (b, h), snap in snaps.items():
+        ref = S.oracle_unit(case, b, h, 0, snap)
+        assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3
+    assert torch.max(torch.abs(out_c - out_p)) < 1e-4   # every unit, against the plain decode
+
+
 @pytest.mark.parametrize("scale", [-0.3, 0.0, 2.5])
 def test_cascade_negative_zero_and_large_scales(scale):
     # the prefix kernel applies the logit multiplier inside the exponent and
