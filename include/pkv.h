@@ -148,6 +148,8 @@ pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32
  * list; softmax(q K^T * scale) V as in [UI] "Mathematical Formulation of Block
  * Salience", definition of A).
  *
+ *   batch          0..65535 sequences (the split kernel puts the sequence on
+ *                  the grid's z axis); more is rejected with PKV_ERR_INVALID_ARG.
  *   q              bf16 [batch, num_q_heads, head_dim], 16-byte aligned.
  *                  num_q_heads = G * num_kv_heads with 1 <= G <= 16; query
  *                  head hq reads KV head hq / G ([SC] "Attention Architectures:
@@ -321,6 +323,8 @@ pkv_status pkv_decode_attention_noalloc(const void* q, int32_t batch, int32_t nu
  * of once per sequence, and merged with each private suffix by the same
  * log-sum-exp combine.
  *
+ *   batch          0..65535 sequences (0: nothing to do; pkv_cascade_plan
+ *                  takes 1..65535); more is rejected with PKV_ERR_INVALID_ARG.
  *   prefix_blocks  int32 [prefix_len / block_size]: the prefix's physical
  *                  blocks.  For every sequence b the first prefix_len /
  *                  block_size entries of block_tables[b] must equal them
@@ -367,6 +371,8 @@ pkv_status pkv_cascade_decode_attention(const void* q, int32_t batch, int32_t nu
  * parallel pass ([SC] "7. Practical applications", item 3, Speculative
  * Decoding).
  *
+ *   batch          0..65535 sequences; more is rejected with
+ *                  PKV_ERR_INVALID_ARG.
  *   q              bf16 [batch, q_len, num_q_heads, head_dim], 16-byte aligned;
  *                  1 <= q_len <= 16.
  *   context_lens   int32 [batch]: tokens of sequence b, its q_len new tokens
