@@ -45,7 +45,13 @@ def test_decode_at_the_largest_batch():
     out64 = S.run_step(case, 0, split_tokens=64)   # up to four 64-token splits per sequence
     plan = pkv.decode_plan(B_MAX, 4, case["k_cache"], int(case["ctx"].max()) + 1, split_tokens=64)
     assert plan.max_splits >= 3
+    dev = case["k_cache"].device
+    lens = (case["ctx"] + 1).to(torch.int32).to(dev)
+    fused = pkv.decode_attention(case["q"][0].contiguous(), case["k_cache"], case["v_cache"],
+                                 case["block_tables"].to(dev), lens, case["scale"], max_context_len=int(lens.max()),
+                                 k_new=case["k_new"][0].contiguous(), v_new=case["v_new"][0].contiguous())
     assert pkv.device_error(DEV) == 0
+    assert torch.equal(out0, fused)                 # the one-launch step, same plan
     assert bool(torch.isfinite(out0).all()) and bool(torch.isfinite(out64).all())
     assert float((out0 - out64).abs().max()) < 1e-5
     got = out0.cpu().numpy()
