@@ -148,3 +148,33 @@ def test_decode_over_a_million_tokens():
     for b, h in units:
         ref = S.oracle_unit(case, b, h, 0, snaps[(b, h)])
         assert np.max(np.abs(got[b, h * G:(h + 1) * G] - ref)) <= 2e-3, (b, h)
+
+
+def test_fp8_decode_at_the_largest_batch():
+    """E4M3 caches at 65,535 sequences: the fill (every position through
+    pkv_append with per-(sequence, head) scales, row b * stride + h up to
+    sequence 65,534), then decode with one split and with 64-token splits.
+    P enters P.V as one f16 term, so splits move results by up to the FP8
+    tolerance; both are checked against the oracle on sampled units, every
+    row for finiteness, and the fused step against the two-call step."""
+    spec = dict(B=B_MAX, H_q=4, H_kv=1, D=64, bs=16, kv="e4m3", free_frac=0.25, steps=1, seed=68,
+                q_mult=1.0, ctx_range=(0, 200))
+    case = W.make_case(spec, device=DEV)
+    case["k_cache"].fill_(S.E4M3_NAN)
+    case["v_cache"].fill_(S.E4M3_NAN)
+    S.fill_fp8_cache(case)
+    outs = [S.run_step(case, 0, split_tokens=st) for st in (0, 64)]
+    dev = case["k_cache"].device
+    lens = (case["ctx"] + 1).to(torch.int32).to(dev)
+    fused = pkv.decode_attention(case["q"][0].contiguous(), case["k_cache"], case["v_cache"],
+                                 case["block_tables"].to(dev), lens, case["scale"], case["k_scale"],
+                                 case["v_scale"], max_context_len=int(lens.max()),
+                                 k_new=case["k_new"][0].contiguous(), v_new=case["v_new"][0].contiguous())
+    assert pkv.device_error(DEV) == 0
+    assert torch.equal(outs[0], fused)
+    for o in outs:
+        assert bool(torch.isfinite(o).all())
+        got = o.cpu().numpy()
+        for b in SAMPLED:
+            ref = S.oracle_unit(case, b, 0, 0)
+            assert np.max(np.abs(got[b] - ref)) <= S.tolerance(case), b
